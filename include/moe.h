@@ -1,0 +1,217 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) MXFP8-activation x MXFP4-weight
+ * top-16 routed mixture-of-experts decode layer.
+ *
+ * What one call computes (pages "vllm.models.kimi_k3.nvidia.specialized_decode.
+ * cutedsl.moe.experts" [experts] and "...cutedsl.moe.experts_runtime"
+ * [runtime]): every token row x[t, :] (BF16) is quantized to MXFP8 (e4m3
+ * codes, one E8M0 scale per 32 elements); for each of the token's 16 routed
+ * experts e = ids[t, s], FC1 multiplies it by e's MXFP4 gate+up rows with FP32
+ * accumulation, the hidden row SiLU(gate) * up is requantized to MXFP8, FC2
+ * multiplies it by e's MXFP4 down rows, and the result is written as one BF16
+ * row out[t, s, :] in the caller's top-16 order ([runtime] module docstring,
+ * PersistentExperts.run; [experts] ExpertsKernel.store_hidden, ExpertsKernel.fc2).
+ *
+ * Conventions for every entry point:
+ *  - Return value: 0 (MOE_OK) or one of enum moe_status. No entry point
+ *    aborts the process; errors found before a launch leave nothing queued.
+ *  - Device pointers are raw CUDA device addresses of the current device;
+ *    host pointers are ordinary (preferably pinned) host memory. Stream
+ *    arguments are cudaStream_t values passed as void*; NULL is the legacy
+ *    default stream.
+ *  - Ownership: the caller owns x, ids and out (and the weight arrays passed
+ *    to moe_prepare, which may be freed once it returns). The handle owns
+ *    every other buffer (repacked weights, activation plan, unit table,
+ *    workspace) until moe_destroy.
+ *  - A handle is bound to the device that was current at moe_prepare and
+ *    serves one stream at a time: calls that overlap on the GPU race on its
+ *    workspace.
+ */
+#ifndef MXFP4_WEIGHT_MXFP8_GB300_MOE_H
+#define MXFP4_WEIGHT_MXFP8_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_TOPK 16      /* routed experts per token */
+#define MOE_UNIT_ROWS 8  /* pair rows per unit: the MMA's N */
+#define MOE_MAX_BATCH 256
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_HIDDEN 16384
+#define MOE_MAX_INTER 512
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,            /* null/misaligned pointer, size out of range */
+  MOE_ERR_UNSUPPORTED = 2,    /* no sm_103/sm_100-family device, grid not co-resident */
+  MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
+  MOE_ERR_DEVICE_IDS = 5,     /* an id out of [0, E) or repeated within a token */
+  MOE_ERR_STATE = 6           /* call order: e.g. moe_copy_units before any grouping */
+};
+
+typedef struct moe_ctx* moe_handle;
+
+/* Geometry of a prepared handle (moe_info). */
+typedef struct moe_info_t {
+  int experts, hidden, inter;
+  int hidden_floor_rule;      /* 1: hidden requant uses floor(log2 amax) - 8 */
+  int grid;                   /* persistent experts CTAs (one per SM) */
+  int ring_stages;            /* weight-ring depth */
+  int smem_bytes;             /* dynamic shared memory of the experts kernel */
+  int stages_per_expert;      /* 16 KB weight + 1 KB scale stages per expert */
+  int unit_capacity;          /* unit-table rows reserved (MOE_MAX_BATCH) */
+  int hidden_image_bytes;     /* per-unit hidden image in the workspace */
+  size_t weight_bytes;        /* repacked weight stages held by the handle */
+  size_t workspace_bytes;     /* plan + unit table + workspace */
+} moe_info_t;
+
+/*
+ * moe_prepare - take a copy of one layer's expert weights.
+ * Source: [runtime] PersistentExperts.__init__ (weights w13, s13, w2, s2;
+ * tp = 8 exactly when w13 has 768 rows) and scratch (model-owned workspace).
+ *
+ *   w13 uint8 [E, 2I, H/2]  e2m1 pairs, element 2i in the low nibble of byte i;
+ *                           rows 0..I-1 are the gate rows, I..2I-1 the up rows
+ *   s13 uint8 [E, 2I, H/32] E8M0 scale of each 32 consecutive k
+ *   w2  uint8 [E, H, I/2]   e2m1 pairs (down projection)
+ *   s2  uint8 [E, H, I/32]  E8M0
+ * Each may be device or host memory (detected). Sizes: 1 <= E <= 1024,
+ * H % 256 == 0 and H <= 16384, I % 32 == 0 and 32 <= I <= 512.
+ * The hidden requant uses the floor rule iff 2I == 768, else the ceil rule.
+ * Synchronous: repacks the weights into library-owned device memory (one
+ * contiguous 17,408-byte block per 128-K stage of two 128-row tiles, scales
+ * pre-tiled for the tensor core), allocates the plan, unit table and
+ * workspace for batches up to MOE_MAX_BATCH, builds the TMA descriptor and
+ * checks that the persistent grid fits one CTA per SM.
+ * Errors: MOE_ERR_ARG (null out/pointers, sizes), MOE_ERR_UNSUPPORTED (not an
+ * sm_100-family GPU with >= 227 KB shared memory per block), MOE_ERR_CUDA.
+ * On error *out is NULL and nothing is leaked.
+ */
+int moe_prepare(moe_handle* out, const void* w13, const void* s13, const void* w2, const void* s2,
+                int experts, int hidden, int inter);
+
+/*
+ * moe_quantize - MXFP8 activation plan of x.
+ * Source: [experts] mx_block, plan_chunk and ExpertsPlanKernel (one E8M0
+ * scale per 32 BF16 values; codes e4m3 of x * 2^-E). The scale rule is the
+ * smallest E with max|x| <= 448 * 2^E (E = -127 for an all-zero block), so
+ * no code saturates; codes round to nearest even, keeping the sign.
+ *   x_bf16  device, BF16 [batch, H] row-major, 16-byte aligned
+ *   1 <= batch <= MOE_MAX_BATCH
+ * Asynchronous on `stream`; writes the handle's plan (read back with
+ * moe_copy_plan). Errors: MOE_ERR_ARG, MOE_ERR_CUDA (launch).
+ */
+int moe_quantize(moe_handle h, const void* x_bf16, int batch, void* stream);
+
+/*
+ * moe_group - unit table of the routing ids.
+ * Source: [experts] ExpertsKernel.group and ExpertsGroupKernel: experts in
+ * ascending order; expert e's pairs p = token * 16 + slot, in token order,
+ * fill ceil(n_e / 8) units of 8 rows, the last padded with -1.
+ *   topk_ids  device, int32 [batch, 16]; ids must lie in [0, E) and be
+ *             distinct within a token: a violating pair is dropped (its
+ *             output row is not written) and the call reports
+ *             MOE_ERR_DEVICE_IDS through moe_sync_status.
+ * Asynchronous; also clears the per-call workspace counters. Read back with
+ * moe_copy_units. Errors: MOE_ERR_ARG, MOE_ERR_CUDA.
+ */
+int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream);
+
+/*
+ * moe_run - the whole layer: quantize + group + experts + output epilogue.
+ * Source: [runtime] PersistentExperts.run; [experts] ExpertsKernel (FC1 and
+ * FC2 block-scaled FP4 x FP8 tensor-core stages with FP32 accumulation,
+ * store_hidden, fc2).
+ *   x_bf16     device BF16 [batch, H], 16-byte aligned
+ *   topk_ids   device int32 [batch, 16] (same rules as moe_group)
+ *   out_bf16   device BF16 [batch, 16, H], 16-byte aligned; row t*16+s is
+ *              expert ids[t, s]'s output for token t
+ * Asynchronous on `stream` (two kernel launches, the second overlapping the
+ * first's tail); device-side errors surface through moe_sync_status.
+ * Errors: MOE_ERR_ARG (nulls, misalignment, batch range), MOE_ERR_CUDA.
+ */
+int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
+            void* stream);
+
+/*
+ * moe_experts - kernels 3 and 4 alone: the persistent experts kernel and its
+ * output epilogue, on the plan and unit table that moe_quantize and
+ * moe_group (called in that order, with the same batch, on the same stream)
+ * left in the handle. moe_quantize + moe_group + moe_experts computes
+ * exactly what moe_run does. Source: [runtime] PersistentExperts.group / run
+ * (a unit-table kernel launched ahead of the experts kernel).
+ *   out_bf16  device BF16 [batch, 16, H], 16-byte aligned
+ * Errors: MOE_ERR_ARG, MOE_ERR_STATE (no plan or unit table of this batch),
+ * MOE_ERR_CUDA.
+ */
+int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream);
+
+/*
+ * moe_run_host - moe_run on host buffers: copies x and ids to handle-owned
+ * device buffers, runs the layer and copies out back, all on `stream`, then
+ * synchronizes the stream and returns moe_sync_status's result. Pinned host
+ * memory makes the copies asynchronous DMA transfers.
+ *   x_host BF16 [batch, H], ids_host int32 [batch, 16], out_host BF16
+ *   [batch, 16, H]. Errors: as moe_run, plus device-side status.
+ */
+int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void* out_host,
+                 int batch, void* stream);
+
+/*
+ * moe_sync_status - synchronize `stream` and return (and clear) the status
+ * word the kernels write: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded wait on
+ * another CTA's result ran out; the kernel still finished) or
+ * MOE_ERR_DEVICE_IDS. MOE_ERR_CUDA if the synchronization itself fails.
+ */
+int moe_sync_status(moe_handle h, void* stream);
+
+/*
+ * Read-back hooks (synchronous, for stage-by-stage checks):
+ *  moe_copy_plan   codes uint8 [batch, H], scales uint8 [batch, H/32] of the
+ *                  last quantize/run (batch <= that call's batch);
+ *  moe_copy_units  unit count, experts int32 [capacity], rows int16
+ *                  [capacity, 8] of the last group/run (MOE_ERR_ARG if the
+ *                  count exceeds capacity);
+ *  moe_copy_hidden hidden codes uint8 [units, 8, I] and scales uint8
+ *                  [units, 8, I/32] of the last run, row r of unit u being
+ *                  the unit's r-th pair.
+ * All write host memory; MOE_ERR_STATE before the producing call.
+ */
+int moe_copy_plan(moe_handle h, uint8_t* codes, uint8_t* scales, int batch);
+int moe_copy_units(moe_handle h, int32_t* count, int32_t* experts, int16_t* rows, int capacity);
+int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
+
+/*
+ * moe_set_timeout - bound, in nanoseconds, of every device-side wait on
+ * another CTA's hidden vector or on an mbarrier (default 2 s). After it
+ * runs out the kernel records MOE_ERR_DEVICE_TIMEOUT and finishes without
+ * waiting further. 0 restores the default.
+ * moe_debug_withhold - test hook: the unit with this index never publishes
+ * its hidden vector, so its consumers' waits run out (-1 = off, the
+ * default). Used to check the bounded waits without faulting the GPU.
+ */
+int moe_set_timeout(moe_handle h, uint64_t nanoseconds);
+int moe_debug_withhold(moe_handle h, int unit);
+
+int moe_info(moe_handle h, moe_info_t* info);
+
+/* Free every buffer of the handle (synchronizes its device). NULL is a no-op. */
+void moe_destroy(moe_handle h);
+
+/* Static description of a status code. */
+const char* moe_error_string(int status);
+
+/* Text of the last CUDA failure seen by this thread (for MOE_ERR_CUDA /
+ * MOE_ERR_UNSUPPORTED diagnostics); empty if none. */
+const char* moe_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_WEIGHT_MXFP8_GB300_MOE_H */

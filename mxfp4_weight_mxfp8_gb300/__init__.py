@@ -1,0 +1,227 @@
+"""GB300 (sm_103a) MXFP8-activation x MXFP4-weight top-16 MoE decode layer.
+
+A thin ctypes binding over the C ABI declared in ``include/moe.h``: every
+function here only marshals arguments (tensor or array -> pointer, torch
+stream -> cudaStream_t) and raises ``MoeError`` on a non-zero status. All of
+the layer's work runs in the library's CUDA kernels; there is no other path.
+Importing fails loudly when the library has not been built
+(``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIBRARY
+
+__all__ = [
+    "MoeError", "MoeInfo", "MoeLayer", "library", "moe_prepare", "moe_quantize", "moe_group",
+    "moe_run", "moe_experts", "moe_run_host", "moe_sync_status", "moe_copy_plan", "moe_copy_units",
+    "moe_copy_hidden", "moe_set_timeout", "moe_debug_withhold", "moe_info", "moe_destroy",
+    "moe_error_string", "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA",
+    "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS", "MOE_ERR_STATE", "TOPK", "UNIT_ROWS",
+    "MAX_BATCH",
+]
+
+MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
+MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_IDS, MOE_ERR_STATE = 4, 5, 6
+TOPK, UNIT_ROWS, MAX_BATCH = 16, 8, 256
+
+
+class MoeInfo(ctypes.Structure):
+    _fields_ = [("experts", ctypes.c_int), ("hidden", ctypes.c_int), ("inter", ctypes.c_int),
+                ("hidden_floor_rule", ctypes.c_int), ("grid", ctypes.c_int),
+                ("ring_stages", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("stages_per_expert", ctypes.c_int), ("unit_capacity", ctypes.c_int),
+                ("hidden_image_bytes", ctypes.c_int), ("weight_bytes", ctypes.c_size_t),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def _load():
+    if not os.path.exists(LIBRARY):
+        raise ImportError(f"CUDA library not built ({LIBRARY} missing): run "
+                          "`python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(LIBRARY)
+    vp, i32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+    signatures = {
+        "moe_prepare": ([ctypes.POINTER(vp), vp, vp, vp, vp, i32, i32, i32], i32),
+        "moe_quantize": ([vp, vp, i32, vp], i32),
+        "moe_group": ([vp, vp, i32, vp], i32),
+        "moe_run": ([vp, vp, vp, vp, i32, vp], i32),
+        "moe_experts": ([vp, vp, i32, vp], i32),
+        "moe_run_host": ([vp, vp, vp, vp, i32, vp], i32),
+        "moe_sync_status": ([vp, vp], i32),
+        "moe_copy_plan": ([vp, vp, vp, i32], i32),
+        "moe_copy_units": ([vp, vp, vp, vp, i32], i32),
+        "moe_copy_hidden": ([vp, vp, vp, i32], i32),
+        "moe_set_timeout": ([vp, u64], i32),
+        "moe_debug_withhold": ([vp, i32], i32),
+        "moe_info": ([vp, ctypes.POINTER(MoeInfo)], i32),
+        "moe_destroy": ([vp], None),
+        "moe_error_string": ([i32], ctypes.c_char_p),
+        "moe_last_error_detail": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in signatures.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes library (its path is ``library()._name``)."""
+    return _lib
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, call: str):
+        detail = _lib.moe_last_error_detail().decode()
+        text = _lib.moe_error_string(code).decode()
+        super().__init__(f"{call}: {text} (status {code}){': ' + detail if detail else ''}")
+        self.code = code
+
+
+def _check(code: int, call: str) -> int:
+    if code != MOE_OK:
+        raise MoeError(code, call)
+    return code
+
+
+def _ptr(obj):
+    """Address of a torch tensor, numpy array or raw integer pointer."""
+    if obj is None:
+        return None
+    if isinstance(obj, int):
+        return obj
+    if hasattr(obj, "data_ptr"):
+        return obj.data_ptr()
+    if hasattr(obj, "ctypes"):
+        return obj.ctypes.data
+    raise TypeError(f"cannot take the address of {type(obj).__name__}")
+
+
+def _stream(stream):
+    """cudaStream_t of a torch stream / raw handle; default: torch's current stream."""
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def moe_prepare(w13, s13, w2, s2, experts: int, hidden: int, inter: int):
+    """Handle (an int) of a prepared layer; see include/moe.h."""
+    handle = ctypes.c_void_p()
+    _check(_lib.moe_prepare(ctypes.byref(handle), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2),
+                            experts, hidden, inter), "moe_prepare")
+    return handle.value
+
+
+def moe_quantize(handle, x, batch: int, stream=None):
+    return _check(_lib.moe_quantize(handle, _ptr(x), batch, _stream(stream)), "moe_quantize")
+
+
+def moe_group(handle, ids, batch: int, stream=None):
+    return _check(_lib.moe_group(handle, _ptr(ids), batch, _stream(stream)), "moe_group")
+
+
+def moe_run(handle, x, ids, out, batch: int, stream=None):
+    return _check(_lib.moe_run(handle, _ptr(x), _ptr(ids), _ptr(out), batch, _stream(stream)),
+                  "moe_run")
+
+
+def moe_experts(handle, out, batch: int, stream=None):
+    return _check(_lib.moe_experts(handle, _ptr(out), batch, _stream(stream)), "moe_experts")
+
+
+def moe_run_host(handle, x, ids, out, batch: int, stream=None):
+    return _check(_lib.moe_run_host(handle, _ptr(x), _ptr(ids), _ptr(out), batch,
+                                    _stream(stream)), "moe_run_host")
+
+
+def moe_sync_status(handle, stream=None) -> int:
+    """Device status of the finished calls (not raised: tests inspect it)."""
+    return _lib.moe_sync_status(handle, _stream(stream))
+
+
+def moe_copy_plan(handle, codes, scales, batch: int):
+    return _check(_lib.moe_copy_plan(handle, _ptr(codes), _ptr(scales), batch), "moe_copy_plan")
+
+
+def moe_copy_units(handle, count, experts, rows, capacity: int):
+    return _check(_lib.moe_copy_units(handle, _ptr(count), _ptr(experts), _ptr(rows), capacity),
+                  "moe_copy_units")
+
+
+def moe_copy_hidden(handle, codes, scales, units: int):
+    return _check(_lib.moe_copy_hidden(handle, _ptr(codes), _ptr(scales), units),
+                  "moe_copy_hidden")
+
+
+def moe_set_timeout(handle, nanoseconds: int):
+    return _check(_lib.moe_set_timeout(handle, nanoseconds), "moe_set_timeout")
+
+
+def moe_debug_withhold(handle, unit: int):
+    return _check(_lib.moe_debug_withhold(handle, unit), "moe_debug_withhold")
+
+
+def moe_info(handle) -> MoeInfo:
+    info = MoeInfo()
+    _check(_lib.moe_info(handle, ctypes.byref(info)), "moe_info")
+    return info
+
+
+def moe_destroy(handle):
+    _lib.moe_destroy(handle)
+
+
+def moe_error_string(code: int) -> str:
+    return _lib.moe_error_string(code).decode()
+
+
+class MoeLayer:
+    """One prepared layer: owns a handle and allocates outputs with torch.
+
+    ``weights`` = (w13, s13, w2, s2) uint8 tensors or arrays in the layout of
+    include/moe.h (device or host). ``layer(x, ids)`` returns the BF16
+    [B, 16, H] rows on x's device, on the current torch stream.
+    """
+
+    def __init__(self, weights):
+        w13, s13, w2, s2 = weights
+        experts, rows, half_hidden = (int(d) for d in w13.shape)
+        self.experts, self.hidden, self.inter = experts, 2 * half_hidden, rows // 2
+        self._keep = weights
+        self.handle = moe_prepare(w13, s13, w2, s2, self.experts, self.hidden, self.inter)
+        self._keep = None
+
+    def __call__(self, x, ids, out=None, stream=None):
+        import torch
+
+        batch = int(x.shape[0])
+        if out is None:
+            out = torch.empty((batch, TOPK, self.hidden), dtype=torch.bfloat16, device=x.device)
+        moe_run(self.handle, x, ids, out, batch, stream)
+        return out
+
+    def info(self) -> dict:
+        return moe_info(self.handle).as_dict()
+
+    def close(self):
+        if self.handle:
+            moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,61 @@
+// Kernel argument blocks and host launchers shared by the translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Prep kernel: MXFP8 activation plan (blocks 0 .. quant_blocks-1) and the
+// unit table (the last block), as requested by `roles`.
+enum PrepRoles : int { kPrepQuantize = 1, kPrepGroup = 2 };
+
+struct PrepArgs {
+  const uint16_t* x;        // BF16 [B, H]
+  const int32_t* ids;       // [B, 16]
+  int B, H, E, P1, KC2, unit_cap;
+  uint8_t* plan_codes;      // [B, H]
+  uint8_t* plan_scales;     // [B, H / 32]
+  int32_t* unit_count;      // [1]
+  int32_t* unit_expert;     // [unit_cap]
+  int16_t* unit_rows;       // [unit_cap, 8]
+  uint32_t* item_counters;  // [unit_cap * P1], cleared per call
+  uint32_t* hidden_flags;   // [unit_cap * KC2], cleared per call
+  int32_t* status;
+  int roles;
+  int quant_blocks;
+};
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
+int prep_group_smem_bytes(int experts);
+
+// Persistent experts kernel.
+struct ExpertsArgs {
+  CUtensorMap wmap;           // 3-D map over the stage blocks (first: 64-byte aligned)
+  const uint8_t* stages;      // [E * SPE] blocks of kStageBytes
+  const uint8_t* plan_codes;  // [B, H]
+  const uint8_t* plan_scales; // [B, H / 32]
+  const int32_t* unit_count;
+  const int32_t* unit_expert;
+  const int16_t* unit_rows;
+  uint32_t* item_counters;
+  uint32_t* hidden_flags;
+  float* partials;            // [grid, 2, 2 tiles, 8 tokens, 128 rows]
+  uint8_t* hidden;            // [unit_cap, hidden_bytes]
+  uint16_t* out;              // BF16 [B * 16, H]
+  int32_t* status;
+  Geometry g;
+  uint64_t timeout_ns;
+  int withhold_unit;          // test hook: never publish this unit's hidden (-1 = off)
+};
+
+int experts_smem_bytes(const Geometry& g);
+cudaError_t experts_configure(const Geometry& g);
+cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);
+cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
+
+// Weight repack into stage blocks.
+cudaError_t launch_repack(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                          const uint8_t* s2, const Geometry& g, uint8_t* stages,
+                          cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,445 @@
+// The C ABI (include/moe.h): handle, weight repack, buffers, launches.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kernels.h"
+
+using moe::Geometry;
+
+struct moe_ctx {
+  int device = 0;
+  Geometry g{};
+  int sms = 0, grid = 0, smem_bytes = 0, unit_cap = 0;
+  uint8_t* stages = nullptr;
+  size_t stage_bytes = 0;
+  uint8_t* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  uint8_t* plan_codes = nullptr;
+  uint8_t* plan_scales = nullptr;
+  int32_t* unit_count = nullptr;
+  int32_t* unit_expert = nullptr;
+  int16_t* unit_rows = nullptr;
+  uint32_t* item_counters = nullptr;
+  uint32_t* hidden_flags = nullptr;
+  float* partials = nullptr;
+  uint8_t* hidden = nullptr;
+  int32_t* status = nullptr;
+  uint8_t* io = nullptr;  // device buffers of moe_run_host (x, ids, out), made on first use
+  CUtensorMap wmap{};
+  uint64_t timeout_ns = 2000000000ull;
+  int withhold = -1;
+  int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
+};
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call)                                  \
+  do {                                                  \
+    cudaError_t moe_e_ = (call);                        \
+    if (moe_e_ != cudaSuccess) return cuda_fail(moe_e_, #call); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+bool is_device_pointer(const void* p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+int encode_weight_map(moe_ctx* h) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  cudaDriverEntryPointQueryResult found{};
+  MOE_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled",
+                                            reinterpret_cast<void**>(&encode), 12000,
+                                            cudaEnableDefault, &found));
+  if (encode == nullptr || found != cudaDriverEntryPointSuccess) {
+    std::snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled unavailable");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  // Dimension 0: 128 e2m1 values of one row (64 bytes, expanded to 128 in
+  // shared memory); dimension 1: the 256 rows of a stage's two tiles;
+  // dimension 2: stage blocks. One box = one whole stage.
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(moe::kChunkK), 2u * moe::kTileM,
+                              static_cast<cuuint64_t>(h->g.E) * h->g.SPE};
+  const cuuint64_t strides[2] = {moe::kChunkK / 2, static_cast<cuuint64_t>(moe::kStageBytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(moe::kChunkK), 2u * moe::kTileM, 1u};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = encode(&h->wmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, h->stages, dims, strides,
+                      box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+void release(moe_ctx* h) {
+  if (h == nullptr) return;
+  int current = 0;
+  cudaGetDevice(&current);
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->stages);
+  cudaFree(h->workspace);
+  cudaFree(h->io);
+  cudaSetDevice(current);
+  delete h;
+}
+
+// Copy a weight array to the device when it lives in host memory.
+int stage_input(const void* src, size_t bytes, const uint8_t** dev, std::vector<void*>& temps) {
+  if (is_device_pointer(src)) {
+    *dev = static_cast<const uint8_t*>(src);
+    return MOE_OK;
+  }
+  void* p = nullptr;
+  MOE_CUDA(cudaMalloc(&p, bytes));
+  temps.push_back(p);
+  MOE_CUDA(cudaMemcpy(p, src, bytes, cudaMemcpyHostToDevice));
+  *dev = static_cast<const uint8_t*>(p);
+  return MOE_OK;
+}
+
+int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, const void* s2) {
+  const Geometry& g = h->g;
+  cudaDeviceProp prop{};
+  MOE_CUDA(cudaGetDevice(&h->device));
+  MOE_CUDA(cudaGetDeviceProperties(&prop, h->device));
+  h->smem_bytes = moe::experts_smem_bytes(g);
+  if (prop.major != 10 ||
+      static_cast<int>(prop.sharedMemPerBlockOptin) < moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER))) {
+    std::snprintf(g_detail, sizeof g_detail, "needs an sm_100-family GPU with %d B shared memory",
+                  h->smem_bytes);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  h->sms = prop.multiProcessorCount;
+  MOE_CUDA(moe::experts_configure(g));
+  int per_sm = 0;
+  MOE_CUDA(moe::experts_occupancy(g, &per_sm));
+  if (per_sm < 1) {
+    std::snprintf(g_detail, sizeof g_detail, "experts kernel does not fit on an SM");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  h->grid = h->sms;  // one co-resident CTA per SM
+
+  // Weights: one 17 KB block per stage.
+  h->stage_bytes = static_cast<size_t>(g.E) * g.SPE * moe::kStageBytes;
+  MOE_CUDA(cudaMalloc(&h->stages, h->stage_bytes));
+  std::vector<void*> temps;
+  const uint8_t *d13, *ds13, *d2, *ds2;
+  const size_t n13 = static_cast<size_t>(g.E) * 2 * g.I * (g.H / 2);
+  const size_t n2 = static_cast<size_t>(g.E) * g.H * (g.I / 2);
+  int rc = stage_input(w13, n13, &d13, temps);
+  if (rc == MOE_OK) rc = stage_input(s13, n13 / 16, &ds13, temps);
+  if (rc == MOE_OK) rc = stage_input(w2, n2, &d2, temps);
+  if (rc == MOE_OK) rc = stage_input(s2, n2 / 16, &ds2, temps);
+  if (rc == MOE_OK) {
+    cudaError_t e = moe::launch_repack(d13, ds13, d2, ds2, g, h->stages, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = cuda_fail(e, "weight repack");
+  }
+  for (void* p : temps) cudaFree(p);
+  if (rc != MOE_OK) return rc;
+
+  // Plan, unit table and workspace in one allocation.
+  h->unit_cap = moe::unit_capacity(MOE_MAX_BATCH, g.E);
+  const size_t sizes[] = {
+      static_cast<size_t>(MOE_MAX_BATCH) * g.H,                 // plan codes
+      static_cast<size_t>(MOE_MAX_BATCH) * (g.H / moe::kBlock), // plan scales
+      4,                                                        // unit count
+      static_cast<size_t>(h->unit_cap) * 4,                     // unit experts
+      static_cast<size_t>(h->unit_cap) * moe::kUnitRows * 2,    // unit rows
+      static_cast<size_t>(h->unit_cap) * g.P1 * 4,              // FC1 item counters
+      static_cast<size_t>(h->unit_cap) * g.KC2 * 4,             // hidden flags
+      static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
+      static_cast<size_t>(h->unit_cap) * g.hidden_bytes,        // hidden images
+      4,                                                        // status
+  };
+  size_t offsets[10], total = 0;
+  for (int i = 0; i < 10; ++i) {
+    offsets[i] = total;
+    total += round256(sizes[i]);
+  }
+  h->workspace_bytes = total;
+  MOE_CUDA(cudaMalloc(&h->workspace, total));
+  MOE_CUDA(cudaMemset(h->workspace, 0, total));
+  uint8_t* w = h->workspace;
+  h->plan_codes = w + offsets[0];
+  h->plan_scales = w + offsets[1];
+  h->unit_count = reinterpret_cast<int32_t*>(w + offsets[2]);
+  h->unit_expert = reinterpret_cast<int32_t*>(w + offsets[3]);
+  h->unit_rows = reinterpret_cast<int16_t*>(w + offsets[4]);
+  h->item_counters = reinterpret_cast<uint32_t*>(w + offsets[5]);
+  h->hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
+  h->partials = reinterpret_cast<float*>(w + offsets[7]);
+  h->hidden = w + offsets[8];
+  h->status = reinterpret_cast<int32_t*>(w + offsets[9]);
+  return encode_weight_map(h);
+}
+
+moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch, int roles) {
+  moe::PrepArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.ids = ids;
+  a.B = batch;
+  a.H = h->g.H;
+  a.E = h->g.E;
+  a.P1 = h->g.P1;
+  a.KC2 = h->g.KC2;
+  a.unit_cap = h->unit_cap;
+  a.plan_codes = h->plan_codes;
+  a.plan_scales = h->plan_scales;
+  a.unit_count = h->unit_count;
+  a.unit_expert = h->unit_expert;
+  a.unit_rows = h->unit_rows;
+  a.item_counters = h->item_counters;
+  a.hidden_flags = h->hidden_flags;
+  a.status = h->status;
+  a.roles = roles;
+  a.quant_blocks = (batch * (h->g.H / 8) + 255) / 256;
+  return a;
+}
+
+int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE_OK : MOE_ERR_ARG; }
+
+int launch_experts(moe_ctx* h, void* out, cudaStream_t stream) {
+  moe::ExpertsArgs a{};
+  a.wmap = h->wmap;
+  a.stages = h->stages;
+  a.plan_codes = h->plan_codes;
+  a.plan_scales = h->plan_scales;
+  a.unit_count = h->unit_count;
+  a.unit_expert = h->unit_expert;
+  a.unit_rows = h->unit_rows;
+  a.item_counters = h->item_counters;
+  a.hidden_flags = h->hidden_flags;
+  a.partials = h->partials;
+  a.hidden = h->hidden;
+  a.out = static_cast<uint16_t*>(out);
+  a.status = h->status;
+  a.g = h->g;
+  a.timeout_ns = h->timeout_ns;
+  a.withhold_unit = h->withhold;
+  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_prepare(moe_handle* out, const void* w13, const void* s13, const void* w2, const void* s2,
+                int experts, int hidden, int inter) {
+  if (out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  if (!w13 || !s13 || !w2 || !s2) return MOE_ERR_ARG;
+  if (experts < 1 || experts > MOE_MAX_EXPERTS) return MOE_ERR_ARG;
+  if (hidden < 256 || hidden > MOE_MAX_HIDDEN || hidden % 256 != 0) return MOE_ERR_ARG;
+  if (inter < 32 || inter > MOE_MAX_INTER || inter % 32 != 0) return MOE_ERR_ARG;
+  moe_ctx* h = new (std::nothrow) moe_ctx();
+  if (h == nullptr) return MOE_ERR_CUDA;
+  h->g = moe::make_geometry(experts, hidden, inter);
+  const int rc = build_handle(h, w13, s13, w2, s2);
+  if (rc != MOE_OK) {
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_quantize(moe_handle h, const void* x_bf16, int batch, void* stream) {
+  if (h == nullptr || x_bf16 == nullptr || !aligned16(x_bf16) || check_batch(batch)) return MOE_ERR_ARG;
+  MOE_CUDA(moe::launch_prep(prep_args(h, x_bf16, nullptr, batch, moe::kPrepQuantize),
+                            static_cast<cudaStream_t>(stream)));
+  h->plan_batch = batch;
+  return MOE_OK;
+}
+
+int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream) {
+  if (h == nullptr || topk_ids == nullptr || !aligned16(topk_ids) || check_batch(batch))
+    return MOE_ERR_ARG;
+  MOE_CUDA(moe::launch_prep(prep_args(h, nullptr, topk_ids, batch, moe::kPrepGroup),
+                            static_cast<cudaStream_t>(stream)));
+  h->grouped = 1;
+  h->group_batch = batch;
+  return MOE_OK;
+}
+
+int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
+            void* stream) {
+  if (h == nullptr || !x_bf16 || !topk_ids || !out_bf16) return MOE_ERR_ARG;
+  if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(out_bf16) || check_batch(batch))
+    return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(moe::launch_prep(
+      prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
+  const int rc = launch_experts(h, out_bf16, s);
+  if (rc != MOE_OK) return rc;
+  h->plan_batch = batch;
+  h->group_batch = batch;
+  h->grouped = 1;
+  h->ran = 1;
+  return MOE_OK;
+}
+
+int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
+  if (h == nullptr || out_bf16 == nullptr || !aligned16(out_bf16) || check_batch(batch))
+    return MOE_ERR_ARG;
+  if (h->plan_batch != batch || h->group_batch != batch) return MOE_ERR_STATE;
+  const int rc = launch_experts(h, out_bf16, static_cast<cudaStream_t>(stream));
+  if (rc == MOE_OK) h->ran = 1;
+  return rc;
+}
+
+int moe_sync_status(moe_handle h, void* stream) {
+  if (h == nullptr) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t status = 0;
+  MOE_CUDA(cudaMemcpyAsync(&status, h->status, 4, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemsetAsync(h->status, 0, 4, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  return status;
+}
+
+int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void* out_host,
+                 int batch, void* stream) {
+  if (h == nullptr || !x_host || !ids_host || !out_host || check_batch(batch)) return MOE_ERR_ARG;
+  const size_t xb = round256(static_cast<size_t>(MOE_MAX_BATCH) * h->g.H * 2);
+  const size_t ib = round256(static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * 4);
+  const size_t ob = static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * h->g.H * 2;
+  if (h->io == nullptr) MOE_CUDA(cudaMalloc(&h->io, xb + ib + ob));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* dx = h->io;
+  int32_t* dids = reinterpret_cast<int32_t*>(h->io + xb);
+  uint8_t* dout = h->io + xb + ib;
+  const size_t x_bytes = static_cast<size_t>(batch) * h->g.H * 2;
+  const size_t ids_bytes = static_cast<size_t>(batch) * MOE_TOPK * 4;
+  const size_t out_bytes = static_cast<size_t>(batch) * MOE_TOPK * h->g.H * 2;
+  MOE_CUDA(cudaMemcpyAsync(dx, x_host, x_bytes, cudaMemcpyHostToDevice, s));
+  MOE_CUDA(cudaMemcpyAsync(dids, ids_host, ids_bytes, cudaMemcpyHostToDevice, s));
+  const int rc = moe_run(h, dx, dids, dout, batch, stream);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, s));
+  return moe_sync_status(h, stream);
+}
+
+int moe_copy_plan(moe_handle h, uint8_t* codes, uint8_t* scales, int batch) {
+  if (h == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_ARG;
+  if (h->plan_batch == 0) return MOE_ERR_STATE;
+  if (batch < 1 || batch > h->plan_batch) return MOE_ERR_ARG;
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(codes, h->plan_codes, static_cast<size_t>(batch) * h->g.H,
+                      cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(scales, h->plan_scales, static_cast<size_t>(batch) * (h->g.H / moe::kBlock),
+                      cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+int moe_copy_units(moe_handle h, int32_t* count, int32_t* experts, int16_t* rows, int capacity) {
+  if (h == nullptr || count == nullptr) return MOE_ERR_ARG;
+  if (!h->grouped) return MOE_ERR_STATE;
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(count, h->unit_count, 4, cudaMemcpyDeviceToHost));
+  if (*count > capacity || (*count > 0 && (experts == nullptr || rows == nullptr))) return MOE_ERR_ARG;
+  if (*count > 0) {
+    MOE_CUDA(cudaMemcpy(experts, h->unit_expert, static_cast<size_t>(*count) * 4,
+                        cudaMemcpyDeviceToHost));
+    MOE_CUDA(cudaMemcpy(rows, h->unit_rows, static_cast<size_t>(*count) * moe::kUnitRows * 2,
+                        cudaMemcpyDeviceToHost));
+  }
+  return MOE_OK;
+}
+
+int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units) {
+  if (h == nullptr || codes == nullptr || scales == nullptr || units < 0) return MOE_ERR_ARG;
+  if (!h->ran) return MOE_ERR_STATE;
+  if (units > h->unit_cap) return MOE_ERR_ARG;
+  const Geometry& g = h->g;
+  std::vector<uint8_t> img(static_cast<size_t>(units) * g.hidden_bytes);
+  MOE_CUDA(cudaDeviceSynchronize());
+  if (!img.empty())
+    MOE_CUDA(cudaMemcpy(img.data(), h->hidden, img.size(), cudaMemcpyDeviceToHost));
+  for (int u = 0; u < units; ++u) {
+    const uint8_t* base = img.data() + static_cast<size_t>(u) * g.hidden_bytes;
+    for (int r = 0; r < moe::kUnitRows; ++r) {
+      for (int j = 0; j < g.I; ++j) {
+        const int c = j / moe::kChunkK, k = j % moe::kChunkK;
+        codes[(static_cast<size_t>(u) * moe::kUnitRows + r) * g.I + j] =
+            base[c * moe::kActImageBytes + moe::swizzle128(r, k >> 4) + (k & 15)];
+      }
+      for (int b = 0; b < g.I / moe::kBlock; ++b) {
+        const int c = b / 4, kb = b % 4;
+        scales[(static_cast<size_t>(u) * moe::kUnitRows + r) * (g.I / moe::kBlock) + b] =
+            base[g.KC2 * moe::kActImageBytes + c * moe::kScaleAtomBytes + moe::scale_atom(r, kb)];
+      }
+    }
+  }
+  return MOE_OK;
+}
+
+int moe_set_timeout(moe_handle h, uint64_t nanoseconds) {
+  if (h == nullptr) return MOE_ERR_ARG;
+  h->timeout_ns = nanoseconds ? nanoseconds : 2000000000ull;
+  return MOE_OK;
+}
+
+int moe_debug_withhold(moe_handle h, int unit) {
+  if (h == nullptr || unit < -1) return MOE_ERR_ARG;
+  h->withhold = unit;
+  return MOE_OK;
+}
+
+int moe_info(moe_handle h, moe_info_t* info) {
+  if (h == nullptr || info == nullptr) return MOE_ERR_ARG;
+  info->experts = h->g.E;
+  info->hidden = h->g.H;
+  info->inter = h->g.I;
+  info->hidden_floor_rule = h->g.floor_rule;
+  info->grid = h->grid;
+  info->ring_stages = moe::kRingStages;
+  info->smem_bytes = h->smem_bytes;
+  info->stages_per_expert = h->g.SPE;
+  info->unit_capacity = h->unit_cap;
+  info->hidden_image_bytes = h->g.hidden_bytes;
+  info->weight_bytes = h->stage_bytes;
+  info->workspace_bytes = h->workspace_bytes;
+  return MOE_OK;
+}
+
+void moe_destroy(moe_handle h) { release(h); }
+
+const char* moe_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_IDS: return "expert id out of range or repeated within a token";
+    case MOE_ERR_STATE: return "call order: the data asked for was not produced yet";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+}  // extern "C"

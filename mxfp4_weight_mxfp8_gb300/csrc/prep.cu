@@ -1,0 +1,171 @@
+// Kernel 1 (MXFP8 activation plan) and kernel 2 (unit table), launched as one
+// grid by moe_run and separately by moe_quantize / moe_group.
+//
+// Quantizer: page ...cutedsl.moe.experts, mx_block / plan_chunk /
+// ExpertsPlanKernel: one E8M0 scale per 32 BF16 values (the smallest E with
+// max|x| <= 448 * 2^E), codes e4m3(x * 2^-E). Each thread owns 8 consecutive
+// values (one 16-byte load); the four threads of a 32-block combine their
+// maxima with two butterfly shuffles, so the result is bit-identical to a
+// whole-block maximum.
+//
+// Grouping: ExpertsKernel.group / ExpertsGroupKernel: per-expert token
+// bitmasks (atomic OR), unit counts ceil(n_e / 8), an exclusive scan in
+// expert order, and each pair's row = popcount of the lower tokens' bits.
+// Experts ascend, rows keep token order, padding is -1.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+__device__ void quantize_role(const PrepArgs& a, int block) {
+  const int per_row = a.H / 8;  // 8-value chunks per token
+  const int total = a.B * per_row;
+  const int chunk = block * kPrepThreads + threadIdx.x;
+  const bool active = chunk < total;  // uniform across each 4-lane block (total % 4 == 0)
+  const int token = active ? chunk / per_row : 0;
+  const int c = active ? chunk % per_row : 0;
+  float v[8];
+  float amax = 0.f;
+  if (active) {
+    uint4 w = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(token) * a.H + c * 8);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(words[i] << 16);
+      v[2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  if (!active) return;
+  const int E = mx_exponent(amax, false);
+  const float inv = pow2f(-E);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(e4m3_code(v[4 + i] * inv)) << (8 * i);
+  *reinterpret_cast<uint2*>(a.plan_codes + static_cast<size_t>(token) * a.H + c * 8) =
+      make_uint2(lo, hi);
+  if ((c & 3) == 0)
+    a.plan_scales[static_cast<size_t>(token) * (a.H / kBlock) + c / 4] =
+        static_cast<uint8_t>(E + 127);
+}
+
+__device__ void group_role(const PrepArgs& a, uint8_t* smem) {
+  const int E = a.E, pairs = a.B * kTopK, words = (a.B + 31) / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem);          // [E][words]
+  int32_t* ustart = reinterpret_cast<int32_t*>(masks + E * words);  // [E]
+  uint32_t* owner = reinterpret_cast<uint32_t*>(ustart + E);    // [128]: pair kept its bit
+  int32_t* warp_total = reinterpret_cast<int32_t*>(owner + 128);  // [8]
+  int32_t* grand = warp_total + 8;                              // [1]
+
+  for (int i = tid; i < E * words; i += kPrepThreads) masks[i] = 0;
+  for (int i = tid; i < 128; i += kPrepThreads) owner[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < pairs; p += kPrepThreads) {
+    const int e = a.ids[p], t = p >> 4;
+    if (e < 0 || e >= E) {
+      report(a.status, MOE_ERR_DEVICE_IDS);
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    const uint32_t old = atomicOr(&masks[e * words + (t >> 5)], bit);
+    if (old & bit)
+      report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within token t
+    else
+      atomicOr(&owner[p >> 5], 1u << (p & 31));
+  }
+  __syncthreads();
+
+  // Units per expert over a contiguous expert range per thread, then an
+  // exclusive scan in expert order.
+  const int span = (E + kPrepThreads - 1) / kPrepThreads;
+  const int e0 = tid * span, e1 = min(E, e0 + span);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) {
+    int n = 0;
+    for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
+    local += (n + 7) >> 3;
+  }
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int other = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += other;
+  }
+  if (lane == 31) warp_total[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_total[w];
+  if (tid == kPrepThreads - 1) *grand = before + incl;
+  int start = before + incl - local;
+  for (int e = e0; e < e1; ++e) {
+    int n = 0;
+    for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
+    const int units = (n + 7) >> 3;
+    ustart[e] = start;
+    for (int v = 0; v < units && start + v < a.unit_cap; ++v) {
+      a.unit_expert[start + v] = e;
+      const int valid = min(kUnitRows, n - kUnitRows * v);
+      for (int r = valid; r < kUnitRows; ++r) a.unit_rows[(start + v) * kUnitRows + r] = -1;
+    }
+    start += units;
+  }
+  __syncthreads();
+  int units = *grand;
+  if (units > a.unit_cap) {  // cannot happen: units <= 2B + min(E, 16B)
+    report(a.status, MOE_ERR_DEVICE_IDS);
+    units = 0;
+  }
+  if (tid == 0) *a.unit_count = units;
+  if (units == 0) return;
+  for (int p = tid; p < pairs; p += kPrepThreads) {
+    if (!((owner[p >> 5] >> (p & 31)) & 1u)) continue;
+    const int e = a.ids[p], t = p >> 4, w = t >> 5;
+    int rank = __popc(masks[e * words + w] & ((1u << (t & 31)) - 1u));
+    for (int i = 0; i < w; ++i) rank += __popc(masks[e * words + i]);
+    a.unit_rows[(ustart[e] + (rank >> 3)) * kUnitRows + (rank & 7)] = static_cast<int16_t>(p);
+  }
+  for (int i = tid; i < units * a.P1; i += kPrepThreads) a.item_counters[i] = 0;
+  for (int i = tid; i < units * a.KC2; i += kPrepThreads) a.hidden_flags[i] = 0;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  // Let the experts kernel start its prologue; it waits for this grid's end
+  // before reading anything written here.
+  ptx::grid_launch_dependents();
+  const int block = blockIdx.x;
+  if ((a.roles & kPrepQuantize) && block < a.quant_blocks) {
+    quantize_role(a, block);
+  } else if ((a.roles & kPrepGroup) &&
+             block == ((a.roles & kPrepQuantize) ? a.quant_blocks : 0)) {
+    group_role(a, smem);
+  }
+}
+
+}  // namespace
+
+int prep_group_smem_bytes(int experts) {
+  const int words = (MOE_MAX_BATCH + 31) / 32;
+  return experts * words * 4 + experts * 4 + 128 * 4 + 9 * 4;
+}
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
+  int blocks = 0;
+  if (a.roles & kPrepQuantize) blocks += a.quant_blocks;
+  if (a.roles & kPrepGroup) blocks += 1;
+  if (blocks == 0) return cudaSuccess;
+  const int smem = (a.roles & kPrepGroup) ? prep_group_smem_bytes(a.E) : 0;
+  prep_kernel<<<blocks, kPrepThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

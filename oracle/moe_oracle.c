@@ -207,21 +207,40 @@ typedef struct {
   int E, H, I;
 } orc_weights;
 
-static double weight_value(const uint8_t* w, const uint8_t* s, size_t row, int K, int k) {
-  unsigned byte = w[row * (size_t)(K / 2) + (size_t)(k / 2)];
-  unsigned code = (k & 1) ? (byte >> 4) : (byte & 15u);
-  return orc_e2m1_value(code) * orc_e8m0_value(s[row * (size_t)(K / 32) + (size_t)(k / 32)]);
+/* Decode tables: the value of every e4m3 code and every E8M0 byte, filled
+ * once from the functions above (decoding "by table"). */
+static double E4M3_TABLE[256], E8M0_TABLE[256];
+static int tables_ready = 0;
+
+static void fill_tables(void) {
+  if (tables_ready) return;
+  for (unsigned c = 0; c < 256; ++c) {
+    E4M3_TABLE[c] = orc_e4m3_value(c);
+    E8M0_TABLE[c] = orc_e8m0_value(c);
+  }
+  tables_ready = 1;
+}
+
+/* Row `row` of an MXFP4 matrix with K columns, decoded to float64. */
+static void decode_row(const uint8_t* w, const uint8_t* s, size_t row, int K, double* out) {
+  const uint8_t* wr = w + row * (size_t)(K / 2);
+  const uint8_t* sr = s + row * (size_t)(K / 32);
+  for (int k = 0; k < K; ++k) {
+    unsigned byte = wr[k / 2];
+    unsigned code = (k & 1) ? (byte >> 4) : (byte & 15u);
+    out[k] = orc_e2m1_value(code) * E8M0_TABLE[sr[k / 32]];
+  }
 }
 
 /* FC1 of expert e on one dequantized activation row xv[H] (float64):
  * y[r] = sum_k W13[e, r, k] * xv[k], r in [0, 2I) (rows 0..I-1 gate,
  * I..2I-1 up). [experts] stage ("fc1": FP4 weights x MXFP8 activations,
  * block-scaled, FP32 accumulation on the GPU; exact sums here). */
-static void fc1(const orc_weights* W, int e, const double* xv, double* y) {
+static void fc1(const orc_weights* W, int e, const double* xv, double* y, double* wrow) {
   for (int r = 0; r < 2 * W->I; ++r) {
-    size_t row = (size_t)e * 2 * W->I + r;
+    decode_row(W->w13, W->s13, (size_t)e * 2 * W->I + r, W->H, wrow);
     double acc = 0.0;
-    for (int k = 0; k < W->H; ++k) acc += weight_value(W->w13, W->s13, row, W->H, k) * xv[k];
+    for (int k = 0; k < W->H; ++k) acc += wrow[k] * xv[k];
     y[r] = acc;
   }
 }
@@ -236,11 +255,11 @@ double orc_gated(double gate, double up) { return gate / (1.0 + exp(-gate)) * up
 
 /* FC2 of expert e on the dequantized hidden row hv[I]:
  * o[n] = sum_j W2[e, n, j] * hv[j], n in [0, H). [experts] stage ("fc2"). */
-static void fc2(const orc_weights* W, int e, const double* hv, double* o) {
+static void fc2(const orc_weights* W, int e, const double* hv, double* o, double* wrow) {
   for (int n = 0; n < W->H; ++n) {
-    size_t row = (size_t)e * W->H + n;
+    decode_row(W->w2, W->s2, (size_t)e * W->H + n, W->I, wrow);
     double acc = 0.0;
-    for (int j = 0; j < W->I; ++j) acc += weight_value(W->w2, W->s2, row, W->I, j) * hv[j];
+    for (int j = 0; j < W->I; ++j) acc += wrow[j] * hv[j];
     o[n] = acc;
   }
 }
@@ -262,6 +281,7 @@ void orc_pairs(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const 
                int threads) {
   orc_weights W = {w13, s13, w2, s2, E, H, I};
   int floor_rule = orc_hidden_floor_rule(I);
+  fill_tables();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
   for (int i = 0; i < n; ++i) {
     int pair = pairs[i], token = pair / ORC_SLOTS, e = ids[pair];
@@ -271,19 +291,19 @@ void orc_pairs(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const 
     double* o = (double*)malloc(sizeof(double) * (size_t)H);
     uint8_t* codes = (uint8_t*)malloc((size_t)I);
     uint8_t* scales = (uint8_t*)malloc((size_t)(I / 32));
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
     for (int k = 0; k < H; ++k)
-      xv[k] = orc_e4m3_value(xq[(size_t)token * H + k]) *
-              orc_e8m0_value(xs[(size_t)token * (H / 32) + k / 32]);
-    fc1(&W, e, xv, yy);
+      xv[k] = E4M3_TABLE[xq[(size_t)token * H + k]] * E8M0_TABLE[xs[(size_t)token * (H / 32) + k / 32]];
+    fc1(&W, e, xv, yy, wrow);
     for (int j = 0; j < I; ++j) hv[j] = orc_gated(yy[j], yy[I + j]);
     for (int b = 0; b < I / 32; ++b) orc_mxfp8_block(hv + 32 * b, floor_rule, codes + 32 * b, scales + b);
-    for (int j = 0; j < I; ++j) hv[j] = orc_e4m3_value(codes[j]) * orc_e8m0_value(scales[j / 32]);
-    fc2(&W, e, hv, o);
+    for (int j = 0; j < I; ++j) hv[j] = E4M3_TABLE[codes[j]] * E8M0_TABLE[scales[j / 32]];
+    fc2(&W, e, hv, o, wrow);
     for (int c = 0; c < H; ++c) out[(size_t)i * H + c] = orc_bf16_encode(o[c]);
     if (hq) memcpy(hq + (size_t)i * I, codes, (size_t)I);
     if (hs) memcpy(hs + (size_t)i * (I / 32), scales, (size_t)(I / 32));
     if (y) memcpy(y + (size_t)i * 2 * I, yy, sizeof(double) * 2 * (size_t)I);
-    free(xv), free(yy), free(hv), free(o), free(codes), free(scales);
+    free(xv), free(yy), free(hv), free(o), free(codes), free(scales), free(wrow);
   }
 }
 
@@ -292,14 +312,16 @@ void orc_pairs(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const 
 void orc_fc2_rows(const uint8_t* w2, const uint8_t* s2, int E, int H, int I, const int32_t* experts,
                   const uint8_t* hq, const uint8_t* hs, int n, uint16_t* out, int threads) {
   orc_weights W = {NULL, NULL, w2, s2, E, H, I};
+  fill_tables();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
   for (int i = 0; i < n; ++i) {
     double* hv = (double*)malloc(sizeof(double) * (size_t)I);
     double* o = (double*)malloc(sizeof(double) * (size_t)H);
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)I);
     for (int j = 0; j < I; ++j)
-      hv[j] = orc_e4m3_value(hq[(size_t)i * I + j]) * orc_e8m0_value(hs[(size_t)i * (I / 32) + j / 32]);
-    fc2(&W, experts[i], hv, o);
+      hv[j] = E4M3_TABLE[hq[(size_t)i * I + j]] * E8M0_TABLE[hs[(size_t)i * (I / 32) + j / 32]];
+    fc2(&W, experts[i], hv, o, wrow);
     for (int c = 0; c < H; ++c) out[(size_t)i * H + c] = orc_bf16_encode(o[c]);
-    free(hv), free(o);
+    free(hv), free(o), free(wrow);
   }
 }

@@ -19,9 +19,16 @@ _CACHE: dict = {}
 
 
 def cached_inputs(name: str):
-    """(weights, x, ids) of a named workload, generated once per session."""
+    """(weights, x, ids) of a named workload, generated once per session;
+    workloads of the same layer shape share one weight set (same seeds)."""
     import workload
 
     if name not in _CACHE:
-        _CACHE[name] = workload.make_inputs(workload.CONFIGS[name])
+        cfg = workload.CONFIGS[name]
+        shape = (cfg.experts, cfg.hidden, cfg.inter)
+        if shape not in _CACHE:
+            _CACHE[shape] = workload.make_weights(*shape)
+        x = workload.make_x(cfg.batch, cfg.hidden, outlier_fraction=cfg.outlier_fraction)
+        ids = workload.make_ids(cfg.batch, cfg.experts, dist=cfg.ids, s=cfg.zipf_s)
+        _CACHE[name] = (_CACHE[shape], x, ids)
     return _CACHE[name]

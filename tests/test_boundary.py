@@ -1,0 +1,93 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+entry point include/moe.h declares, and rejects bad arguments before touching
+the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|void)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mxfp4_weight_mxfp8_gb300 as moe
+
+    return moe
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for call in ("moe_prepare", "moe_quantize", "moe_group", "moe_run"):
+        assert call in names
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.library()._name)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_library_is_built_for_sm103a(lib):
+    data = open(lib.library()._name, "rb").read()
+    assert b"sm_103a" in data or b"sm_103" in data
+
+
+def test_error_strings(lib):
+    for code in range(7):
+        assert lib.moe_error_string(code)
+    assert lib.moe_error_string(99) == "unknown status"
+
+
+def test_prepare_rejects_bad_arguments_before_any_cuda_call(lib):
+    raw = lib.library()
+    handle = ctypes.c_void_p(1234)
+    fake = ctypes.c_void_p(0x1000)
+    assert raw.moe_prepare(None, fake, fake, fake, fake, 32, 256, 64) == lib.MOE_ERR_ARG
+    bad_sizes = [(0, 256, 64), (1025, 256, 64), (32, 255, 64), (32, 384, 64), (32, 256, 48),
+                 (32, 256, 16), (32, 256, 544), (32, 16640, 64)]
+    for experts, hidden, inter in bad_sizes:
+        rc = raw.moe_prepare(ctypes.byref(handle), fake, fake, fake, fake, experts, hidden, inter)
+        assert rc == lib.MOE_ERR_ARG, (experts, hidden, inter)
+        assert handle.value is None
+    assert raw.moe_prepare(ctypes.byref(handle), None, fake, fake, fake, 32, 256, 64) == lib.MOE_ERR_ARG
+
+
+def test_calls_reject_null_handles_and_bad_batches(lib):
+    raw = lib.library()
+    p = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+    assert raw.moe_run(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_quantize(None, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_group(None, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_run_host(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_experts(None, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_sync_status(None, None) == lib.MOE_ERR_ARG
+    assert raw.moe_copy_plan(None, p, p, 1) == lib.MOE_ERR_ARG
+    assert raw.moe_copy_units(None, p, p, p, 1) == lib.MOE_ERR_ARG
+    assert raw.moe_copy_hidden(None, p, p, 1) == lib.MOE_ERR_ARG
+    assert raw.moe_set_timeout(None, 5) == lib.MOE_ERR_ARG
+    assert raw.moe_debug_withhold(None, 0) == lib.MOE_ERR_ARG
+    info = lib.MoeInfo()
+    assert raw.moe_info(None, ctypes.byref(info)) == lib.MOE_ERR_ARG
+    raw.moe_destroy(None)  # no-op
+
+
+def test_python_binding_names_match_the_c_abi(lib):
+    for name in declared_functions():
+        if name == "moe_last_error_detail":
+            continue
+        assert hasattr(lib, name), name

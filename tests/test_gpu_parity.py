@@ -1,0 +1,319 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.
+
+Bars (pages ...cutedsl.moe.experts / ...experts_runtime as read for this
+build): the MXFP8 activation plan and the unit table match bit for bit; the
+output matches within relative L2 <= 1e-2 over all rows and
+|err| <= 3e-2 * rms(row) for every element; hidden requant flips (codes that
+differ because the GPU sums FP32 in another order than the float64 oracle) are
+counted and reported, and FC2 alone is re-checked on the GPU's own hidden
+codes.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workload
+from conftest import cached_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+ROW_TOL = 3e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    import mxfp4_weight_mxfp8_gb300 as m
+
+    return m
+
+
+_LAYERS: dict = {}
+
+
+def layer_for(moe, weights):
+    import torch
+
+    w13 = weights[0]
+    key = (w13.shape, id(weights))
+    if key not in _LAYERS:
+        dev = torch.device("cuda:0")
+        _LAYERS[key] = moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights))
+    return _LAYERS[key]
+
+
+def to_device(x_bits, ids):
+    import torch
+
+    dev = torch.device("cuda:0")
+    xd = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    return xd, torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).to(dev)
+
+
+def bf16_to_float(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def run_layer(moe, layer, x_bits, ids):
+    import torch
+
+    xd, idsd = to_device(x_bits, ids)
+    out = layer(xd, idsd)
+    status = moe.moe_sync_status(layer.handle)
+    B = x_bits.shape[0]
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * 16, layer.hidden)
+    return got, status
+
+
+def check_rows(got_bits, ref_bits, label):
+    got, ref = bf16_to_float(got_bits).astype(np.float64), bf16_to_float(ref_bits).astype(np.float64)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    worst = np.max(np.abs(got - ref) / np.maximum(rms, 1e-300))
+    print(f"[{label}] rel L2 {rel:.3e}, worst |err|/rms(row) {worst:.3e}")
+    assert rel <= REL_L2, f"{label}: relative L2 {rel}"
+    assert worst <= ROW_TOL, f"{label}: element error {worst} x rms(row)"
+    return rel, worst
+
+
+def units_of(moe, layer, batch):
+    count = np.zeros(1, np.int32)
+    cap = batch * 16
+    experts = np.zeros(cap, np.int32)
+    rows = np.zeros(cap * 8, np.int16)
+    moe.moe_copy_units(layer.handle, count, experts, rows, cap)
+    n = int(count[0])
+    return experts[:n], rows[: n * 8].reshape(n, 8)
+
+
+CONFIGS = ["tiny", "tp8_b1", "tp16_b8", "tp8_b64", "tp8_b256"]
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_quantize_plan_is_bit_exact(moe, name):
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    xd, _ = to_device(x, ids)
+    B, H = x.shape
+    moe.moe_quantize(layer.handle, xd, B)
+    assert moe.moe_sync_status(layer.handle) == moe.MOE_OK
+    codes = np.zeros((B, H), np.uint8)
+    scales = np.zeros((B, H // 32), np.uint8)
+    moe.moe_copy_plan(layer.handle, codes, scales, B)
+    ref_codes, ref_scales = oracle.quantize_x(x)
+    np.testing.assert_array_equal(scales, ref_scales)
+    np.testing.assert_array_equal(codes, ref_codes)
+
+
+def test_quantize_edge_values_are_bit_exact(moe):
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    H = 256
+    rng = np.random.default_rng(17)
+    rows = []
+    rows.append(np.zeros(H, np.uint16))                                   # all-zero blocks
+    rows.append(np.full(H, 0x8000, np.uint16))                           # negative zeros
+    rows.append(rng.integers(1, 0x80, H).astype(np.uint16))              # BF16 subnormals
+    rows.append((rng.integers(1, 0x80, H) | 0x8000).astype(np.uint16))   # negative subnormals
+    rows.append(np.full(H, 0x7F7F, np.uint16))                            # largest finite BF16
+    big = rng.integers(0x7F00, 0x7F80, H).astype(np.uint16)
+    big[::3] |= 0x8000
+    rows.append(big)                                                      # huge magnitudes
+    mixed = workload.float_to_bf16_bits(rng.standard_normal(H).astype(np.float32))
+    mixed[::32] = workload.float_to_bf16_bits(np.float32(1.75))[()]        # the 1.75 boundary
+    mixed[1::32] = workload.float_to_bf16_bits(np.float32(-1e-6))[()]
+    rows.append(mixed)
+    tiny_block = workload.float_to_bf16_bits((rng.standard_normal(H) * 1e-38).astype(np.float32))
+    rows.append(tiny_block)
+    x = np.stack(rows)
+    xd, _ = to_device(x, np.zeros((len(rows), 16), np.int32))
+    moe.moe_quantize(layer.handle, xd, x.shape[0])
+    codes = np.zeros(x.shape, np.uint8)
+    scales = np.zeros((x.shape[0], H // 32), np.uint8)
+    moe.moe_copy_plan(layer.handle, codes, scales, x.shape[0])
+    ref_codes, ref_scales = oracle.quantize_x(x)
+    np.testing.assert_array_equal(scales, ref_scales)
+    np.testing.assert_array_equal(codes, ref_codes)
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_group_matches_oracle_exactly(moe, name):
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    _, idsd = to_device(x, ids)
+    B = ids.shape[0]
+    moe.moe_group(layer.handle, idsd, B)
+    assert moe.moe_sync_status(layer.handle) == moe.MOE_OK
+    experts, rows = units_of(moe, layer, B)
+    ref_experts, ref_rows = oracle.group(ids, layer.experts)
+    np.testing.assert_array_equal(experts, ref_experts)
+    np.testing.assert_array_equal(rows, ref_rows)
+
+
+def oracle_pairs_for(name, weights, x, ids):
+    if name == "tp8_b256":  # every pair of 64 tokens, including the x50 outlier rows
+        outliers = np.flatnonzero(np.abs(bf16_to_float(x)).max(axis=1) > 20)
+        rng = np.random.default_rng(0)
+        tokens = np.unique(np.concatenate([outliers, rng.choice(x.shape[0], 64, replace=False)]))
+        return (tokens[:, None] * 16 + np.arange(16)).reshape(-1).astype(np.int32)
+    return np.arange(ids.size, dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_run_matches_oracle(moe, name):
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    pairs = oracle_pairs_for(name, weights, x, ids)
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=pairs, want_hidden=True)
+    check_rows(got[pairs], ref["out"], name)
+
+    # Hidden requant flips, unit row by unit row.
+    experts, rows = units_of(moe, layer, x.shape[0])
+    I = layer.inter
+    hq = np.zeros((len(experts), 8, I), np.uint8)
+    hs = np.zeros((len(experts), 8, I // 32), np.uint8)
+    moe.moe_copy_hidden(layer.handle, hq, hs, len(experts))
+    where = {int(p): i for i, p in enumerate(pairs)}
+    gpu_hq, gpu_hs, sel = [], [], []
+    for u in range(len(experts)):
+        for r in range(8):
+            p = int(rows[u, r])
+            if p >= 0 and p in where:
+                gpu_hq.append(hq[u, r])
+                gpu_hs.append(hs[u, r])
+                sel.append(where[p])
+    gpu_hq, gpu_hs, sel = np.array(gpu_hq), np.array(gpu_hs), np.array(sel)
+    code_flips = int(np.sum(gpu_hq != ref["hq"][sel]))
+    scale_flips = int(np.sum(gpu_hs != ref["hs"][sel]))
+    total = gpu_hq.size
+    print(f"[{name}] hidden requant flips: {code_flips} / {total} codes, "
+          f"{scale_flips} / {gpu_hs.size} scales")
+    assert code_flips <= max(8, total // 100), "hidden codes differ far more than rounding flips"
+
+    # FC2 alone on the GPU's own hidden codes: isolates the flips.
+    fc2 = oracle.fc2_rows(weights[2], weights[3], ids.reshape(-1)[pairs[sel]], gpu_hq, gpu_hs)
+    got_sel = bf16_to_float(got[pairs[sel]]).astype(np.float64)
+    ref_sel = bf16_to_float(fc2).astype(np.float64)
+    rel = np.linalg.norm(got_sel - ref_sel) / max(np.linalg.norm(ref_sel), 1e-300)
+    print(f"[{name}] FC2 on GPU hidden codes: rel L2 {rel:.3e}")
+    assert rel <= 2e-3
+
+
+@pytest.mark.parametrize("batch", [1, 3, 8, 9, 17, 64, 256])
+def test_ragged_batches_tiny_layer(moe, batch):
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    x = workload.make_x(batch, 256, seed=100 + batch)
+    ids = workload.make_ids(batch, 32, seed=200 + batch, dist="zipf" if batch % 2 else "uniform")
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids)
+    check_rows(got, ref["out"], f"tiny B={batch}")
+
+
+def test_partial_tiles_and_host_weights(moe):
+    """I = 96: a gate/up tile pair with 32 padded rows and a 96-K FC2 chunk;
+    H = 512; the weights are passed as host arrays."""
+    E, H, I, B = 16, 512, 96, 5
+    weights = workload.make_weights(E, H, I, seed13=7, seed2=8)
+    layer = moe.MoeLayer(weights)
+    x = workload.make_x(B, H, seed=9)
+    ids = workload.make_ids(B, E, seed=10)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids)
+    check_rows(got, ref["out"], "E=16 H=512 I=96")
+    layer.close()
+
+
+def test_repeated_expert_is_reported_and_others_kept(moe):
+    weights, x, ids = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    bad = ids.copy()
+    bad[0, 7] = bad[0, 2]  # token 0 names one expert twice: one of the two pairs is dropped
+    got, status = run_layer(moe, layer, x, bad)
+    assert status == moe.MOE_ERR_DEVICE_IDS
+    keep = np.array([p for p in range(32) if p not in (2, 7)], np.int32)
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, bad, pairs=keep)
+    check_rows(got[keep], ref["out"], "tiny with a repeated id")
+
+
+def test_run_host_equals_device_run(moe):
+    import torch
+
+    weights, x, ids = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    got, _ = run_layer(moe, layer, x, ids)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    idsh = torch.from_numpy(ids).pin_memory()
+    outh = torch.empty((x.shape[0], 16, 256), dtype=torch.int16).pin_memory()
+    moe.moe_run_host(layer.handle, xh, idsh, outh, x.shape[0])
+    np.testing.assert_array_equal(outh.numpy().view(np.uint16).reshape(-1, 256), got)
+
+
+def test_quantize_group_experts_equals_run(moe):
+    weights, x, ids = cached_inputs("tp16_b8")
+    layer = layer_for(moe, weights)
+    import torch
+
+    got, _ = run_layer(moe, layer, x, ids)
+    xd, idsd = to_device(x, ids)
+    B = x.shape[0]
+    out = torch.empty((B, 16, layer.hidden), dtype=torch.bfloat16, device="cuda:0")
+    moe.moe_quantize(layer.handle, xd, B)
+    moe.moe_group(layer.handle, idsd, B)
+    moe.moe_experts(layer.handle, out, B)
+    assert moe.moe_sync_status(layer.handle) == moe.MOE_OK
+    np.testing.assert_array_equal(
+        out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * 16, -1), got)
+
+
+def test_runs_are_deterministic(moe):
+    weights, x, ids = cached_inputs("tp8_b64")
+    layer = layer_for(moe, weights)
+    a, _ = run_layer(moe, layer, x, ids)
+    b, _ = run_layer(moe, layer, x, ids)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_out_of_range_ids_are_reported_and_skipped(moe):
+    weights, x, ids = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    bad = ids.copy()
+    bad[0, 3] = 32   # out of range
+    bad[1, 5] = -1
+    got, status = run_layer(moe, layer, x, bad)
+    assert status == moe.MOE_ERR_DEVICE_IDS
+    keep = np.array([p for p in range(32) if p not in (3, 16 + 5)], np.int32)
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=keep)
+    check_rows(got[keep], ref["out"], "tiny with bad ids")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(moe):
+    weights, x, ids = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
+    moe.moe_debug_withhold(layer.handle, 0)        # unit 0 never publishes its hidden vector
+    _, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_ERR_DEVICE_TIMEOUT
+    moe.moe_debug_withhold(layer.handle, -1)
+    moe.moe_set_timeout(layer.handle, 0)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
