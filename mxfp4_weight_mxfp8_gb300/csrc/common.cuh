@@ -8,7 +8,7 @@
 
 #include <cstdint>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
