@@ -27,12 +27,19 @@ constexpr int kActImageBytes = kUnitRows * kChunkK;      // 1024: one 128B-swizz
 constexpr int kHiddenChunkBytes = kActImageBytes + kScaleAtomBytes;  // codes + scale atom
 
 constexpr int kRingStages = 6;
-constexpr int kAccSets = 4;               // TMEM accumulator sets (2 tiles x 8 columns each)
-constexpr int kTmemColumns = 256;
-constexpr int kTmemScaleBase = kAccSets * 2 * 8;  // 64: per-slot scale columns start
-constexpr int kThreads = 256;             // 8 warps
-constexpr int kEpilogueWarp0 = 4;         // warps 4..7: the epilogue warpgroup
+constexpr int kMmaWarps = 4;              // MMA issuers: (tile 0/1) x (K-steps 0-1 / 2-3)
+constexpr int kAccSets = 4;               // TMEM accumulator sets
+constexpr int kAccSetColumns = kMmaWarps * 8;       // one N = 8 accumulator per issuer
+constexpr int kTmemScaleBase = kAccSets * kAccSetColumns;  // 128: per-slot scale columns
+constexpr int kSlotScaleColumns = kMmaWarps * 8;    // per issuer: A atom (4) + B atom (4)
+constexpr int kTmemColumns = 512;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp0 = 1;              // warps 1..4
+constexpr int kGatherWarp = 5;
+constexpr int kEpilogueWarp0 = 6;         // warps 6..9: the epilogue warpgroup
+constexpr int kThreads = 320;             // 10 warps
 constexpr int kMaxInterChunks = MOE_MAX_INTER / kChunkK;  // 4
+constexpr int kMaxGrid = 256;             // partition table capacity (CTAs)
 
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `r` (0..7) in a
 // 1024-byte, 128-byte-swizzled 8-row image.

@@ -5,25 +5,27 @@
 // fc2 output rows) and ...cutedsl.moe.experts_runtime (PersistentExperts:
 // one co-resident persistent grid, per-call workspace).
 //
-// One CTA per SM, 8 warps:
-//   warp 0  TMA producer: one 17 KB stage per ring slot (two 128-row e2m1
-//           tiles x 128 K, expanded to 32 KB of 8-bit slots in shared
-//           memory with the 128-byte swizzle, plus 1 KB of pre-tiled scales)
-//   warp 1  MMA issuer: per stage, copies the scale atoms into TMEM and
-//           issues 2 x 4 tcgen05.mma kind::mxf8f6f4.block_scale (M = 128
-//           weight rows, N = 8 unit rows, K = 32) into a TMEM accumulator set
-//   warp 2  FC1: cp.async gather of each stage's 8 MXFP8 activation rows
-//           from the plan; FC2: waits for each unit's hidden vector (bounded)
-//           and loads it into shared memory
-//   warp 3  TMEM allocation
-//   warps 4-7 epilogue: FC1 -> split-K reduction, SiLU(gate) * up, MXFP8
-//           hidden requant, publish; FC2 -> BF16 rows with 16-byte stores
+// One CTA per SM, 10 warps:
+//   warp 0     TMA producer: one 17 KB stage per ring slot (two 128-row e2m1
+//              tiles x 128 K, expanded to 32 KB of 8-bit slots in shared
+//              memory with the 128-byte swizzle, plus 1 KB of pre-tiled scales)
+//   warps 1-4  MMA issuers. Issuer i owns tile i / 2 and K-steps
+//              2 (i % 2), 2 (i % 2) + 1 of every stage: it copies its scale
+//              atoms into TMEM and issues tcgen05.mma kind::mxf8f6f4.block_scale
+//              (M = 128 weight rows, N = 8 unit rows, K = 32) into its own
+//              accumulator. One thread issues an MMA about every hundred
+//              cycles, so four issuers keep up with HBM.
+//   warp 5     FC1: cp.async gather of each stage's 8 MXFP8 activation rows;
+//              FC2: bounded wait for each unit's hidden vector, then a copy of
+//              its image into shared memory
+//   warps 6-9  epilogue: FC1 -> split-K reduction, SiLU(gate) * up, MXFP8
+//              hidden requant, publish; FC2 -> BF16 rows with 16-byte stores
 //
 // Work split: FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256
 // output rows) are cut into contiguous per-CTA ranges of near-equal bytes.
 // An FC1 item split across CTAs is reduced by the last CTA to finish its
-// piece (an atomic counter; a fixed CTA order keeps the sum deterministic).
-// Every wait is bounded by a time limit and reports MOE_ERR_DEVICE_TIMEOUT.
+// piece (an acquire-release counter; a fixed CTA order keeps the sum
+// deterministic). Every wait is bounded by a time limit.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -35,28 +37,38 @@ using namespace ptx;
 constexpr int S = kRingStages;
 constexpr int NACC = kAccSets;
 
+// Shared-memory carve-up. The swizzled operand images (weights, activation
+// and hidden codes) start on 1024-byte boundaries, every other region on a
+// 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
 struct Layout {
-  int w, act, asf, hcodes, out, bsf, hsf, bars, meta, misc, bytes;
+  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, bytes;
+  __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
   __host__ __device__ explicit Layout(int kc2) {
     int o = 0;
-    w = o;      o += S * kStageSmemWeights;
-    act = o;    o += S * kActImageBytes;
-    asf = o;    o += S * 2 * kScaleAtomBytes;
-    hcodes = o; o += 2 * kc2 * kActImageBytes;
-    out = o;    o += kUnitRows * 2 * kTileM * 2;
-    bsf = o;    o += S * kScaleAtomBytes;
-    hsf = o;    o += 2 * kc2 * kScaleAtomBytes;
-    bars = o;   o += (2 * S + 2 * NACC + 4) * 8;
-    meta = o;   o += NACC * 16;
-    misc = o;   o += 16;
-    bytes = o + 1024;  // alignment slack
+    w = o;                 o += S * kStageSmemWeights;
+    act = o = up(o, 1024); o += S * kActImageBytes;
+    hcodes = o = up(o, 1024); o += 2 * kc2 * kActImageBytes;
+    asf = o = up(o, 16);   o += S * 2 * kScaleAtomBytes;
+    out = o = up(o, 16);   o += kUnitRows * 2 * kTileM * 2;
+    bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
+    hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
+    table = o = up(o, 16); o += (kMaxGrid + 1) * 4;
+    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4) * 8;
+    meta = o = up(o, 16);  o += NACC * 16;
+    misc = o = up(o, 16);  o += 16;
+    bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
+  }
+  __host__ __device__ bool aligned() const {
+    return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
+           out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
+           meta % 16 == 0 && misc % 16 == 0;
   }
 };
 
-// Per-call split of the work over the grid; every CTA and role computes the
-// same function. FC2 jobs are cut evenly; FC1 stages fill each CTA up to an
-// equal share of all stages (both kinds stream 17 KB per stage). When the
-// shares are too small for that to stay monotone, both are cut evenly.
+// Per-call split of the work over the grid. FC2 jobs are cut evenly; FC1
+// stages fill each CTA up to an equal share of all stages (both kinds stream
+// 17 KB per stage). When the shares are too small for that to stay
+// monotone, both are cut evenly. Every CTA computes the same table.
 struct Split {
   int T1, J, KC2, G;
   long long T;
@@ -78,16 +90,17 @@ struct Split {
     long long v = static_cast<long long>(c) * T / G - static_cast<long long>(KC2) * fc2_begin(c);
     return static_cast<int>(v < 0 ? 0 : (v > T1 ? T1 : v));
   }
-  // The CTA whose FC1 range holds stage s (largest c with fc1_begin(c) <= s).
-  __device__ int cta_of(int s) const {
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (fc1_begin(mid) <= s) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  }
 };
+
+// The CTA whose FC1 range holds stage s: the largest c with start[c] <= s.
+__device__ int cta_of(const int* start, int G, int s) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start[mid] <= s) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 struct Ctx {
   const ExpertsArgs* a;
@@ -114,6 +127,12 @@ __device__ bool wait_bar(const Ctx& cx, uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ float silu_times(float gate, float up) {
   return gate / (1.0f + expf(-gate)) * up;
 }
@@ -124,6 +143,44 @@ __device__ __forceinline__ uint64_t desc_sw128(const void* p) {
 __device__ __forceinline__ uint64_t desc_scales(const void* p) {
   return smem_desc(smem_addr(p), 128, 128, 0);
 }
+
+// FC1 stage cursor: stage s = (item * KC1 + c), item = u * P1 + p.
+struct Fc1Cursor {
+  int s, item, c, u, p;
+  __device__ Fc1Cursor(int s0, const Geometry& g) : s(s0) {
+    item = s0 / g.KC1;
+    c = s0 - item * g.KC1;
+    u = item / g.P1;
+    p = item - u * g.P1;
+  }
+  __device__ void next(const Geometry& g) {
+    ++s;
+    if (++c == g.KC1) {
+      c = 0;
+      ++item;
+      if (++p == g.P1) {
+        p = 0;
+        ++u;
+      }
+    }
+  }
+};
+
+// FC2 job cursor: job j = u * NQ + q.
+struct Fc2Cursor {
+  int j, u, q;
+  __device__ Fc2Cursor(int j0, const Geometry& g) : j(j0) {
+    u = j0 / g.NQ;
+    q = j0 - u * g.NQ;
+  }
+  __device__ void next(const Geometry& g) {
+    ++j;
+    if (++q == g.NQ) {
+      q = 0;
+      ++u;
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ ExpertsArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -138,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   uint16_t* OUT = reinterpret_cast<uint16_t*>(sm + L.out);
   uint8_t* BSF = sm + L.bsf;
   uint8_t* HSF = sm + L.hsf;
+  int* start = reinterpret_cast<int*>(sm + L.table);  // FC1 range start of every CTA, [G + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + S;
   uint64_t* accfull = empty + S;
@@ -153,16 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 32);  // producer (with bytes) + 32 gather lanes or a stand-in
-      mbar_init(&empty[s], 1);      // MMA commit
+      mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
+      mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
     }
     for (int i = 0; i < NACC; ++i) {
-      mbar_init(&accfull[i], 2);    // MMA commit + metadata arrival
-      mbar_init(&accempty[i], 4);   // one per epilogue warp
+      mbar_init(&accfull[i], kMmaWarps + 1);  // issuer commits + the metadata arrival
+      mbar_init(&accempty[i], 4);             // one per epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&hfull[b], 1);
-      mbar_init(&hempty[b], 1);
+      mbar_init(&hempty[b], kMmaWarps);
     }
     misc[1] = 0;
     misc[2] = 0;
@@ -171,32 +229,32 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   }
   for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
-  if (warp == 3) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(&misc[0], kTmemColumns);
     tmem_relinquish();
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = misc[0];
 
   // The plan, unit table and cleared counters of the preceding prep grid.
   grid_dependency_wait();
   const int units = *a.unit_count;
   const Split sp(units, g, G);
-  const int f0 = sp.fc1_begin(cta), f1 = sp.fc1_begin(cta + 1);
+  for (int c = tid; c <= G; c += kThreads) start[c] = sp.fc1_begin(c);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const int f0 = start[cta], f1 = start[cta + 1];
   const int j0 = sp.fc2_begin(cta), j1 = sp.fc2_begin(cta + 1);
-  const int fc1_base = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
+  const int fc1_stages = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      int n = 0;
+      int n = 0, slot = 0;
+      uint32_t phase = 0;
       bool ok = true;
       auto issue = [&](int stage, bool stand_in) {
-        const int slot = n % S;
-        const uint32_t phase = (n / S) & 1;
         if (n >= S && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
         mbar_arrive_expect_tx(&full[slot], kStageWeightBytes + 2 * kScaleAtomBytes);
         if (stand_in) mbar_arrive_count(&full[slot], 32);
@@ -205,19 +263,22 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                   a.stages + static_cast<size_t>(stage) * kStageBytes + kStageWeightBytes,
                   2 * kScaleAtomBytes, &full[slot], policy);
         ++n;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
         return true;
       };
       int cu = -1, e = 0;
-      for (int s = f0; s < f1 && ok; ++s) {
-        const int item = s / g.KC1, c = s % g.KC1, u = item / g.P1, p = item % g.P1;
-        if (u != cu) { e = a.unit_expert[u]; cu = u; }
-        ok = issue(e * g.SPE + p * g.KC1 + c, false);
+      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
+        if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+        ok = issue(e * g.SPE + cur.p * g.KC1 + cur.c, false);
       }
       cu = -1;
-      for (int j = j0; j < j1 && ok; ++j) {
-        const int u = j / g.NQ, q = j % g.NQ;
-        if (u != cu) { e = a.unit_expert[u]; cu = u; }
-        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(e * g.SPE + fc1_base + q * g.KC2 + c, true);
+      for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
+        if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+        const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
+        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
       }
       if (ok) {
         // Drain: every issued stage consumed and released before exit.
@@ -227,118 +288,123 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         __nanosleep(50000);  // in-flight copies land before the CTA exits
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
+    // --------------------------------------------------------- MMA issuers
     if (lane == 0) {
-      int n = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_stage = 0;
+      const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
+      const bool lead = issuer == 0;  // writes the accumulator metadata
+      int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
       auto acquire = [&](int set) {
         return k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
       };
-      for (int s = f0; s < f1 && ok; ++s) {
-        const int item = s / g.KC1, c = s % g.KC1;
-        const bool first = (s == f0) || (c == 0), last = (s == f1 - 1) || (c == g.KC1 - 1);
+      auto advance = [&]() {
+        ++n;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+      };
+      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
+        const bool first = (cur.s == f0) || (cur.c == 0);
+        const bool last = (cur.s == f1 - 1) || (cur.c == g.KC1 - 1);
         const int set = k % NACC;
         if (first) {
           if (!(ok = acquire(set))) break;
-          first_stage = s;
+          first_stage = cur.s;
         }
-        const int slot = n % S;
-        if (!(ok = wait_bar(cx, &full[slot], (n / S) & 1))) break;
+        if (!(ok = wait_bar(cx, &full[slot], phase))) break;
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
         tc_fence_after_sync();
-        const uint32_t sf = tmem + kTmemScaleBase + slot * 16;
-        const uint8_t* asf = ASF + slot * 2 * kScaleAtomBytes;
-        tc_copy_scales(sf + 0, desc_scales(asf));
-        tc_copy_scales(sf + 4, desc_scales(asf + kScaleAtomBytes));
-        tc_copy_scales(sf + 8, desc_scales(BSF + slot * kScaleAtomBytes));
-        const uint8_t* w = W + slot * kStageSmemWeights;
+        const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+        tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+        tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
+        const uint8_t* w = W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2);
         const uint8_t* x = ACT + slot * kActImageBytes;
+        const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_mxf8f6f4(tmem + set * 16 + t * 8, desc_sw128(w + t * (kStageSmemWeights / 2) + kk * 32),
-                            desc_sw128(x + kk * 32), mma_idesc(kk), sf + 4 * t, sf + 8,
-                            (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < 2; ++kk)
+          tc_mma_mxf8f6f4(d, desc_sw128(w + (k0 + kk) * 32), desc_sw128(x + (k0 + kk) * 32),
+                          mma_idesc(k0 + kk), sf, sf + 4, (first && kk == 0) ? 0u : 1u);
         tc_commit(&empty[slot]);
-        ++n;
+        advance();
         if (last) {
-          meta[set] = make_int4(0, item, first_stage, s);
+          if (lead) meta[set] = make_int4(0, cur.item, first_stage, cur.s);
           tc_commit(&accfull[set]);
-          mbar_arrive(&accfull[set]);
+          if (lead) mbar_arrive(&accfull[set]);
           ++k;
         }
       }
-      for (int j = j0; j < j1 && ok; ++j) {
-        const int u = j / g.NQ;
-        if (u != cu) {
+      for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
+        if (cur.u != cu) {
           if (cu >= 0) tc_commit(&hempty[hb]);
           ++ordinal;
           hb = ordinal & 1;
           if (!(ok = wait_bar(cx, &hfull[hb], (ordinal >> 1) & 1))) break;
           tc_fence_after_sync();
-          cu = u;
+          cu = cur.u;
         }
         const int set = k % NACC;
         if (!(ok = acquire(set))) break;
+        bool started = false;
         for (int c = 0; c < g.KC2 && ok; ++c) {
-          const int slot = n % S;
-          if (!(ok = wait_bar(cx, &full[slot], (n / S) & 1))) break;
+          if (!(ok = wait_bar(cx, &full[slot], phase))) break;
           tc_fence_after_sync();
-          const uint32_t sf = tmem + kTmemScaleBase + slot * 16;
-          const uint8_t* asf = ASF + slot * 2 * kScaleAtomBytes;
-          tc_copy_scales(sf + 0, desc_scales(asf));
-          tc_copy_scales(sf + 4, desc_scales(asf + kScaleAtomBytes));
-          tc_copy_scales(sf + 8, desc_scales(HSF + (hb * g.KC2 + c) * kScaleAtomBytes));
-          const uint8_t* w = W + slot * kStageSmemWeights;
-          const uint8_t* h = HC + (hb * g.KC2 + c) * kActImageBytes;
           const int ksteps = min(4, (g.I - c * kChunkK) / kBlock);
-          for (int t = 0; t < 2; ++t)
-            for (int kk = 0; kk < ksteps; ++kk)
-              tc_mma_mxf8f6f4(tmem + set * 16 + t * 8,
-                              desc_sw128(w + t * (kStageSmemWeights / 2) + kk * 32),
-                              desc_sw128(h + kk * 32), mma_idesc(kk), sf + 4 * t, sf + 8,
-                              (c == 0 && kk == 0) ? 0u : 1u);
+          if (k0 < ksteps) {
+            const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+            tc_copy_scales(sf + 4, desc_scales(HSF + (hb * g.KC2 + c) * kScaleAtomBytes));
+            const uint8_t* w = W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2);
+            const uint8_t* h = HC + (hb * g.KC2 + c) * kActImageBytes;
+            const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+            for (int kk = k0; kk < k0 + 2 && kk < ksteps; ++kk) {
+              tc_mma_mxf8f6f4(d, desc_sw128(w + kk * 32), desc_sw128(h + kk * 32), mma_idesc(kk),
+                              sf, sf + 4, started ? 1u : 0u);
+              started = true;
+            }
+          }
           tc_commit(&empty[slot]);
-          ++n;
+          advance();
         }
         if (!ok) break;
-        meta[set] = make_int4(1, j, 0, 0);
+        if (lead) meta[set] = make_int4(1, cur.j, 0, 0);
         tc_commit(&accfull[set]);
-        mbar_arrive(&accfull[set]);
+        if (lead) mbar_arrive(&accfull[set]);
         ++k;
       }
       // End marker for the epilogue (also after a timeout, so it exits).
-      const int set = k % NACC;
-      if (k >= NACC) wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
-      meta[set] = make_int4(2, 0, 0, 0);
-      mbar_arrive_count(&accfull[set], 2);
+      if (lead) {
+        const int set = k % NACC;
+        if (k >= NACC) wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
+        meta[set] = make_int4(2, 0, 0, 0);
+        mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+      }
     }
-  } else if (warp == 2) {
+  } else if (warp == kGatherWarp) {
     // ------------------------------- activation gather (FC1), hidden loader (FC2)
-    int n = 0, cu = -1;
+    int n = 0, slot = 0, cu = -1;
+    uint32_t phase = 0;
     int tok_code = -1, tok_scale = -1;
     bool ok = true;
-    for (int s = f0; s < f1 && ok; ++s) {
-      const int item = s / g.KC1, c = s % g.KC1, u = item / g.P1;
-      if (u != cu) {
-        const int pc = a.unit_rows[u * kUnitRows + (lane >> 2)];
-        const int ps = a.unit_rows[u * kUnitRows + (lane & 7)];
+    for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
+      if (cur.u != cu) {
+        const int pc = a.unit_rows[cur.u * kUnitRows + (lane >> 2)];
+        const int ps = a.unit_rows[cur.u * kUnitRows + (lane & 7)];
         tok_code = pc >= 0 ? (pc >> 4) : -1;
         tok_scale = ps >= 0 ? (ps >> 4) : -1;
-        cu = u;
+        cu = cur.u;
       }
-      const int slot = n % S;
       if (n >= S) {
         bool freed = true;
-        if (lane == 0) freed = wait_bar(cx, &empty[slot], ((n / S) & 1) ^ 1);
+        if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
       const int r = lane >> 2, piece = lane & 3;
       uint8_t* img = ACT + slot * kActImageBytes;
       const uint8_t* row = a.plan_codes + static_cast<size_t>(tok_code < 0 ? 0 : tok_code) * g.H +
-                           c * kChunkK;
+                           cur.c * kChunkK;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c16 = piece * 2 + h;
@@ -347,20 +413,23 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       if (lane < 8) {
         const uint8_t* src = a.plan_scales +
                              static_cast<size_t>(tok_scale < 0 ? 0 : tok_scale) * (g.H / kBlock) +
-                             c * (kChunkK / kBlock);
+                             cur.c * (kChunkK / kBlock);
         cp_async_4(BSF + slot * kScaleAtomBytes + lane * 16, src, tok_scale < 0 ? 0u : 4u);
       }
       cp_async_arrive_noinc(&full[slot]);
       ++n;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     // Hidden loader: one image per FC2 unit, double-buffered.
     int ordinal = -1;
     cu = -1;
-    for (int j = j0; j < j1 && ok; ++j) {
-      const int u = j / g.NQ;
-      if (u == cu) continue;
-      cu = u;
+    for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
+      if (cur.u == cu) continue;
+      cu = cur.u;
       ++ordinal;
       const int b = ordinal & 1;
       if (ordinal >= 2) {
@@ -369,17 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
       // Wait (bounded) for every K chunk of the unit's hidden vector.
-      const uint64_t start = global_timer_ns();
+      const uint64_t t_start = global_timer_ns();
       for (int c = 0; c < g.KC2; ++c) {
-        const uint32_t* flag = a.hidden_flags + u * g.KC2 + c;
+        const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + c;
         for (uint32_t i = 0; load_acquire_gpu(flag) == 0; ++i) {
-          if ((i & 15u) == 15u && global_timer_ns() - start > a.timeout_ns) {
+          if ((i & 15u) == 15u && global_timer_ns() - t_start > a.timeout_ns) {
             report(a.status, MOE_ERR_DEVICE_TIMEOUT);
             break;  // proceed with whatever the image holds
           }
         }
       }
-      const uint8_t* src = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
+      const uint8_t* src = a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes;
       uint8_t* codes = HC + b * g.KC2 * kActImageBytes;
       uint8_t* scales = HSF + b * g.KC2 * kScaleAtomBytes;
       for (int i = lane; i < g.KC2 * kActImageBytes / 16; i += 32)
@@ -392,9 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp - kEpilogueWarp0;  // TMEM lane quarter
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int et = tid - kEpilogueWarp0 * 32;
-    const int m = wq * 32 + lane;          // tile row of this thread
+    const int m = q * 32 + lane;             // tile row of this thread
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+    const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     int k = 0, out_unit = -1, out_pair = -1;
     for (;;) {
       const int set = k % NACC;
@@ -402,38 +473,47 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       tc_fence_after_sync();
       const int4 md = meta[set];
       if (md.x == 2) break;
-      float v0[8], v1[8];
-      tmem_load_8(tmem + (static_cast<uint32_t>(wq * 32) << 16) + set * 16, v0);
-      tmem_load_8(tmem + (static_cast<uint32_t>(wq * 32) << 16) + set * 16 + 8, v1);
+      float v0[8], v1[8], x0[8], x1[8];
+      const uint32_t base = tmem + lanes + set * kAccSetColumns;
+      tmem_load_8(base + 0, v0);
+      tmem_load_8(base + 8, x0);
+      tmem_load_8(base + 16, v1);
+      tmem_load_8(base + 24, x1);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[set]);
       ++k;
+      if (md.x == 0 || fc2_upper_half) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          v0[t] += x0[t];
+          v1[t] += x1[t];
+        }
+      }
       if (md.x == 0) {
         // ---- FC1 piece: gate = v0, up = v1 for rows 128p + m.
-        const int item = md.y, u = item / g.P1, p = item % g.P1;
+        const int item = md.y, u = item / g.P1, p = item - u * g.P1;
         const uint4 rw = *reinterpret_cast<const uint4*>(a.unit_rows + u * kUnitRows);
         const int16_t* rows = reinterpret_cast<const int16_t*>(&rw);
         int valid = 0;
         while (valid < kUnitRows && rows[valid] >= 0) ++valid;
         const bool whole = (md.z % g.KC1 == 0) && (md.w % g.KC1 == g.KC1 - 1);
         if (!whole) {
-          const int slot = (f0 >= item * g.KC1) ? 0 : 1;
+          const int item_first = item * g.KC1;
+          const int slot = (f0 >= item_first) ? 0 : 1;
           float* dst = a.partials + static_cast<size_t>(cta * 2 + slot) * 2 * kUnitRows * kTileM;
           for (int t = 0; t < valid; ++t) {
             dst[t * kTileM + m] = v0[t];
             dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
           }
           epilogue_sync();
+          const int c_lo = cta_of(start, G, item_first);
+          const int c_hi = cta_of(start, G, item_first + g.KC1 - 1);
           if (et == 0) {
-            __threadfence();
-            const uint32_t before = atomicAdd(&a.item_counters[item], 1u);
-            const int c_lo = sp.cta_of(item * g.KC1), c_hi = sp.cta_of(item * g.KC1 + g.KC1 - 1);
             uint32_t pieces = 0;
-            for (int c = c_lo; c <= c_hi; ++c) pieces += sp.fc1_begin(c) < sp.fc1_begin(c + 1);
-            const bool last = before + 1 == pieces;
-            if (last) __threadfence();
-            misc[2] = last ? 1u : 0u;
+            for (int c = c_lo; c <= c_hi; ++c) pieces += start[c] < start[c + 1];
+            const uint32_t before = atomic_add_acq_rel_gpu(&a.item_counters[item], 1u);
+            misc[2] = (before + 1 == pieces) ? 1u : 0u;
           }
           epilogue_sync();
           const bool last = misc[2] != 0;
@@ -443,10 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           float gs[8], us[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) gs[t] = us[t] = 0.f;
-          const int c_lo = sp.cta_of(item * g.KC1), c_hi = sp.cta_of(item * g.KC1 + g.KC1 - 1);
           for (int c = c_lo; c <= c_hi; ++c) {
-            const int b0 = sp.fc1_begin(c);
-            if (b0 == sp.fc1_begin(c + 1)) continue;
+            const int b0 = start[c];
+            if (b0 == start[c + 1]) continue;
             if (c == cta) {
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
@@ -454,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 us[t] += v1[t];
               }
             } else {
-              const int sl = (b0 >= item * g.KC1) ? 0 : 1;
+              const int sl = (b0 >= item_first) ? 0 : 1;
               const float* src = a.partials + static_cast<size_t>(c * 2 + sl) * 2 * kUnitRows * kTileM;
               for (int t = 0; t < valid; ++t) {
                 gs[t] += __ldcg(src + t * kTileM + m);
@@ -469,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           }
         }
         // SiLU(gate) * up, MXFP8 per 32 hidden values (= this warp's 32 rows).
-        if (p * kTileM + wq * 32 < g.I) {
+        if (p * kTileM + q * 32 < g.I) {
           uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
@@ -480,18 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             const int E = mx_exponent(amax, g.floor_rule != 0);
             img[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
             if (lane == 0)
-              img[g.KC2 * kActImageBytes + p * kScaleAtomBytes + scale_atom(t, wq)] =
+              img[g.KC2 * kActImageBytes + p * kScaleAtomBytes + scale_atom(t, q)] =
                   static_cast<uint8_t>(E + 127);
           }
         }
         epilogue_sync();
-        if (et == 0) {
-          __threadfence();
-          if (u != a.withhold_unit) store_release_gpu(&a.hidden_flags[u * g.KC2 + p], 1u);
-        }
+        if (et == 0 && u != a.withhold_unit)
+          store_release_gpu(&a.hidden_flags[u * g.KC2 + p], 1u);
       } else {
-        // ---- FC2 job: rows 256q + m (v0) and 256q + 128 + m (v1) -> BF16.
-        const int j = md.y, u = j / g.NQ, q = j % g.NQ;
+        // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
+        const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         if (u != out_unit) {
           out_pair = a.unit_rows[u * kUnitRows + (et >> 4)];
           out_unit = u;
@@ -504,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         epilogue_sync();
         if (out_pair >= 0) {
           const int r = et >> 4, ch = et & 15;
-          uint16_t* dst = a.out + static_cast<size_t>(out_pair) * g.H + q * 2 * kTileM;
+          uint16_t* dst = a.out + static_cast<size_t>(out_pair) * g.H + qq * 2 * kTileM;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int chunk = ch + 16 * h;
@@ -520,12 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 3) tmem_dealloc(tmem, kTmemColumns);
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
 }
 
 }  // namespace
 
 int experts_smem_bytes(const Geometry& g) { return Layout(g.KC2).bytes; }
+
+bool experts_layout_aligned(const Geometry& g) { return Layout(g.KC2).aligned(); }
 
 cudaError_t experts_configure(const Geometry& g) {
   // The attribute belongs to the kernel, not to a handle: allow the largest

@@ -49,6 +49,7 @@ struct ExpertsArgs {
 };
 
 int experts_smem_bytes(const Geometry& g);
+bool experts_layout_aligned(const Geometry& g);
 cudaError_t experts_configure(const Geometry& g);
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);

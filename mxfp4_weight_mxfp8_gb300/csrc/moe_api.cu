@@ -124,6 +124,10 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   MOE_CUDA(cudaGetDevice(&h->device));
   MOE_CUDA(cudaGetDeviceProperties(&prop, h->device));
   h->smem_bytes = moe::experts_smem_bytes(g);
+  if (!moe::experts_layout_aligned(g)) {
+    std::snprintf(g_detail, sizeof g_detail, "internal: misaligned shared-memory layout");
+    return MOE_ERR_UNSUPPORTED;
+  }
   if (prop.major != 10 ||
       static_cast<int>(prop.sharedMemPerBlockOptin) < moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER))) {
     std::snprintf(g_detail, sizeof g_detail, "needs an sm_100-family GPU with %d B shared memory",
@@ -138,7 +142,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     std::snprintf(g_detail, sizeof g_detail, "experts kernel does not fit on an SM");
     return MOE_ERR_UNSUPPORTED;
   }
-  h->grid = h->sms;  // one co-resident CTA per SM
+  h->grid = h->sms < moe::kMaxGrid ? h->sms : moe::kMaxGrid;  // one co-resident CTA per SM
 
   // Weights: one 17 KB block per stage.
   h->stage_bytes = static_cast<size_t>(g.E) * g.SPE * moe::kStageBytes;
