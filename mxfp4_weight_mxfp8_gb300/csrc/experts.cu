@@ -21,8 +21,11 @@
 //   warps 6-9  epilogue: FC1 -> split-K reduction, SiLU(gate) * up, MXFP8
 //              hidden requant, publish; FC2 -> BF16 rows with 16-byte stores
 //
-// Work split: FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256
-// output rows) are cut into contiguous per-CTA ranges of near-equal bytes.
+// Work split: the units are cut into two halves, A and B. Within each half,
+// FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256 output rows)
+// are cut into contiguous per-CTA ranges of near-equal bytes, and every CTA
+// runs FC1(A), FC1(B), FC2(A), FC2(B): half A's hidden vectors are reduced
+// and published while half B's FC1 weights stream.
 // An FC1 item split across CTAs is reduced by the last CTA to finish its
 // piece (an acquire-release counter; a fixed CTA order keeps the sum
 // deterministic). Every wait is bounded by a time limit.
@@ -36,12 +39,14 @@ using namespace ptx;
 
 constexpr int S = kRingStages;
 constexpr int NACC = kAccSets;
+constexpr int kHalvesFrom = 256;  // more units than this: split them into halves A and B
+constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memory
 
 // Shared-memory carve-up. The swizzled operand images (weights, activation
 // and hidden codes) start on 1024-byte boundaries, every other region on a
 // 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
 struct Layout {
-  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, bytes;
+  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, bytes;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
   __host__ __device__ explicit Layout(int kc2) {
     int o = 0;
@@ -52,16 +57,17 @@ struct Layout {
     out = o = up(o, 16);   o += kUnitRows * 2 * kTileM * 2;
     bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
     hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
-    table = o = up(o, 16); o += (kMaxGrid + 1) * 4;
+    table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
     bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4) * 8;
     meta = o = up(o, 16);  o += NACC * 16;
     misc = o = up(o, 16);  o += 16;
+    rows = o = up(o, 16);  o += kRowCache * (4 + kUnitRows * 2);
     bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }
   __host__ __device__ bool aligned() const {
     return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
            out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
-           meta % 16 == 0 && misc % 16 == 0;
+           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0;
   }
 };
 
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   uint16_t* OUT = reinterpret_cast<uint16_t*>(sm + L.out);
   uint8_t* BSF = sm + L.bsf;
   uint8_t* HSF = sm + L.hsf;
-  int* start = reinterpret_cast<int*>(sm + L.table);  // FC1 range start of every CTA, [G + 1]
+  int* start = reinterpret_cast<int*>(sm + L.table);  // FC1 range starts, [2 halves][G + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + S;
   uint64_t* accfull = empty + S;
@@ -237,14 +243,28 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   // The plan, unit table and cleared counters of the preceding prep grid.
   grid_dependency_wait();
   const int units = *a.unit_count;
-  const Split sp(units, g, G);
-  for (int c = tid; c <= G; c += kThreads) start[c] = sp.fc1_begin(c);
+  // Half A = units [0, units_a). Small calls keep one half: their chain of
+  // reductions is latency-bound and more pieces per item only lengthen it.
+  const int units_a = units > kHalvesFrom ? (units + 1) / 2 : units;
+  const Split half[2] = {Split(units_a, g, G), Split(units - units_a, g, G)};
+  const int stage_base[2] = {0, units_a * g.P1 * g.KC1};
+  const int job_base[2] = {0, units_a * g.NQ};
+  const int items_a = units_a * g.P1;
+  for (int c = tid; c <= G; c += kThreads) {
+    start[c] = half[0].fc1_begin(c);
+    start[G + 1 + c] = stage_base[1] + half[1].fc1_begin(c);
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = misc[0];
-  const int f0 = start[cta], f1 = start[cta + 1];
-  const int j0 = sp.fc2_begin(cta), j1 = sp.fc2_begin(cta + 1);
+  int f0[2], f1[2], j0[2], j1[2];
+  for (int h = 0; h < 2; ++h) {
+    f0[h] = start[h * (G + 1) + cta];
+    f1[h] = start[h * (G + 1) + cta + 1];
+    j0[h] = job_base[h] + half[h].fc2_begin(cta);
+    j1[h] = job_base[h] + half[h].fc2_begin(cta + 1);
+  }
   const int fc1_stages = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
 
   if (warp == kProducerWarp) {
@@ -270,16 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         return true;
       };
       int cu = -1, e = 0;
-      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
-        if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
-        ok = issue(e * g.SPE + cur.p * g.KC1 + cur.c, false);
-      }
+      for (int h = 0; h < 2; ++h)
+        for (Fc1Cursor cur(f0[h], g); cur.s < f1[h] && ok; cur.next(g)) {
+          if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+          ok = issue(e * g.SPE + cur.p * g.KC1 + cur.c, false);
+        }
       cu = -1;
-      for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
-        if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
-        const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
-        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
-      }
+      for (int h = 0; h < 2; ++h)
+        for (Fc2Cursor cur(j0[h], g); cur.j < j1[h] && ok; cur.next(g)) {
+          if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+          const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
+          for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
+        }
       if (ok) {
         // Drain: every issued stage consumed and released before exit.
         for (int k = (n > S ? n - S : 0); k < n; ++k)
@@ -306,9 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           phase ^= 1;
         }
       };
-      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
-        const bool first = (cur.s == f0) || (cur.c == 0);
-        const bool last = (cur.s == f1 - 1) || (cur.c == g.KC1 - 1);
+      for (int hf = 0; hf < 2; ++hf)
+      for (Fc1Cursor cur(f0[hf], g); cur.s < f1[hf] && ok; cur.next(g)) {
+        const bool first = (cur.s == f0[hf]) || (cur.c == 0);
+        const bool last = (cur.s == f1[hf] - 1) || (cur.c == g.KC1 - 1);
         const int set = k % NACC;
         if (first) {
           if (!(ok = acquire(set))) break;
@@ -336,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           ++k;
         }
       }
-      for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
+      for (int hf = 0; hf < 2; ++hf)
+      for (Fc2Cursor cur(j0[hf], g); cur.j < j1[hf] && ok; cur.next(g)) {
         if (cur.u != cu) {
           if (cu >= 0) tc_commit(&hempty[hb]);
           ++ordinal;
@@ -388,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     uint32_t phase = 0;
     int tok_code = -1, tok_scale = -1;
     bool ok = true;
-    for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
+    for (int hf = 0; hf < 2; ++hf)
+    for (Fc1Cursor cur(f0[hf], g); cur.s < f1[hf] && ok; cur.next(g)) {
       if (cur.u != cu) {
         const int pc = a.unit_rows[cur.u * kUnitRows + (lane >> 2)];
         const int ps = a.unit_rows[cur.u * kUnitRows + (lane & 7)];
@@ -427,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // Hidden loader: one image per FC2 unit, double-buffered.
     int ordinal = -1;
     cu = -1;
-    for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
+    for (int hf = 0; hf < 2; ++hf)
+    for (Fc2Cursor cur(j0[hf], g); cur.j < j1[hf] && ok; cur.next(g)) {
       if (cur.u == cu) continue;
       cu = cur.u;
       ++ordinal;
@@ -466,7 +492,33 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     const int m = q * 32 + lane;             // tile row of this thread
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
-    int k = 0, out_unit = -1, out_pair = -1;
+    // Unit rows of this CTA's first units, fetched while the first stages stream.
+    int* cache_unit = reinterpret_cast<int*>(sm + L.rows);
+    int16_t* cache_rows = reinterpret_cast<int16_t*>(cache_unit + kRowCache);
+    {
+      const int per_unit_fc1 = g.P1 * g.KC1;
+      int lo = units, hi = -1;
+      for (int h = 0; h < 2; ++h) {
+        if (f0[h] < f1[h]) { lo = min(lo, f0[h] / per_unit_fc1); hi = max(hi, (f1[h] - 1) / per_unit_fc1); }
+        if (j0[h] < j1[h]) { lo = min(lo, j0[h] / g.NQ); hi = max(hi, (j1[h] - 1) / g.NQ); }
+      }
+      if (et < kRowCache) {
+        const int u = lo + et;
+        cache_unit[et] = (u <= hi) ? u : -1;
+      }
+      if (et < kRowCache * kUnitRows) {
+        const int u = lo + et / kUnitRows;
+        cache_rows[et] = (u <= hi) ? a.unit_rows[u * kUnitRows + et % kUnitRows] : -1;
+      }
+      epilogue_sync();
+    }
+    auto unit_row = [&](int u, int r) -> int {
+      const int i = u - cache_unit[0];
+      if (cache_unit[0] >= 0 && i >= 0 && i < kRowCache && cache_unit[i] == u)
+        return cache_rows[i * kUnitRows + r];
+      return a.unit_rows[u * kUnitRows + r];
+    };
+    int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;
     for (;;) {
       const int set = k % NACC;
       if (!wait_bar(cx, &accfull[set], (k / NACC) & 1)) break;
@@ -474,11 +526,22 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       const int4 md = meta[set];
       if (md.x == 2) break;
       float v0[8], v1[8], x0[8], x1[8];
-      const uint32_t base = tmem + lanes + set * kAccSetColumns;
-      tmem_load_8(base + 0, v0);
-      tmem_load_8(base + 8, x0);
-      tmem_load_8(base + 16, v1);
-      tmem_load_8(base + 24, x1);
+      {
+        uint32_t r0[8], r1[8], r2[8], r3[8];
+        const uint32_t base = tmem + lanes + set * kAccSetColumns;
+        tmem_load_8_async(base + 0, r0);
+        tmem_load_8_async(base + 8, r1);
+        tmem_load_8_async(base + 16, r2);
+        tmem_load_8_async(base + 24, r3);
+        tmem_wait_loads();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          v0[t] = __uint_as_float(r0[t]);
+          x0[t] = __uint_as_float(r1[t]);
+          v1[t] = __uint_as_float(r2[t]);
+          x1[t] = __uint_as_float(r3[t]);
+        }
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[set]);
@@ -493,25 +556,25 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       if (md.x == 0) {
         // ---- FC1 piece: gate = v0, up = v1 for rows 128p + m.
         const int item = md.y, u = item / g.P1, p = item - u * g.P1;
-        const uint4 rw = *reinterpret_cast<const uint4*>(a.unit_rows + u * kUnitRows);
-        const int16_t* rows = reinterpret_cast<const int16_t*>(&rw);
         int valid = 0;
-        while (valid < kUnitRows && rows[valid] >= 0) ++valid;
+        while (valid < kUnitRows && unit_row(u, valid) >= 0) ++valid;
         const bool whole = (md.z % g.KC1 == 0) && (md.w % g.KC1 == g.KC1 - 1);
         if (!whole) {
           const int item_first = item * g.KC1;
-          const int slot = (f0 >= item_first) ? 0 : 1;
-          float* dst = a.partials + static_cast<size_t>(cta * 2 + slot) * 2 * kUnitRows * kTileM;
+          const int hf = item < items_a ? 0 : 1;
+          const int* st = start + hf * (G + 1);
+          const int slot = (f0[hf] >= item_first) ? 0 : 1;
+          float* dst = a.partials + static_cast<size_t>((cta * 2 + hf) * 2 + slot) * 2 * kUnitRows * kTileM;
           for (int t = 0; t < valid; ++t) {
             dst[t * kTileM + m] = v0[t];
             dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
           }
           epilogue_sync();
-          const int c_lo = cta_of(start, G, item_first);
-          const int c_hi = cta_of(start, G, item_first + g.KC1 - 1);
+          const int c_lo = cta_of(st, G, item_first);
+          const int c_hi = cta_of(st, G, item_first + g.KC1 - 1);
           if (et == 0) {
             uint32_t pieces = 0;
-            for (int c = c_lo; c <= c_hi; ++c) pieces += start[c] < start[c + 1];
+            for (int c = c_lo; c <= c_hi; ++c) pieces += st[c] < st[c + 1];
             const uint32_t before = atomic_add_acq_rel_gpu(&a.item_counters[item], 1u);
             misc[2] = (before + 1 == pieces) ? 1u : 0u;
           }
@@ -524,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 #pragma unroll
           for (int t = 0; t < 8; ++t) gs[t] = us[t] = 0.f;
           for (int c = c_lo; c <= c_hi; ++c) {
-            const int b0 = start[c];
-            if (b0 == start[c + 1]) continue;
+            const int b0 = st[c];
+            if (b0 == st[c + 1]) continue;
             if (c == cta) {
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
@@ -534,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
               }
             } else {
               const int sl = (b0 >= item_first) ? 0 : 1;
-              const float* src = a.partials + static_cast<size_t>(c * 2 + sl) * 2 * kUnitRows * kTileM;
+              const float* src = a.partials + static_cast<size_t>((c * 2 + hf) * 2 + sl) * 2 * kUnitRows * kTileM;
               for (int t = 0; t < valid; ++t) {
                 gs[t] += __ldcg(src + t * kTileM + m);
                 us[t] += __ldcg(src + kUnitRows * kTileM + t * kTileM + m);
@@ -570,8 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         if (u != out_unit) {
-          out_pair = a.unit_rows[u * kUnitRows + (et >> 4)];
+          out_pair = unit_row(u, et >> 4);
+          out_valid = 0;
+          while (out_valid < kUnitRows && unit_row(u, out_valid) >= 0) ++out_valid;
           out_unit = u;
+        }
+        if (out_valid <= 2) {
+          // Few rows: each thread stores its two values of each row directly
+          // (a warp writes 64 contiguous bytes per row and tile).
+          for (int t = 0; t < out_valid; ++t) {
+            uint16_t* dst = a.out + static_cast<size_t>(unit_row(u, t)) * g.H + qq * 2 * kTileM;
+            dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
+            dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
+          }
+          continue;
         }
 #pragma unroll
         for (int t = 0; t < 8; ++t) {

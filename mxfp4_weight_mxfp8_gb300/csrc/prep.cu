@@ -19,11 +19,11 @@ namespace moe {
 namespace {
 
 constexpr int kPrepThreads = 256;
+constexpr int kQuantChunks = 4;  // 256-chunk runs per quantizer block
 
-__device__ void quantize_role(const PrepArgs& a, int block) {
+__device__ void quantize_chunk(const PrepArgs& a, int chunk) {
   const int per_row = a.H / 8;  // 8-value chunks per token
   const int total = a.B * per_row;
-  const int chunk = block * kPrepThreads + threadIdx.x;
   const bool active = chunk < total;  // uniform across each 4-lane block (total % 4 == 0)
   const int token = active ? chunk / per_row : 0;
   const int c = active ? chunk % per_row : 0;
@@ -57,6 +57,12 @@ __device__ void quantize_role(const PrepArgs& a, int block) {
         static_cast<uint8_t>(E + 127);
 }
 
+// Quantizer blocks own kQuantChunks consecutive runs of 256 chunks each.
+__device__ void quantize_role(const PrepArgs& a, int block) {
+  for (int r = 0; r < kQuantChunks; ++r)
+    quantize_chunk(a, (block * kQuantChunks + r) * kPrepThreads + threadIdx.x);
+}
+
 __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   const int E = a.E, pairs = a.B * kTopK, words = (a.B + 31) / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -67,20 +73,25 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   int32_t* grand = warp_total + 8;                              // [1]
 
   for (int i = tid; i < E * words; i += kPrepThreads) masks[i] = 0;
-  for (int i = tid; i < 128; i += kPrepThreads) owner[i] = 0;
   __syncthreads();
-  for (int p = tid; p < pairs; p += kPrepThreads) {
-    const int e = a.ids[p], t = p >> 4;
-    if (e < 0 || e >= E) {
-      report(a.status, MOE_ERR_DEVICE_IDS);
-      continue;
+  // A warp covers 32 consecutive pairs (one owner word), so the owner bits
+  // are a ballot rather than 32 colliding atomics.
+  for (int base = warp * 32; base < pairs; base += kPrepThreads) {
+    const int p = base + lane;
+    bool kept = false;
+    if (p < pairs) {
+      const int e = a.ids[p], t = p >> 4;
+      if (e < 0 || e >= E) {
+        report(a.status, MOE_ERR_DEVICE_IDS);
+      } else {
+        const uint32_t bit = 1u << (t & 31);
+        const uint32_t old = atomicOr(&masks[e * words + (t >> 5)], bit);
+        kept = !(old & bit);
+        if (!kept) report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within token t
+      }
     }
-    const uint32_t bit = 1u << (t & 31);
-    const uint32_t old = atomicOr(&masks[e * words + (t >> 5)], bit);
-    if (old & bit)
-      report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within token t
-    else
-      atomicOr(&owner[p >> 5], 1u << (p & 31));
+    const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, kept);
+    if (lane == 0) owner[base >> 5] = ballot;
   }
   __syncthreads();
 
@@ -142,12 +153,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   // Let the experts kernel start its prologue; it waits for this grid's end
   // before reading anything written here.
   ptx::grid_launch_dependents();
-  const int block = blockIdx.x;
-  if ((a.roles & kPrepQuantize) && block < a.quant_blocks) {
-    quantize_role(a, block);
-  } else if ((a.roles & kPrepGroup) &&
-             block == ((a.roles & kPrepQuantize) ? a.quant_blocks : 0)) {
+  // The grouping block is block 0, dispatched first: it has the longest run.
+  const int group_blocks = (a.roles & kPrepGroup) ? 1 : 0;
+  if (group_blocks && blockIdx.x == 0) {
     group_role(a, smem);
+  } else if (a.roles & kPrepQuantize) {
+    quantize_role(a, blockIdx.x - group_blocks);
   }
 }
 
@@ -156,6 +167,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 int prep_group_smem_bytes(int experts) {
   const int words = (MOE_MAX_BATCH + 31) / 32;
   return experts * words * 4 + experts * 4 + 128 * 4 + 9 * 4;
+}
+
+int prep_quant_blocks(int batch, int hidden) {
+  const int chunks = batch * (hidden / 8);
+  return (chunks + kPrepThreads * kQuantChunks - 1) / (kPrepThreads * kQuantChunks);
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {

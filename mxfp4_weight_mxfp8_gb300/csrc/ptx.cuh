@@ -236,6 +236,21 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Eight consecutive 32-bit TMEM columns of this thread's lane, without the
+// wait: call tmem_wait_loads() before using the registers.
+__device__ __forceinline__ void tmem_load_8_async(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_loads() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Eight consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_load_8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
