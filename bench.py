@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default=MAIN_CONFIG)
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    p.add_argument("--profile-case", action="store_true",
+                   help="no timing: prepare one layer and run --steps calls of --config "
+                        "(a small case for ncu captures)")
     return p.parse_args()
 
 
@@ -490,9 +493,33 @@ def run_reference(args, rank, world):
     print(json.dumps(result), flush=True)
 
 
+def profile_case(args):
+    """Run --steps calls of one workload on one prepared layer, nothing else."""
+    import torch
+
+    import mxfp4_weight_mxfp8_gb300 as moe
+
+    cfg = workload.CONFIGS[args.config]
+    weights, x, ids = workload.make_inputs(cfg)
+    device = torch.device("cuda", 0)
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to(device) for w in weights))
+    xd = torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16)
+    idsd = torch.from_numpy(ids).to(device)
+    for _ in range(max(1, args.steps)):
+        layer(xd, idsd)
+    status = moe.moe_sync_status(layer.handle)
+    print(json.dumps({"profile_case": describe(cfg), "calls": args.steps, "status": status}))
+    layer.close()
+    if status != moe.MOE_OK:
+        sys.exit(1)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -26,9 +26,10 @@
 // are cut into contiguous per-CTA ranges of near-equal bytes, and every CTA
 // runs FC1(A), FC1(B), FC2(A), FC2(B): half A's hidden vectors are reduced
 // and published while half B's FC1 weights stream.
-// An FC1 item split across CTAs is reduced by the last CTA to finish its
-// piece (an acquire-release counter; a fixed CTA order keeps the sum
-// deterministic). Every wait is bounded by a time limit.
+// An FC1 item split across CTAs is reduced by the CTA holding its first
+// stage: the others store FP32 partial sums and release-increment a counter
+// that the owner acquires; a fixed CTA order keeps the sum deterministic.
+// Every wait is bounded by a time limit.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -133,10 +134,10 @@ __device__ bool wait_bar(const Ctx& cx, uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+// Release increment (no result): the caller's earlier stores, and those of
+// the threads it synchronized with, are visible to whoever acquires the count.
+__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ float silu_times(float gate, float up) {
@@ -463,15 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lane == 0) freed = wait_bar(cx, &hempty[b], ((ordinal >> 1) - 1) & 1);
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
-      // Wait (bounded) for every K chunk of the unit's hidden vector.
+      // Wait (bounded) for every K chunk of the unit's hidden vector: lane l
+      // polls chunk l % KC2, so all chunks are polled at once and every lane
+      // holds an acquire before it reads the image.
       const uint64_t t_start = global_timer_ns();
-      for (int c = 0; c < g.KC2; ++c) {
-        const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + c;
-        for (uint32_t i = 0; load_acquire_gpu(flag) == 0; ++i) {
-          if ((i & 15u) == 15u && global_timer_ns() - t_start > a.timeout_ns) {
-            report(a.status, MOE_ERR_DEVICE_TIMEOUT);
-            break;  // proceed with whatever the image holds
-          }
+      const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + (lane % g.KC2);
+      for (uint32_t i = 0;; ++i) {
+        if (__all_sync(0xFFFFFFFFu, load_acquire_gpu(flag) != 0)) break;
+        if ((i & 7u) == 7u && global_timer_ns() - t_start > a.timeout_ns) {
+          if (lane == 0) report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+          break;  // proceed with whatever the image holds
         }
       }
       const uint8_t* src = a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes;
@@ -560,54 +562,44 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         while (valid < kUnitRows && unit_row(u, valid) >= 0) ++valid;
         const bool whole = (md.z % g.KC1 == 0) && (md.w % g.KC1 == g.KC1 - 1);
         if (!whole) {
+          // Split-K: the item's owner is the CTA holding its first stage. Its
+          // piece is the last one of its own range, so the other pieces (each
+          // the first piece of a later CTA) are usually in L2 by then.
           const int item_first = item * g.KC1;
           const int hf = item < items_a ? 0 : 1;
           const int* st = start + hf * (G + 1);
-          const int slot = (f0[hf] >= item_first) ? 0 : 1;
-          float* dst = a.partials + static_cast<size_t>((cta * 2 + hf) * 2 + slot) * 2 * kUnitRows * kTileM;
-          for (int t = 0; t < valid; ++t) {
-            dst[t * kTileM + m] = v0[t];
-            dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
-          }
-          epilogue_sync();
           const int c_lo = cta_of(st, G, item_first);
-          const int c_hi = cta_of(st, G, item_first + g.KC1 - 1);
-          if (et == 0) {
-            uint32_t pieces = 0;
-            for (int c = c_lo; c <= c_hi; ++c) pieces += st[c] < st[c + 1];
-            const uint32_t before = atomic_add_acq_rel_gpu(&a.item_counters[item], 1u);
-            misc[2] = (before + 1 == pieces) ? 1u : 0u;
+          if (cta != c_lo) {
+            // Hand the partial sums to the owner and move on: a CTA owns
+            // every item whose first stage it holds, so this is its only
+            // hand-off in this half.
+            float* dst = a.partials + static_cast<size_t>(cta * 2 + hf) * 2 * kUnitRows * kTileM;
+            for (int t = 0; t < valid; ++t) {
+              dst[t * kTileM + m] = v0[t];
+              dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
+            }
+            epilogue_sync();
+            if (et == 0) red_release_add_gpu(&a.item_counters[item], 1u);
+            continue;
           }
-          epilogue_sync();
-          const bool last = misc[2] != 0;
-          epilogue_sync();  // misc[2] is reused by the next piece
-          if (!last) continue;
-          // Sum every piece in CTA order (deterministic whoever finishes last).
-          float gs[8], us[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) gs[t] = us[t] = 0.f;
-          for (int c = c_lo; c <= c_hi; ++c) {
-            const int b0 = st[c];
-            if (b0 == st[c + 1]) continue;
-            if (c == cta) {
-#pragma unroll
-              for (int t = 0; t < 8; ++t) {
-                gs[t] += v0[t];
-                us[t] += v1[t];
-              }
-            } else {
-              const int sl = (b0 >= item_first) ? 0 : 1;
-              const float* src = a.partials + static_cast<size_t>((c * 2 + hf) * 2 + sl) * 2 * kUnitRows * kTileM;
-              for (int t = 0; t < valid; ++t) {
-                gs[t] += __ldcg(src + t * kTileM + m);
-                us[t] += __ldcg(src + kUnitRows * kTileM + t * kTileM + m);
-              }
+          const int c_hi = cta_of(st, G, item_first + g.KC1 - 1);
+          uint32_t others = 0;
+          for (int c = c_lo + 1; c <= c_hi; ++c) others += st[c] < st[c + 1];
+          const uint64_t t_wait = global_timer_ns();
+          for (uint32_t i = 0; load_acquire_gpu(&a.item_counters[item]) < others; ++i) {
+            if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
+              report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+              break;
             }
           }
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            v0[t] = gs[t];
-            v1[t] = us[t];
+          // Sum the pieces in CTA order: the owner's own piece first.
+          for (int c = c_lo + 1; c <= c_hi; ++c) {
+            if (st[c] == st[c + 1]) continue;
+            const float* src = a.partials + static_cast<size_t>(c * 2 + hf) * 2 * kUnitRows * kTileM;
+            for (int t = 0; t < valid; ++t) {
+              v0[t] += __ldcg(src + t * kTileM + m);
+              v1[t] += __ldcg(src + kUnitRows * kTileM + t * kTileM + m);
+            }
           }
         }
         // SiLU(gate) * up, MXFP8 per 32 hidden values (= this warp's 32 rows).

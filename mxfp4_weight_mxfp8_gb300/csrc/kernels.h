@@ -40,7 +40,7 @@ struct ExpertsArgs {
   const int16_t* unit_rows;
   uint32_t* item_counters;
   uint32_t* hidden_flags;
-  float* partials;            // [grid, 2 halves, 2 pieces, 2 tiles, 8 tokens, 128 rows]
+  float* partials;            // [grid, 2 halves, 2 tiles, 8 tokens, 128 rows]
   uint8_t* hidden;            // [unit_cap, hidden_bytes]
   uint16_t* out;              // BF16 [B * 16, H]
   int32_t* status;

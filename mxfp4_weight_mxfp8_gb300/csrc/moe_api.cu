@@ -173,7 +173,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(h->unit_cap) * moe::kUnitRows * 2,    // unit rows
       static_cast<size_t>(h->unit_cap) * g.P1 * 4,              // FC1 item counters
       static_cast<size_t>(h->unit_cap) * g.KC2 * 4,             // hidden flags
-      static_cast<size_t>(h->grid) * 4 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
+      static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
       static_cast<size_t>(h->unit_cap) * g.hidden_bytes,        // hidden images
       4,                                                        // status
   };
