@@ -43,6 +43,7 @@ extern "C" {
 #define MOE_MAX_EXPERTS 1024
 #define MOE_MAX_HIDDEN 16384
 #define MOE_MAX_INTER 512
+#define MOE_NOALLOC_SCRATCH_BYTES (4 << 20) /* static scratch of moe_run_noalloc */
 
 enum moe_status {
   MOE_OK = 0,
@@ -150,6 +151,38 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
  * MOE_ERR_CUDA.
  */
 int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream);
+
+/*
+ * moe_run_noalloc - moe_run for callers that cannot allocate device memory
+ * when they run the layer. The pages have no counterpart to this call.
+ *
+ * Some runtimes hand all device memory to their own pool at start-up, or
+ * must not call cudaMalloc on the decode path. This call computes exactly
+ * what moe_run computes, with the same kernels, but takes none of its
+ * per-call scratch (activation plan, unit table, split-K counters and
+ * partial sums, hidden-vector images) from the handle's workspace: all of it
+ * comes from one module-scope device array of MOE_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading this library keeps until the process exits. It
+ * calls no cudaMalloc, cudaFree or other allocating routine. The caller
+ * still passes x, ids and out (layouts as for moe_run) and a handle from
+ * moe_prepare, the one-time set-up call that does allocate.
+ *   - The scratch a call needs grows with batch, the layer's shape and the
+ *     grid; a call that would need more than MOE_NOALLOC_SCRATCH_BYTES is
+ *     rejected with MOE_ERR_ARG before any launch (moe_last_error_detail
+ *     says how much it needed). The TP8 shard (H 3584, I 384, 384 experts)
+ *     fits for batches up to 16 on a 152-SM GB300.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and the counters that
+ *     must start at zero are cleared inside each call: calls that overlap on
+ *     the GPU (other streams, other handles) race and corrupt each other.
+ * Asynchronous on `stream`; device-side errors surface through
+ * moe_sync_status on the same handle. Errors: as moe_run, and
+ * MOE_ERR_UNSUPPORTED on a device ordinal of 64 or more.
+ */
+int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16,
+                    int batch, void* stream);
 
 /*
  * moe_run_host - moe_run on host buffers: copies x and ids to handle-owned

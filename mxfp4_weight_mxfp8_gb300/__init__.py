@@ -16,15 +16,17 @@ from .build import LIBRARY
 
 __all__ = [
     "MoeError", "MoeInfo", "MoeLayer", "library", "moe_prepare", "moe_quantize", "moe_group",
-    "moe_run", "moe_experts", "moe_run_host", "moe_sync_status", "moe_copy_plan", "moe_copy_units",
-    "moe_copy_hidden", "moe_set_timeout", "moe_debug_withhold", "moe_info", "moe_destroy",
+    "moe_run", "moe_experts", "moe_run_noalloc", "moe_run_host", "moe_sync_status",
+    "moe_copy_plan", "moe_copy_units", "moe_copy_hidden", "moe_set_timeout", "moe_debug_withhold", "moe_info", "moe_destroy",
     "moe_error_string", "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA",
     "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS", "MOE_ERR_STATE", "TOPK", "UNIT_ROWS",
+    "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
     "MAX_BATCH",
 ]
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_IDS, MOE_ERR_STATE = 4, 5, 6
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20  # static scratch of moe_run_noalloc
 TOPK, UNIT_ROWS, MAX_BATCH = 16, 8, 256
 
 
@@ -52,6 +54,7 @@ def _load():
         "moe_group": ([vp, vp, i32, vp], i32),
         "moe_run": ([vp, vp, vp, vp, i32, vp], i32),
         "moe_experts": ([vp, vp, i32, vp], i32),
+        "moe_run_noalloc": ([vp, vp, vp, vp, i32, vp], i32),
         "moe_run_host": ([vp, vp, vp, vp, i32, vp], i32),
         "moe_sync_status": ([vp, vp], i32),
         "moe_copy_plan": ([vp, vp, vp, i32], i32),
@@ -84,6 +87,11 @@ class MoeError(RuntimeError):
         text = _lib.moe_error_string(code).decode()
         super().__init__(f"{call}: {text} (status {code}){': ' + detail if detail else ''}")
         self.code = code
+
+
+def moe_last_error_detail() -> str:
+    """Detail of this thread's last argument or CUDA error ("" if none)."""
+    return _lib.moe_last_error_detail().decode()
 
 
 def _check(code: int, call: str) -> int:
@@ -139,6 +147,13 @@ def moe_run(handle, x, ids, out, batch: int, stream=None):
 
 def moe_experts(handle, out, batch: int, stream=None):
     return _check(_lib.moe_experts(handle, _ptr(out), batch, _stream(stream)), "moe_experts")
+
+
+def moe_run_noalloc(handle, x, ids, out, batch: int, stream=None):
+    """moe_run with all per-call scratch in the library's static device
+    buffer (for callers that cannot allocate when they run the layer)."""
+    return _check(_lib.moe_run_noalloc(handle, _ptr(x), _ptr(ids), _ptr(out), batch,
+                                       _stream(stream)), "moe_run_noalloc")
 
 
 def moe_run_host(handle, x, ids, out, batch: int, stream=None):

@@ -3,6 +3,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -445,5 +446,122 @@ const char* moe_error_string(int status) {
 }
 
 const char* moe_last_error_detail(void) { return g_detail; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_run without allocation (no counterpart on the pages).
+//
+// Some callers cannot call cudaMalloc when they run a layer: a runtime that
+// hands all device memory to its own pool at start-up, or code that must not
+// allocate on the decode path. moe_run itself allocates nothing either, but
+// its scratch lives in the handle's workspace, which is sized for the largest
+// batch. moe_run_noalloc runs the same two kernels with every per-call
+// scratch buffer (activation plan, unit table, split-K counters and partial
+// sums, hidden-vector images) carved out of one fixed, module-scope device
+// array instead; the caller still passes x, ids and out, and the handle still
+// supplies the prepared weights.
+
+namespace {
+
+// Scratch shared by every moe_run_noalloc call on a device. Every GPU that
+// loads this library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch per device. In host code the array's
+// name is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr int kNoallocDevices = 64;
+void* g_noalloc_address[kNoallocDevices] = {};
+std::mutex g_noalloc_mutex;
+
+int noalloc_scratch(int device, uint8_t** base) {
+  if (device < 0 || device >= kNoallocDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_address[device] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_address[device] = ptr;
+  }
+  *base = static_cast<uint8_t*>(g_noalloc_address[device]);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
+                               void* out_bf16, int batch, void* stream) {
+  if (h == nullptr || !x_bf16 || !topk_ids || !out_bf16) return MOE_ERR_ARG;
+  if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(out_bf16) || check_batch(batch))
+    return MOE_ERR_ARG;
+  const Geometry& g = h->g;
+  const int cap = moe::unit_capacity(batch, g.E);
+  const size_t sizes[] = {
+      static_cast<size_t>(batch) * g.H,                            // plan codes
+      static_cast<size_t>(batch) * (g.H / moe::kBlock),            // plan scales
+      4,                                                           // unit count
+      static_cast<size_t>(cap) * 4,                                // unit experts
+      static_cast<size_t>(cap) * moe::kUnitRows * 2,               // unit rows
+      static_cast<size_t>(cap) * g.P1 * 4,                         // FC1 item counters
+      static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
+      static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
+      static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
+  };
+  size_t offsets[9], total = 0;
+  for (int i = 0; i < 9; ++i) {
+    offsets[i] = total;
+    total += round256(sizes[i]);
+  }
+  if (total > MOE_NOALLOC_SCRATCH_BYTES) {
+    std::snprintf(g_detail, sizeof g_detail,
+                  "moe_run_noalloc: batch %d of this layer needs %zu bytes of scratch, more than "
+                  "the %d-byte static buffer",
+                  batch, total, MOE_NOALLOC_SCRATCH_BYTES);
+    return MOE_ERR_ARG;
+  }
+  int device = 0;
+  MOE_CUDA(cudaGetDevice(&device));
+  uint8_t* w = nullptr;
+  const int rc = noalloc_scratch(device, &w);
+  if (rc != MOE_OK) return rc;
+
+  // The grouping block of the prep kernel clears the counters and flags the
+  // experts kernel needs at zero; every other scratch byte is written before
+  // it is read within the call, so nothing is left over from the last call.
+  moe::PrepArgs pa = prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup);
+  pa.unit_cap = cap;
+  pa.plan_codes = w + offsets[0];
+  pa.plan_scales = w + offsets[1];
+  pa.unit_count = reinterpret_cast<int32_t*>(w + offsets[2]);
+  pa.unit_expert = reinterpret_cast<int32_t*>(w + offsets[3]);
+  pa.unit_rows = reinterpret_cast<int16_t*>(w + offsets[4]);
+  pa.item_counters = reinterpret_cast<uint32_t*>(w + offsets[5]);
+  pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(moe::launch_prep(pa, s));
+
+  moe::ExpertsArgs ea{};
+  ea.wmap = h->wmap;
+  ea.stages = h->stages;
+  ea.plan_codes = pa.plan_codes;
+  ea.plan_scales = pa.plan_scales;
+  ea.unit_count = pa.unit_count;
+  ea.unit_expert = pa.unit_expert;
+  ea.unit_rows = pa.unit_rows;
+  ea.item_counters = pa.item_counters;
+  ea.hidden_flags = pa.hidden_flags;
+  ea.partials = reinterpret_cast<float*>(w + offsets[7]);
+  ea.hidden = w + offsets[8];
+  ea.out = static_cast<uint16_t*>(out_bf16);
+  ea.status = h->status;  // read and cleared by moe_sync_status, as for moe_run
+  ea.g = g;
+  ea.timeout_ns = h->timeout_ns;
+  ea.withhold_unit = -1;
+  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true));
+  return MOE_OK;
+}
+
+extern "C" {
 
 }  // extern "C"

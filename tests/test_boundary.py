@@ -75,6 +75,7 @@ def test_calls_reject_null_handles_and_bad_batches(lib):
     assert raw.moe_group(None, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_run_host(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_experts(None, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_run_noalloc(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_sync_status(None, None) == lib.MOE_ERR_ARG
     assert raw.moe_copy_plan(None, p, p, 1) == lib.MOE_ERR_ARG
     assert raw.moe_copy_units(None, p, p, p, 1) == lib.MOE_ERR_ARG
@@ -88,6 +89,10 @@ def test_calls_reject_null_handles_and_bad_batches(lib):
 
 def test_python_binding_names_match_the_c_abi(lib):
     for name in declared_functions():
-        if name == "moe_last_error_detail":
-            continue
         assert hasattr(lib, name), name
+
+
+def test_noalloc_scratch_limit_matches_the_header(lib):
+    text = open(HEADER, encoding="utf-8").read()
+    m = re.search(r"#define MOE_NOALLOC_SCRATCH_BYTES \((\d+) << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == lib.MOE_NOALLOC_SCRATCH_BYTES
