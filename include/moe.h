@@ -212,7 +212,8 @@ int moe_sync_status(moe_handle h, void* stream);
  *                  count exceeds capacity);
  *  moe_copy_hidden hidden codes uint8 [units, 8, I] and scales uint8
  *                  [units, 8, I/32] of the last run, row r of unit u being
- *                  the unit's r-th pair.
+ *                  the unit's r-th pair (rows past the unit's last pair are
+ *                  padding and hold stale bytes).
  * All write host memory; MOE_ERR_STATE before the producing call.
  */
 int moe_copy_plan(moe_handle h, uint8_t* codes, uint8_t* scales, int batch);

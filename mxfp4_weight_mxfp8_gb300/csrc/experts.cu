@@ -62,7 +62,7 @@ struct Layout {
     bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4) * 8;
     meta = o = up(o, 16);  o += NACC * 16;
     misc = o = up(o, 16);  o += 16;
-    rows = o = up(o, 16);  o += kRowCache * (4 + kUnitRows * 2);
+    rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
     bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }
   __host__ __device__ bool aligned() const {
@@ -77,37 +77,29 @@ struct Layout {
 // 17 KB per stage). When the shares are too small for that to stay
 // monotone, both are cut evenly. Every CTA computes the same table.
 struct Split {
-  int T1, J, KC2, G;
-  long long T;
+  int T1, J, KC2, G, T;
   bool balanced;
   __device__ Split(int units, const Geometry& g, int grid) {
     T1 = units * g.P1 * g.KC1;
     J = units * g.NQ;
     KC2 = g.KC2;
     G = grid;
-    T = static_cast<long long>(T1) + static_cast<long long>(J) * KC2;
-    balanced = T / G >= static_cast<long long>(KC2) * ((J + G - 1) / G);
+    T = T1 + J * KC2;
+    balanced = T / G >= KC2 * ((J + G - 1) / G);
   }
+  // 32-bit products: T < 1.2M stages and c <= 256 for every supported layer.
   __device__ int fc2_begin(int c) const {
-    return static_cast<int>(static_cast<long long>(c) * J / G);
+    const uint32_t cu = static_cast<uint32_t>(c);
+    return static_cast<int>(cu * static_cast<uint32_t>(J) / static_cast<uint32_t>(G));
   }
   __device__ int fc1_begin(int c) const {
     if (c >= G) return T1;
-    if (!balanced) return static_cast<int>(static_cast<long long>(c) * T1 / G);
-    long long v = static_cast<long long>(c) * T / G - static_cast<long long>(KC2) * fc2_begin(c);
-    return static_cast<int>(v < 0 ? 0 : (v > T1 ? T1 : v));
+    const uint32_t cu = static_cast<uint32_t>(c), gu = static_cast<uint32_t>(G);
+    if (!balanced) return static_cast<int>(cu * static_cast<uint32_t>(T1) / gu);
+    const int v = static_cast<int>(cu * static_cast<uint32_t>(T) / gu) - KC2 * fc2_begin(c);
+    return v < 0 ? 0 : (v > T1 ? T1 : v);
   }
 };
-
-// The CTA whose FC1 range holds stage s: the largest c with start[c] <= s.
-__device__ int cta_of(const int* start, int G, int s) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (start[mid] <= s) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
 
 struct Ctx {
   const ExpertsArgs* a;
@@ -316,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (lane == 0) {
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
-      int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_stage = 0;
+      int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
       auto acquire = [&](int set) {
@@ -336,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         const int set = k % NACC;
         if (first) {
           if (!(ok = acquire(set))) break;
-          first_stage = cur.s;
+          first_c = cur.c;
         }
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
@@ -354,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         tc_commit(&empty[slot]);
         advance();
         if (last) {
-          if (lead) meta[set] = make_int4(0, cur.item, first_stage, cur.s);
+          // (FC1, item, piece starts the item's K range, piece ends it)
+          if (lead) meta[set] = make_int4(0, cur.item, first_c == 0, cur.c == g.KC1 - 1);
           tc_commit(&accfull[set]);
           if (lead) mbar_arrive(&accfull[set]);
           ++k;
@@ -467,22 +460,36 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       // Wait (bounded) for every K chunk of the unit's hidden vector: lane l
       // polls chunk l % KC2, so all chunks are polled at once and every lane
       // holds an acquire before it reads the image.
+      // Relaxed polls, then one acquire fence before the image is read.
       const uint64_t t_start = global_timer_ns();
       const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + (lane % g.KC2);
       for (uint32_t i = 0;; ++i) {
-        if (__all_sync(0xFFFFFFFFu, load_acquire_gpu(flag) != 0)) break;
+        if (__all_sync(0xFFFFFFFFu, load_relaxed_gpu(flag) != 0)) break;
         if ((i & 7u) == 7u && global_timer_ns() - t_start > a.timeout_ns) {
           if (lane == 0) report(a.status, MOE_ERR_DEVICE_TIMEOUT);
           break;  // proceed with whatever the image holds
         }
       }
-      const uint8_t* src = a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes;
-      uint8_t* codes = HC + b * g.KC2 * kActImageBytes;
-      uint8_t* scales = HSF + b * g.KC2 * kScaleAtomBytes;
-      for (int i = lane; i < g.KC2 * kActImageBytes / 16; i += 32)
-        reinterpret_cast<uint4*>(codes)[i] = load_cg_v4(src + i * 16);
-      for (int i = lane; i < g.KC2 * kScaleAtomBytes / 16; i += 32)
-        reinterpret_cast<uint4*>(scales)[i] = load_cg_v4(src + g.KC2 * kActImageBytes + i * 16);
+      fence_acquire_gpu();
+      // The image (codes of every K chunk, then their scale atoms) in one
+      // batch of independent 16-byte loads per lane: a single L2 round trip.
+      const uint4* src = reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes);
+      uint4* codes = reinterpret_cast<uint4*>(HC + b * g.KC2 * kActImageBytes);
+      uint4* scales = reinterpret_cast<uint4*>(HSF + b * g.KC2 * kScaleAtomBytes);
+      const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
+      constexpr int kPerLane = kMaxInterChunks * kHiddenChunkBytes / 16 / 32;
+      uint4 v[kPerLane];
+#pragma unroll
+      for (int k = 0; k < kPerLane; ++k) {
+        const int i = lane + 32 * k;
+        if (i < n_all) v[k] = __ldcg(src + i);
+      }
+#pragma unroll
+      for (int k = 0; k < kPerLane; ++k) {
+        const int i = lane + 32 * k;
+        if (i < n_codes) codes[i] = v[k];
+        else if (i < n_all) scales[i - n_codes] = v[k];
+      }
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&hfull[b]);
@@ -496,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     // Unit rows of this CTA's first units, fetched while the first stages stream.
     int* cache_unit = reinterpret_cast<int*>(sm + L.rows);
-    int16_t* cache_rows = reinterpret_cast<int16_t*>(cache_unit + kRowCache);
+    int* cache_valid = cache_unit + kRowCache;
+    int16_t* cache_rows = reinterpret_cast<int16_t*>(cache_valid + kRowCache);
     {
       const int per_unit_fc1 = g.P1 * g.KC1;
       int lo = units, hi = -1;
@@ -513,12 +521,27 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         cache_rows[et] = (u <= hi) ? a.unit_rows[u * kUnitRows + et % kUnitRows] : -1;
       }
       epilogue_sync();
+      if (et < kRowCache) {
+        int v = 0;
+        while (v < kUnitRows && cache_rows[et * kUnitRows + v] >= 0) ++v;
+        cache_valid[et] = v;
+      }
+      epilogue_sync();
     }
-    auto unit_row = [&](int u, int r) -> int {
+    auto cached = [&](int u) {
       const int i = u - cache_unit[0];
-      if (cache_unit[0] >= 0 && i >= 0 && i < kRowCache && cache_unit[i] == u)
-        return cache_rows[i * kUnitRows + r];
-      return a.unit_rows[u * kUnitRows + r];
+      return (cache_unit[0] >= 0 && i >= 0 && i < kRowCache && cache_unit[i] == u) ? i : -1;
+    };
+    auto unit_row = [&](int u, int r) -> int {
+      const int i = cached(u);
+      return i >= 0 ? cache_rows[i * kUnitRows + r] : a.unit_rows[u * kUnitRows + r];
+    };
+    auto unit_valid = [&](int u) -> int {
+      const int i = cached(u);
+      if (i >= 0) return cache_valid[i];
+      int v = 0;
+      while (v < kUnitRows && a.unit_rows[u * kUnitRows + v] >= 0) ++v;
+      return v;
     };
     int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;
     for (;;) {
@@ -558,23 +581,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       if (md.x == 0) {
         // ---- FC1 piece: gate = v0, up = v1 for rows 128p + m.
         const int item = md.y, u = item / g.P1, p = item - u * g.P1;
-        int valid = 0;
-        while (valid < kUnitRows && unit_row(u, valid) >= 0) ++valid;
-        const bool whole = (md.z % g.KC1 == 0) && (md.w % g.KC1 == g.KC1 - 1);
-        if (!whole) {
+        const int valid = unit_valid(u);
+        if (!(md.z && md.w)) {
           // Split-K: the item's owner is the CTA holding its first stage. Its
           // piece is the last one of its own range, so the other pieces (each
           // the first piece of a later CTA) are usually in L2 by then.
-          const int item_first = item * g.KC1;
           const int hf = item < items_a ? 0 : 1;
           const int* st = start + hf * (G + 1);
-          const int c_lo = cta_of(st, G, item_first);
-          if (cta != c_lo) {
+          if (!md.z) {
             // Hand the partial sums to the owner and move on: a CTA owns
             // every item whose first stage it holds, so this is its only
             // hand-off in this half.
             float* dst = a.partials + static_cast<size_t>(cta * 2 + hf) * 2 * kUnitRows * kTileM;
-            for (int t = 0; t < valid; ++t) {
+#pragma unroll
+            for (int t = 0; t < kUnitRows; ++t) {
+              if (t >= valid) break;
               dst[t * kTileM + m] = v0[t];
               dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
             }
@@ -582,32 +603,57 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             if (et == 0) red_release_add_gpu(&a.item_counters[item], 1u);
             continue;
           }
-          const int c_hi = cta_of(st, G, item_first + g.KC1 - 1);
+          // The other pieces sit in the CTAs after this one, up to the item's
+          // last stage.
+          const int item_last = item * g.KC1 + g.KC1 - 1;
+          int c_end = cta + 1;
           uint32_t others = 0;
-          for (int c = c_lo + 1; c <= c_hi; ++c) others += st[c] < st[c + 1];
+          for (; c_end < G && st[c_end] <= item_last; ++c_end) others += st[c_end] < st[c_end + 1];
           const uint64_t t_wait = global_timer_ns();
-          for (uint32_t i = 0; load_acquire_gpu(&a.item_counters[item]) < others; ++i) {
+          for (uint32_t i = 0; load_relaxed_gpu(&a.item_counters[item]) < others; ++i) {
             if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
               report(a.status, MOE_ERR_DEVICE_TIMEOUT);
               break;
             }
           }
-          // Sum the pieces in CTA order: the owner's own piece first.
-          for (int c = c_lo + 1; c <= c_hi; ++c) {
-            if (st[c] == st[c + 1]) continue;
-            const float* src = a.partials + static_cast<size_t>(c * 2 + hf) * 2 * kUnitRows * kTileM;
-            for (int t = 0; t < valid; ++t) {
-              v0[t] += __ldcg(src + t * kTileM + m);
-              v1[t] += __ldcg(src + kUnitRows * kTileM + t * kTileM + m);
+          fence_acquire_gpu();
+          // Sum the pieces in CTA order, the owner's own piece first; the
+          // loads of up to four pieces are issued together.
+          for (int c0 = cta + 1; c0 < c_end; c0 += 4) {
+            float p0[4][kUnitRows], p1[4][kUnitRows];
+            bool has[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = c0 + j;
+              has[j] = c < c_end && st[c] < st[c + 1];
+              const float* src = a.partials + static_cast<size_t>(c * 2 + hf) * 2 * kUnitRows * kTileM;
+#pragma unroll
+              for (int t = 0; t < kUnitRows; ++t) {
+                const bool ld = has[j] && t < valid;
+                p0[j][t] = ld ? __ldcg(src + t * kTileM + m) : 0.f;
+                p1[j][t] = ld ? __ldcg(src + kUnitRows * kTileM + t * kTileM + m) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (!has[j]) continue;
+#pragma unroll
+              for (int t = 0; t < kUnitRows; ++t) {
+                v0[t] += p0[j][t];
+                v1[t] += p1[j][t];
+              }
             }
           }
         }
         // SiLU(gate) * up, MXFP8 per 32 hidden values (= this warp's 32 rows).
         if (p * kTileM + q * 32 < g.I) {
           uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
+          // Rows past `valid` are padding: FC2 reads them but its output
+          // columns for them are never stored, so they stay unwritten.
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
-            const float h = t < valid ? silu_times(v0[t], v1[t]) : 0.f;
+            if (t >= valid) break;
+            const float h = silu_times(v0[t], v1[t]);
             float amax = fabsf(h);
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
@@ -626,14 +672,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         if (u != out_unit) {
           out_pair = unit_row(u, et >> 4);
-          out_valid = 0;
-          while (out_valid < kUnitRows && unit_row(u, out_valid) >= 0) ++out_valid;
+          out_valid = unit_valid(u);
           out_unit = u;
         }
         if (out_valid <= 2) {
           // Few rows: each thread stores its two values of each row directly
           // (a warp writes 64 contiguous bytes per row and tile).
-          for (int t = 0; t < out_valid; ++t) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= out_valid) break;
             uint16_t* dst = a.out + static_cast<size_t>(unit_row(u, t)) * g.H + qq * 2 * kTileM;
             dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
             dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));

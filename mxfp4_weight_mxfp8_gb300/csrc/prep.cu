@@ -68,19 +68,30 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* masks = reinterpret_cast<uint32_t*>(smem);          // [E][words]
   int32_t* ustart = reinterpret_cast<int32_t*>(masks + E * words);  // [E]
-  uint32_t* owner = reinterpret_cast<uint32_t*>(ustart + E);    // [128]: pair kept its bit
-  int32_t* warp_total = reinterpret_cast<int32_t*>(owner + 128);  // [8]
+  int32_t* warp_total = ustart + E;                             // [8]
   int32_t* grand = warp_total + 8;                              // [1]
 
+  // Every id this thread handles, loaded in one batch (pair it * 256 + tid).
+  constexpr int kIters = MOE_MAX_BATCH * kTopK / kPrepThreads;
+  int ev[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int p = it * kPrepThreads + tid;
+    ev[it] = p < pairs ? a.ids[p] : -1;
+  }
   for (int i = tid; i < E * words; i += kPrepThreads) masks[i] = 0;
   __syncthreads();
-  // A warp covers 32 consecutive pairs (one owner word), so the owner bits
-  // are a ballot rather than 32 colliding atomics.
-  for (int base = warp * 32; base < pairs; base += kPrepThreads) {
+  // A pair is kept unless its id is out of range or repeats an earlier slot
+  // of its token (whichever atomic OR lands first keeps the bit).
+  uint32_t kept_bits = 0;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int base = it * kPrepThreads + warp * 32;
+    if (it * kPrepThreads >= pairs) break;
     const int p = base + lane;
     bool kept = false;
     if (p < pairs) {
-      const int e = a.ids[p], t = p >> 4;
+      const int e = ev[it], t = p >> 4;
       if (e < 0 || e >= E) {
         report(a.status, MOE_ERR_DEVICE_IDS);
       } else {
@@ -90,8 +101,7 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
         if (!kept) report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within token t
       }
     }
-    const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, kept);
-    if (lane == 0) owner[base >> 5] = ballot;
+    kept_bits |= static_cast<uint32_t>(kept) << it;
   }
   __syncthreads();
 
@@ -120,14 +130,8 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   for (int e = e0; e < e1; ++e) {
     int n = 0;
     for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
-    const int units = (n + 7) >> 3;
     ustart[e] = start;
-    for (int v = 0; v < units && start + v < a.unit_cap; ++v) {
-      a.unit_expert[start + v] = e;
-      const int valid = min(kUnitRows, n - kUnitRows * v);
-      for (int r = valid; r < kUnitRows; ++r) a.unit_rows[(start + v) * kUnitRows + r] = -1;
-    }
-    start += units;
+    start += (n + 7) >> 3;
   }
   __syncthreads();
   int units = *grand;
@@ -137,15 +141,30 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   }
   if (tid == 0) *a.unit_count = units;
   if (units == 0) return;
-  for (int p = tid; p < pairs; p += kPrepThreads) {
-    if (!((owner[p >> 5] >> (p & 31)) & 1u)) continue;
-    const int e = a.ids[p], t = p >> 4, w = t >> 5;
+  // One thread per unit: its expert is the last one whose first unit is at
+  // or before it (experts without units share the next one's start). Rows
+  // start as padding; the scatter below fills them.
+  for (int u = tid; u < units; u += kPrepThreads) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ustart[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    a.unit_expert[u] = lo;
+    reinterpret_cast<int4*>(a.unit_rows)[u] = make_int4(-1, -1, -1, -1);
+  }
+  for (int i = tid; i < units * a.P1; i += kPrepThreads) a.item_counters[i] = 0;
+  for (int i = tid; i < units * a.KC2; i += kPrepThreads) a.hidden_flags[i] = 0;
+  __syncthreads();  // the padding stores precede the row stores
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    if (!((kept_bits >> it) & 1u)) continue;
+    const int p = it * kPrepThreads + tid;
+    const int e = ev[it], t = p >> 4, w = t >> 5;
     int rank = __popc(masks[e * words + w] & ((1u << (t & 31)) - 1u));
     for (int i = 0; i < w; ++i) rank += __popc(masks[e * words + i]);
     a.unit_rows[(ustart[e] + (rank >> 3)) * kUnitRows + (rank & 7)] = static_cast<int16_t>(p);
   }
-  for (int i = tid; i < units * a.P1; i += kPrepThreads) a.item_counters[i] = 0;
-  for (int i = tid; i < units * a.KC2; i += kPrepThreads) a.hidden_flags[i] = 0;
 }
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
@@ -166,7 +185,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 
 int prep_group_smem_bytes(int experts) {
   const int words = (MOE_MAX_BATCH + 31) / 32;
-  return experts * words * 4 + experts * 4 + 128 * 4 + 9 * 4;
+  return experts * words * 4 + experts * 4 + 9 * 4;
 }
 
 int prep_quant_blocks(int batch, int hidden) {
