@@ -100,7 +100,7 @@ def profiled_traffic():
         text = open(PROFILE_SUMMARY).read()
     except OSError:
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith("- ") and ":" in line)
+    fields = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith("- ") and ": " in line)
     fields = {k[2:].strip(): v.strip() for k, v in fields.items()}
     if fields.get("kernel source sha256[:16]") != kernel_hash():
         return None
