@@ -336,13 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
         tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
         tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
-        const uint8_t* w = W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2);
-        const uint8_t* x = ACT + slot * kActImageBytes;
+        const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
+        const uint64_t dx = desc_sw128(ACT + slot * kActImageBytes + k0 * 32);
         const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          tc_mma_mxf8f6f4(d, desc_sw128(w + (k0 + kk) * 32), desc_sw128(x + (k0 + kk) * 32),
-                          mma_idesc(k0 + kk), sf, sf + 4, (first && kk == 0) ? 0u : 1u);
+        // Descriptor start addresses count 16-byte units: +2 is the next K-step.
+        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
+        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
         tc_commit(&empty[slot]);
         advance();
         if (last) {
@@ -369,19 +368,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         for (int c = 0; c < g.KC2 && ok; ++c) {
           if (!(ok = wait_bar(cx, &full[slot], phase))) break;
           tc_fence_after_sync();
-          const int ksteps = min(4, (g.I - c * kChunkK) / kBlock);
+          // K-steps of this chunk: 4, or fewer in the last chunk when I % 128 != 0.
+          const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
           if (k0 < ksteps) {
             const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            const int hc = hb * g.KC2 + c;
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-            tc_copy_scales(sf + 4, desc_scales(HSF + (hb * g.KC2 + c) * kScaleAtomBytes));
-            const uint8_t* w = W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2);
-            const uint8_t* h = HC + (hb * g.KC2 + c) * kActImageBytes;
+            tc_copy_scales(sf + 4, desc_scales(HSF + hc * kScaleAtomBytes));
+            const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
+            const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
             const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
-            for (int kk = k0; kk < k0 + 2 && kk < ksteps; ++kk) {
-              tc_mma_mxf8f6f4(d, desc_sw128(w + kk * 32), desc_sw128(h + kk * 32), mma_idesc(kk),
-                              sf, sf + 4, started ? 1u : 0u);
-              started = true;
-            }
+            // Descriptor start addresses count 16-byte units: +2 is the next K-step.
+            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sf + 4, started ? 1u : 0u);
+            if (k0 + 1 < ksteps)
+              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+            started = true;
           }
           tc_commit(&empty[slot]);
           advance();

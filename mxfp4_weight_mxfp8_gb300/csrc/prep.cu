@@ -167,6 +167,59 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   }
 }
 
+// Grouping for calls of at most kPrepThreads pairs (16 tokens): thread p owns
+// pair p and counts, over all pairs, those of its own expert (before it and
+// in total) and the units of all smaller experts. The table is the same
+// canonical one (experts ascending, rows in pair order); of two repeated ids
+// of a token the lower slot is kept.
+__device__ void group_small(const PrepArgs& a, uint8_t* smem) {
+  const int pairs = a.B * kTopK, tid = threadIdx.x;
+  int32_t* key = reinterpret_cast<int32_t*>(smem);  // [256]: expert of a kept pair, else INT_MAX
+  int32_t* nun = key + kPrepThreads;                // [256]: units of the expert, on its first pair
+  const int e = tid < pairs ? a.ids[tid] : -1;
+  key[tid] = e;
+  __syncthreads();
+  bool kept = false;
+  if (tid < pairs) {
+    if (e < 0 || e >= a.E) {
+      report(a.status, MOE_ERR_DEVICE_IDS);
+    } else {
+      kept = true;
+      for (int q = tid & ~(kTopK - 1); q < tid; ++q) kept = kept && key[q] != e;
+      if (!kept) report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within the token
+    }
+  }
+  __syncthreads();
+  key[tid] = kept ? e : 0x7FFFFFFF;
+  __syncthreads();
+  int n = 0, before = 0;
+  if (kept)
+    for (int q = 0; q < pairs; ++q) {
+      const int same = key[q] == e;
+      n += same;
+      before += same & (q < tid);
+    }
+  nun[tid] = (kept && before == 0) ? (n + 7) >> 3 : 0;
+  __syncthreads();
+  int units = 0, ubefore = 0;
+  for (int q = 0; q < pairs; ++q) {
+    const int v = nun[q];
+    units += v;
+    ubefore += key[q] < e ? v : 0;
+  }
+  if (tid == 0) *a.unit_count = units;
+  if (kept) {
+    const int u = ubefore + (before >> 3), r = before & 7;
+    a.unit_rows[u * kUnitRows + r] = static_cast<int16_t>(tid);
+    if (r == 0) {  // the unit's first pair: its expert and its padding rows
+      a.unit_expert[u] = e;
+      for (int rr = min(kUnitRows, n - before); rr < kUnitRows; ++rr) a.unit_rows[u * kUnitRows + rr] = -1;
+    }
+  }
+  for (int i = tid; i < units * a.P1; i += kPrepThreads) a.item_counters[i] = 0;
+  for (int i = tid; i < units * a.KC2; i += kPrepThreads) a.hidden_flags[i] = 0;
+}
+
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   // Let the experts kernel start its prologue; it waits for this grid's end
@@ -175,7 +228,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   // The grouping block is block 0, dispatched first: it has the longest run.
   const int group_blocks = (a.roles & kPrepGroup) ? 1 : 0;
   if (group_blocks && blockIdx.x == 0) {
-    group_role(a, smem);
+    if (a.B * kTopK <= kPrepThreads)
+      group_small(a, smem);
+    else
+      group_role(a, smem);
   } else if (a.roles & kPrepQuantize) {
     quantize_role(a, blockIdx.x - group_blocks);
   }
@@ -185,7 +241,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 
 int prep_group_smem_bytes(int experts) {
   const int words = (MOE_MAX_BATCH + 31) / 32;
-  return experts * words * 4 + experts * 4 + 9 * 4;
+  const int general = experts * words * 4 + experts * 4 + 9 * 4;
+  const int small = 2 * kPrepThreads * 4;  // group_small's two arrays
+  return general > small ? general : small;
 }
 
 int prep_quant_blocks(int batch, int hidden) {

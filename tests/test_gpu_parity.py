@@ -158,6 +158,26 @@ def test_group_matches_oracle_exactly(moe, name):
     np.testing.assert_array_equal(rows, ref_rows)
 
 
+@pytest.mark.parametrize("batch", [16, 17])
+def test_grouping_paths_at_the_small_batch_threshold(moe, batch):
+    """Up to 16 tokens the grouping block takes its one-pair-per-thread path,
+    above it the general one. Zipf ids over 32 experts give experts with more
+    than 8 pairs, so both paths must split them into several units."""
+    weights, _, _ = cached_inputs("tiny")
+    x = workload.make_x(batch, 256, seed=7)
+    ids = workload.make_ids(batch, 32, seed=11, dist="zipf", s=1.1)
+    assert np.bincount(ids.ravel(), minlength=32).max() > 8
+    layer = layer_for(moe, weights)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    experts, rows = units_of(moe, layer, batch)
+    ref_experts, ref_rows = oracle.group(ids, layer.experts)
+    np.testing.assert_array_equal(experts, ref_experts)
+    np.testing.assert_array_equal(rows, ref_rows)
+    xq, xs = oracle.quantize_x(x)
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], f"tiny B{batch} zipf")
+
+
 def oracle_pairs_for(name, weights, x, ids):
     if name == "tp8_b256":  # every pair of 64 tokens, including the x50 outlier rows
         outliers = np.flatnonzero(np.abs(bf16_to_float(x)).max(axis=1) > 20)
