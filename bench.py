@@ -228,10 +228,19 @@ class OurArm:
         self.ids = torch.from_numpy(ids_np).to(self.device)
         self.out = torch.empty((B, 16, cfg.hidden), dtype=torch.bfloat16, device=self.device)
         self.io_bytes = {"x": B * cfg.hidden * 2, "ids": B * 16 * 4, "out": B * 16 * cfg.hidden * 2}
+        # Routing weights for the combined call: positive, summing to one per token.
+        rw = np.random.default_rng(5).random((B, 16)).astype(np.float32) + 0.1
+        self.rw = torch.from_numpy(rw / rw.sum(axis=1, keepdims=True)).to(self.device)
+        self.out_combined = torch.empty((B, cfg.hidden), dtype=torch.bfloat16, device=self.device)
+        self.combined = False
 
     def call(self, i):
         layer = self.layers[i % self.R]
-        self.moe.moe_run(layer.handle, self.x, self.ids, self.out, self.cfg.batch)
+        if self.combined:
+            self.moe.moe_run_combined(layer.handle, self.x, self.ids, self.rw, self.out_combined,
+                                      self.cfg.batch)
+        else:
+            self.moe.moe_run(layer.handle, self.x, self.ids, self.out, self.cfg.batch)
 
     def check_status(self):
         for layer in self.layers:
@@ -427,12 +436,9 @@ def run_ours(args, rank, world, local):
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(cfg, weights, x, ids)
     if not args.no_extra:
-        extra = {}
-        for name in EXTRA_CONFIGS:
-            c = workload.CONFIGS[name]
-            w, xx, ii = inputs(c)
-            a = OurArm(c, device)
-            a.setup(w, xx, ii, l2_bytes)
+        def graph_us(a, combined):
+            """us per call of a graph of back-to-back calls (moe_run or moe_run_combined)."""
+            a.combined = combined
             for i in range(max(3, args.warmup)):
                 a.call(i)
             a.check_status()
@@ -442,10 +448,29 @@ def run_ours(args, rank, world, local):
             gg.replay()
             reps = max(1, math.ceil(200 / calls))
             ms = a.time_graphs([(gg, reps)], reps * calls)
+            a.check_status()
+            a.combined = False
+            return ms * 1e3
+
+        extra = {}
+        for name in [args.config] + EXTRA_CONFIGS:
+            c = workload.CONFIGS[name]
+            w, xx, ii = inputs(c)
+            a = OurArm(c, device)
+            a.setup(w, xx, ii, l2_bytes)
+            combined_us = graph_us(a, True)
+            if name == args.config:
+                extra[name + " combined"] = {
+                    "workload": describe(c) + ", routing-weighted combine to [B, H]",
+                    "us_per_call": round(combined_us, 3)}
+                a.close()
+                continue
+            ms = graph_us(a, False) * 1e-3
             kms = a.experts_kernel_ms(30)
             a.check_status()
             extra[name] = {
                 "workload": describe(c), "us_per_call": round(ms * 1e3, 3),
+                "combined_us_per_call": round(combined_us, 3),
                 "touched_weight_bytes": a.touched,
                 "touched_gbs": round(a.touched / (ms * 1e-3) / 1e9, 1),
                 "touched_frac_of_peak": round(a.touched / (ms * 1e-3) / 1e9 / peak, 4),
@@ -454,7 +479,6 @@ def run_ours(args, rank, world, local):
                 "replicas": a.R,
             }
             a.close()
-            del gg
         result["configs"] = extra
     if world > 1:
         torch.distributed.destroy_process_group()

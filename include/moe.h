@@ -140,6 +140,24 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
             void* stream);
 
 /*
+ * moe_run_combined - moe_run, then the routing-weighted combine of each
+ * token's 16 rows into one.
+ * Source: [experts] ExpertsKernel.finalize (its single-GPU part: the 16 BF16
+ * rows of a token are summed with their routing weights as FP32
+ * multiply-adds in slot order and stored once per token).
+ *   out[t, n] = bf16_rne(sum over s = 0..15 of w[t, s] * row[t, s, n]),
+ * row[t, s, :] being the BF16 row moe_run would write for pair (t, s); pairs
+ * the grouping dropped (bad or repeated ids) are left out of the sum.
+ *   topk_weights  device, float32 [batch, 16], 16-byte aligned
+ *   out_bf16      device, BF16 [batch, H]
+ * The per-pair rows go to a handle-owned buffer, not to the caller. Same
+ * stream semantics and errors as moe_run (a third kernel runs after the
+ * experts kernel).
+ */
+int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
+                     const float* topk_weights, void* out_bf16, int batch, void* stream);
+
+/*
  * moe_experts - kernels 3 and 4 alone: the persistent experts kernel and its
  * output epilogue, on the plan and unit table that moe_quantize and
  * moe_group (called in that order, with the same batch, on the same stream)

@@ -16,11 +16,11 @@ from .build import LIBRARY
 
 __all__ = [
     "MoeError", "MoeInfo", "MoeLayer", "library", "moe_prepare", "moe_quantize", "moe_group",
-    "moe_run", "moe_experts", "moe_run_noalloc", "moe_run_host", "moe_sync_status",
-    "moe_copy_plan", "moe_copy_units", "moe_copy_hidden", "moe_set_timeout", "moe_debug_withhold", "moe_info", "moe_destroy",
-    "moe_error_string", "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA",
-    "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS", "MOE_ERR_STATE", "TOPK", "UNIT_ROWS",
-    "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
+    "moe_run", "moe_experts", "moe_run_noalloc", "moe_run_combined", "moe_run_host",
+    "moe_sync_status", "moe_copy_plan", "moe_copy_units", "moe_copy_hidden", "moe_set_timeout",
+    "moe_debug_withhold", "moe_info", "moe_destroy", "moe_error_string", "MOE_OK", "MOE_ERR_ARG",
+    "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
+    "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
     "MAX_BATCH",
 ]
 
@@ -55,6 +55,7 @@ def _load():
         "moe_run": ([vp, vp, vp, vp, i32, vp], i32),
         "moe_experts": ([vp, vp, i32, vp], i32),
         "moe_run_noalloc": ([vp, vp, vp, vp, i32, vp], i32),
+        "moe_run_combined": ([vp, vp, vp, vp, vp, i32, vp], i32),
         "moe_run_host": ([vp, vp, vp, vp, i32, vp], i32),
         "moe_sync_status": ([vp, vp], i32),
         "moe_copy_plan": ([vp, vp, vp, i32], i32),
@@ -147,6 +148,12 @@ def moe_run(handle, x, ids, out, batch: int, stream=None):
 
 def moe_experts(handle, out, batch: int, stream=None):
     return _check(_lib.moe_experts(handle, _ptr(out), batch, _stream(stream)), "moe_experts")
+
+
+def moe_run_combined(handle, x, ids, weights, out, batch: int, stream=None):
+    """moe_run, then out[t] = bf16(sum_s weights[t, s] * row[t, s]) (out: [B, H])."""
+    return _check(_lib.moe_run_combined(handle, _ptr(x), _ptr(ids), _ptr(weights), _ptr(out),
+                                        batch, _stream(stream)), "moe_run_combined")
 
 
 def moe_run_noalloc(handle, x, ids, out, batch: int, stream=None):

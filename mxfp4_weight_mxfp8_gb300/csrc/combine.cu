@@ -1,0 +1,67 @@
+// Routing-weighted combine (the single-GPU half of the pages' finalize step).
+//
+// Page: ...cutedsl.moe.experts, ExpertsKernel.finalize: every token's 16
+// staged BF16 rows are summed with their routing weights, slot by slot, as
+// FP32 multiply-adds, and the sum is stored once per token. Here the rows are
+// the per-pair output of the run; pairs the grouping dropped (bad or
+// repeated ids) wrote no row and are skipped. The result is rounded to BF16
+// (nearest even).
+//
+// One thread per 8 consecutive outputs of a token: a 16-byte load of each
+// slot's row, eight FP32 accumulators, one 16-byte store.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+  ptx::grid_dependency_wait();  // the experts grid's rows
+  const int per_token = a.H / 8;
+  const int i = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (i >= a.B * per_token) return;
+  const int t = i / per_token, n = (i - t * per_token) * 8;
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < kTopK; ++s) {
+    const int p = t * kTopK + s;
+    if (!a.kept[p]) continue;
+    const float w = a.weights[p];
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.rows + static_cast<size_t>(p) * a.H + n));
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[2 * k] = fmaf(__uint_as_float(words[k] << 16), w, acc[2 * k]);
+      acc[2 * k + 1] = fmaf(__uint_as_float(words[k] & 0xFFFF0000u), w, acc[2 * k + 1]);
+    }
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    packed[k] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k]))) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k + 1]))) << 16);
+  *reinterpret_cast<uint4*>(a.out + static_cast<size_t>(t) * a.H + n) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+  const int threads = a.B * (a.H / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((threads + kCombineThreads - 1) / kCombineThreads);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+}
+
+}  // namespace moe

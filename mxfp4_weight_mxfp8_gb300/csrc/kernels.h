@@ -20,6 +20,7 @@ struct PrepArgs {
   int16_t* unit_rows;       // [unit_cap, 8]
   uint32_t* item_counters;  // [unit_cap * P1], cleared per call
   uint32_t* hidden_flags;   // [unit_cap * KC2], cleared per call
+  uint8_t* pair_kept;       // [B * 16] or null: 1 where the pair got a unit row
   int32_t* status;
   int roles;
   int quant_blocks;
@@ -54,6 +55,17 @@ bool experts_layout_aligned(const Geometry& g);
 cudaError_t experts_configure(const Geometry& g);
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
+
+// Routing-weighted combine of each token's 16 rows (after the experts kernel).
+struct CombineArgs {
+  const uint16_t* rows;     // BF16 [B * 16, H]: the per-pair rows of the run
+  const float* weights;     // [B, 16]
+  const uint8_t* kept;      // [B * 16]: 1 where the pair's row was written
+  uint16_t* out;            // BF16 [B, H]
+  int B, H;
+};
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
 // Weight repack into stage blocks.
 cudaError_t launch_repack(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,

@@ -29,6 +29,8 @@ struct moe_ctx {
   float* partials = nullptr;
   uint8_t* hidden = nullptr;
   int32_t* status = nullptr;
+  uint8_t* pair_kept = nullptr;  // [MOE_MAX_BATCH * 16]
+  uint16_t* staged = nullptr;    // BF16 [MOE_MAX_BATCH * 16, H]: moe_run_combined's per-pair rows
   uint8_t* io = nullptr;  // device buffers of moe_run_host (x, ids, out), made on first use
   CUtensorMap wmap{};
   uint64_t timeout_ns = 2000000000ull;
@@ -177,9 +179,11 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
       static_cast<size_t>(h->unit_cap) * g.hidden_bytes,        // hidden images
       4,                                                        // status
+      static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
+      static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
   };
-  size_t offsets[10], total = 0;
-  for (int i = 0; i < 10; ++i) {
+  size_t offsets[12], total = 0;
+  for (int i = 0; i < 12; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -197,6 +201,8 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->partials = reinterpret_cast<float*>(w + offsets[7]);
   h->hidden = w + offsets[8];
   h->status = reinterpret_cast<int32_t*>(w + offsets[9]);
+  h->pair_kept = w + offsets[10];
+  h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
   return encode_weight_map(h);
 }
 
@@ -217,6 +223,7 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
   a.unit_rows = h->unit_rows;
   a.item_counters = h->item_counters;
   a.hidden_flags = h->hidden_flags;
+  a.pair_kept = h->pair_kept;
   a.status = h->status;
   a.roles = roles;
   a.quant_blocks = moe::prep_quant_blocks(batch, h->g.H);
@@ -303,6 +310,25 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
   h->group_batch = batch;
   h->grouped = 1;
   h->ran = 1;
+  return MOE_OK;
+}
+
+int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
+                     const float* topk_weights, void* out_bf16, int batch, void* stream) {
+  if (h == nullptr || !x_bf16 || !topk_ids || !topk_weights || !out_bf16) return MOE_ERR_ARG;
+  if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(topk_weights) ||
+      !aligned16(out_bf16) || check_batch(batch))
+    return MOE_ERR_ARG;
+  const int rc = moe_run(h, x_bf16, topk_ids, h->staged, batch, stream);
+  if (rc != MOE_OK) return rc;
+  moe::CombineArgs c{};
+  c.rows = h->staged;
+  c.weights = topk_weights;
+  c.kept = h->pair_kept;
+  c.out = static_cast<uint16_t*>(out_bf16);
+  c.B = batch;
+  c.H = h->g.H;
+  MOE_CUDA(moe::launch_combine(c, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

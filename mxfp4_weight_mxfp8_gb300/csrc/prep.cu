@@ -102,6 +102,7 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
       }
     }
     kept_bits |= static_cast<uint32_t>(kept) << it;
+    if (a.pair_kept != nullptr && p < pairs) a.pair_kept[p] = kept ? 1 : 0;
   }
   __syncthreads();
 
@@ -190,6 +191,7 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
     }
   }
   __syncthreads();
+  if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   key[tid] = kept ? e : 0x7FFFFFFF;
   __syncthreads();
   int n = 0, before = 0;

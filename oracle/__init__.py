@@ -11,7 +11,8 @@ What it computes (pages: ``...cutedsl.moe.experts`` and
 rule); per (token, slot) pair with expert e = ids[t, s]: FC1 against e's
 MXFP4 gate+up rows, SiLU(gate) * up, MXFP8 requant of the hidden row (floor
 rule iff 2I == 768), FC2 against e's MXFP4 down rows, BF16 (RNE) output row
-``t * 16 + s``. Sums are exact-order float64 loops.
+``t * 16 + s``; and the routing-weighted combine of a token's 16 rows
+(ExpertsKernel.finalize). Sums are exact-order float64 loops.
 """
 from __future__ import annotations
 
@@ -60,6 +61,9 @@ def _library():
         lib.orc_fc2_rows.argtypes = [u8p, u8p, c_int, c_int, c_int, i32p, u8p, u8p, c_int, u16p,
                                      c_int]
         lib.orc_fc2_rows.restype = None
+        f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+        lib.orc_combine.argtypes = [u16p, f32p, u8p, c_int, c_int, u16p]
+        lib.orc_combine.restype = None
         _lib = lib
     return _lib
 
@@ -186,4 +190,19 @@ def fc2_rows(w2, s2, experts, hq, hs, threads=None):
     _library().orc_fc2_rows(w2, s2, E, H, inter, experts, np.ascontiguousarray(hq, np.uint8),
                             np.ascontiguousarray(hs, np.uint8), n, out,
                             int(threads or default_threads()))
+    return out
+
+
+def combine(rows, weights, kept=None):
+    """Routing-weighted combine: rows uint16 BF16 [B*16, H] (pair t*16+s),
+    weights float32 [B, 16], kept uint8 [B*16] (default: all) -> uint16 BF16
+    [B, H] = bf16(sum_s w[t, s] * row[t, s]) in float64, skipped pairs left out."""
+    rows = np.ascontiguousarray(rows, np.uint16)
+    weights = np.ascontiguousarray(weights, np.float32)
+    B = weights.shape[0]
+    H = rows.shape[1]
+    assert rows.shape[0] == B * SLOTS
+    kept = np.ones(B * SLOTS, np.uint8) if kept is None else np.ascontiguousarray(kept, np.uint8)
+    out = np.zeros((B, H), np.uint16)
+    _library().orc_combine(rows, weights.reshape(-1), kept.reshape(-1), B, H, out)
     return out

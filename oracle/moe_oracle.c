@@ -325,3 +325,25 @@ void orc_fc2_rows(const uint8_t* w2, const uint8_t* s2, int E, int H, int I, con
     free(hv), free(o), free(wrow);
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Routing-weighted combine ([experts] ExpertsKernel.finalize, single GPU):  */
+/* out[t, n] = BF16( sum over s of w[t, s] * row[t, s, n] ), where row is   */
+/* the BF16 per-pair output and pairs that got no row (kept == 0) are left  */
+/* out. The sum is taken in float64, in slot order, and rounded once.       */
+/* Pinned by the "not gpu" tests (one-hot weights, zero weights, exact      */
+/* power-of-two scaling, cancellation, skipped pairs).                      */
+/* ------------------------------------------------------------------------ */
+void orc_combine(const uint16_t* rows, const float* weights, const uint8_t* kept, int B, int H,
+                 uint16_t* out) {
+  for (int t = 0; t < B; ++t)
+    for (int n = 0; n < H; ++n) {
+      double acc = 0.0;
+      for (int s = 0; s < ORC_SLOTS; ++s) {
+        const size_t p = (size_t)t * ORC_SLOTS + (size_t)s;
+        if (!kept[p]) continue;
+        acc += (double)weights[p] * orc_bf16_value(rows[p * (size_t)H + (size_t)n]);
+      }
+      out[(size_t)t * (size_t)H + (size_t)n] = orc_bf16_encode(acc);
+    }
+}

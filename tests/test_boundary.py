@@ -76,6 +76,7 @@ def test_calls_reject_null_handles_and_bad_batches(lib):
     assert raw.moe_run_host(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_experts(None, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_run_noalloc(None, p, p, p, 1, None) == lib.MOE_ERR_ARG
+    assert raw.moe_run_combined(None, p, p, p, p, 1, None) == lib.MOE_ERR_ARG
     assert raw.moe_sync_status(None, None) == lib.MOE_ERR_ARG
     assert raw.moe_copy_plan(None, p, p, 1) == lib.MOE_ERR_ARG
     assert raw.moe_copy_units(None, p, p, p, 1) == lib.MOE_ERR_ARG

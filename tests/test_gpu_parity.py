@@ -187,15 +187,45 @@ def oracle_pairs_for(name, weights, x, ids):
     return np.arange(ids.size, dtype=np.int32)
 
 
+_ORACLE_RUNS: dict = {}
+
+
+def oracle_run(name):
+    """(pairs, oracle outputs with hidden codes) of a config, computed once."""
+    if name not in _ORACLE_RUNS:
+        weights, x, ids = cached_inputs(name)
+        pairs = oracle_pairs_for(name, weights, x, ids)
+        xq, xs = oracle.quantize_x(x)
+        _ORACLE_RUNS[name] = (pairs, oracle.pairs_forward(weights, xq, xs, ids, pairs=pairs,
+                                                          want_hidden=True))
+    return _ORACLE_RUNS[name]
+
+
+def routing_weights(batch, seed=5):
+    """Positive float32 weights per token, summing to one (a softmax's shape)."""
+    w = np.random.default_rng(seed).random((batch, 16)).astype(np.float32) + 0.1
+    return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def run_combined(moe, layer, x_bits, ids, rw):
+    import torch
+
+    xd, idsd = to_device(x_bits, ids)
+    B = x_bits.shape[0]
+    wd = torch.from_numpy(rw).to("cuda:0")
+    out = torch.full((B, layer.hidden), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+    moe.moe_run_combined(layer.handle, xd, idsd, wd, out, B)
+    status = moe.moe_sync_status(layer.handle)
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), status
+
+
 @pytest.mark.parametrize("name", CONFIGS)
 def test_run_matches_oracle(moe, name):
     weights, x, ids = cached_inputs(name)
     layer = layer_for(moe, weights)
     got, status = run_layer(moe, layer, x, ids)
     assert status == moe.MOE_OK
-    pairs = oracle_pairs_for(name, weights, x, ids)
-    xq, xs = oracle.quantize_x(x)
-    ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=pairs, want_hidden=True)
+    pairs, ref = oracle_run(name)
     check_rows(got[pairs], ref["out"], name)
 
     # Hidden requant flips, unit row by unit row.
@@ -337,3 +367,34 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     assert status == moe.MOE_OK
     xq, xs = oracle.quantize_x(x)
     check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_run_combined_matches_oracle(moe, name):
+    """Routing-weighted combine (ExpertsKernel.finalize on one GPU) against the
+    oracle's combine of its own per-pair rows, on every token whose 16 pairs
+    the oracle ran."""
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    rw = routing_weights(x.shape[0])
+    got, status = run_combined(moe, layer, x, ids, rw)
+    assert status == moe.MOE_OK
+    pairs, ref = oracle_run(name)
+    tokens = pairs.reshape(-1, 16)[:, 0] // 16
+    assert np.array_equal(pairs.reshape(-1, 16), tokens[:, None] * 16 + np.arange(16))
+    check_rows(got[tokens], oracle.combine(ref["out"], rw[tokens]), f"{name} combined")
+
+
+def test_run_combined_leaves_out_dropped_pairs(moe):
+    weights, x, ids = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    bad = ids.copy()
+    bad[0, 7] = bad[0, 2]  # up to 16 tokens the lower slot of a repeat is kept
+    rw = routing_weights(x.shape[0], seed=9)
+    got, status = run_combined(moe, layer, x, bad, rw)
+    assert status == moe.MOE_ERR_DEVICE_IDS
+    kept = np.ones(32, np.uint8)
+    kept[7] = 0
+    xq, xs = oracle.quantize_x(x)
+    rows = oracle.pairs_forward(weights, xq, xs, bad)["out"]
+    check_rows(got, oracle.combine(rows, rw, kept), "tiny combined with a repeated id")

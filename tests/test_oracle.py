@@ -375,3 +375,76 @@ def test_fc2_with_unit_scales_is_a_matmul_of_decoded_codes():
         o = W[e] @ (E4M3[hq[e]] * 2.0 ** -7)
         expect = torch.from_numpy(o.astype(np.float32)).to(torch.bfloat16)
         assert torch.equal(torch.from_numpy(out[e].view(np.int16)).view(torch.bfloat16), expect)
+
+
+# --- routing-weighted combine (ExpertsKernel.finalize, single GPU) ----------
+
+def bf16_bits(values):
+    return torch.tensor(values, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def random_rows(rng, B, H):
+    """BF16 bits of N(0, 1) rows, with negatives and a few subnormal and huge values."""
+    x = rng.standard_normal((B * 16, H)).astype(np.float32)
+    x[:, :2] = np.float32(1e-39), np.float32(-3e38)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_combine_one_hot_weights_select_each_slot():
+    rng = np.random.default_rng(31)
+    B, H = 3, 40
+    rows = random_rows(rng, B, H)
+    for t in range(B):
+        for s in range(16):
+            w = np.zeros((B, 16), np.float32)
+            w[t, s] = 1.0
+            out = oracle.combine(rows, w)
+            np.testing.assert_array_equal(out[t], rows[t * 16 + s])
+            assert not out[np.arange(B) != t].any()  # other tokens: +0.0
+
+
+def test_combine_zero_weights_and_skipped_pairs_contribute_nothing():
+    rng = np.random.default_rng(32)
+    B, H = 2, 24
+    rows = random_rows(rng, B, H)
+    assert not oracle.combine(rows, np.zeros((B, 16), np.float32)).any()
+    w = np.ones((B, 16), np.float32)
+    assert not oracle.combine(rows, w, kept=np.zeros(B * 16, np.uint8)).any()
+    # Skipping a pair gives the sum over the others: pair 5 of token 1 carries
+    # a huge row that would dominate the sum.
+    rows2 = rows.copy()
+    rows2[16 + 5] = bf16_bits([1e30] * H)
+    kept = np.ones(B * 16, np.uint8)
+    kept[16 + 5] = 0
+    w = np.zeros((B, 16), np.float32)
+    w[1, 3] = 1.0
+    w[1, 5] = 1.0
+    np.testing.assert_array_equal(oracle.combine(rows2, w, kept)[1], rows2[16 + 3])
+
+
+def test_combine_power_of_two_weights_scale_exactly():
+    rng = np.random.default_rng(33)
+    B, H = 1, 64
+    x = (rng.standard_normal((16, H)) * 4).astype(np.float32)
+    rows = torch.from_numpy(x).to(torch.bfloat16)
+    w = np.zeros((B, 16), np.float32)
+    w[0, 9] = 0.25
+    got = torch.from_numpy(oracle.combine(rows.view(torch.int16).numpy().view(np.uint16), w).view(np.int16))
+    expect = (rows[9].float() * 0.25).to(torch.bfloat16)  # exact: normal values times 2^-2
+    assert torch.equal(got.view(torch.bfloat16)[0], expect)
+
+
+def test_combine_cancellation_and_a_worked_sum():
+    rng = np.random.default_rng(34)
+    H = 16
+    rows = random_rows(rng, 1, H)
+    rows[4] = rows[2]
+    w = np.zeros((1, 16), np.float32)
+    w[0, 2], w[0, 4] = 1.0, -1.0
+    assert not oracle.combine(rows, w).any()
+    # 0.5 * 1 + 0.25 * 2 + 0.25 * 4 = 2 exactly, on every column.
+    rows = np.zeros((16, H), np.uint16)
+    rows[0], rows[7], rows[15] = bf16_bits([1.0] * H), bf16_bits([2.0] * H), bf16_bits([4.0] * H)
+    w = np.zeros((1, 16), np.float32)
+    w[0, 0], w[0, 7], w[0, 15] = 0.5, 0.25, 0.25
+    np.testing.assert_array_equal(oracle.combine(rows, w)[0], bf16_bits([2.0] * H))
