@@ -291,7 +291,8 @@ void orc_pairs(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const 
     double* o = (double*)malloc(sizeof(double) * (size_t)H);
     uint8_t* codes = (uint8_t*)malloc((size_t)I);
     uint8_t* scales = (uint8_t*)malloc((size_t)(I / 32));
-    double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
+    /* one decoded weight row: FC1 rows hold H values, FC2 rows I */
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     for (int k = 0; k < H; ++k)
       xv[k] = E4M3_TABLE[xq[(size_t)token * H + k]] * E8M0_TABLE[xs[(size_t)token * (H / 32) + k / 32]];
     fc1(&W, e, xv, yy, wrow);

@@ -289,6 +289,29 @@ def test_partial_tiles_and_host_weights(moe):
     layer.close()
 
 
+@pytest.mark.parametrize("E,H,I,B,dist", [
+    (1024, 256, 64, 256, "uniform"),   # most experts, largest batch: 1,536 units
+    (16, 16384, 512, 2, "uniform"),    # largest hidden and intermediate sizes
+    (1024, 256, 512, 16, "zipf"),      # largest I with many experts
+    (16, 16384, 64, 4, "zipf"),        # largest hidden with the smallest I
+])
+def test_supported_limits(moe, E, H, I, B, dist):
+    """The edges of the supported shapes (include/moe.h): E <= 1024, H <= 16384,
+    I <= 512, B <= 256, against the oracle on every pair."""
+    weights = workload.make_weights(E, H, I, seed13=21, seed2=22)
+    import torch
+
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
+    x = workload.make_x(B, H, seed=23)
+    ids = workload.make_ids(B, E, seed=24, dist=dist)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids)
+    check_rows(got, ref["out"], f"E={E} H={H} I={I} B={B}")
+    layer.close()
+
+
 def test_repeated_expert_is_reported_and_others_kept(moe):
     weights, x, ids = cached_inputs("tiny")
     layer = layer_for(moe, weights)

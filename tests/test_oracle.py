@@ -327,8 +327,9 @@ def naive_pair(w13, s13, w2, s2, xq, xs, e, t, floor_rule):
     return np.array(y), np.array(hq, np.uint8), np.array(hs, np.uint8), np.array(o)
 
 
-@pytest.mark.parametrize("inter", [32, 64])
+@pytest.mark.parametrize("inter", [32, 64, 256])
 def test_pairs_against_naive_triple_loop(inter):
+    """inter = 256 > H: FC2 rows are longer than FC1 rows."""
     rng = np.random.default_rng(inter)
     E, H, B = 4, 64, 2
     weights = random_weights(rng, E, H, inter)
