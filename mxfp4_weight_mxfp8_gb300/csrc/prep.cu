@@ -194,20 +194,24 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   key[tid] = kept ? e : 0x7FFFFFFF;
   __syncthreads();
+  // Both loops read four pairs per 16-byte load (pairs is a multiple of 16).
+  const int4* key4 = reinterpret_cast<const int4*>(key);
+  const int4* nun4 = reinterpret_cast<const int4*>(nun);
   int n = 0, before = 0;
   if (kept)
-    for (int q = 0; q < pairs; ++q) {
-      const int same = key[q] == e;
-      n += same;
-      before += same & (q < tid);
+    for (int q = 0; q < pairs; q += 4) {
+      const int4 k = key4[q >> 2];
+      const int s0 = k.x == e, s1 = k.y == e, s2 = k.z == e, s3 = k.w == e;
+      n += s0 + s1 + s2 + s3;
+      before += (s0 & (q < tid)) + (s1 & (q + 1 < tid)) + (s2 & (q + 2 < tid)) + (s3 & (q + 3 < tid));
     }
   nun[tid] = (kept && before == 0) ? (n + 7) >> 3 : 0;
   __syncthreads();
   int units = 0, ubefore = 0;
-  for (int q = 0; q < pairs; ++q) {
-    const int v = nun[q];
-    units += v;
-    ubefore += key[q] < e ? v : 0;
+  for (int q = 0; q < pairs; q += 4) {
+    const int4 v = nun4[q >> 2], k = key4[q >> 2];
+    units += v.x + v.y + v.z + v.w;
+    ubefore += (k.x < e ? v.x : 0) + (k.y < e ? v.y : 0) + (k.z < e ? v.z : 0) + (k.w < e ? v.w : 0);
   }
   if (tid == 0) *a.unit_count = units;
   if (kept) {
