@@ -459,19 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
       // Wait (bounded) for every K chunk of the unit's hidden vector: lane l
-      // polls chunk l % KC2, so all chunks are polled at once and every lane
-      // holds an acquire before it reads the image.
-      // Relaxed polls, then one acquire fence before the image is read.
+      // polls chunk l % KC2 with acquire loads, so all chunks are polled at
+      // once; the warp barrier then orders every lane's image loads behind
+      // all of the lanes' acquires. (An acquire load costs less than a
+      // relaxed poll followed by a fence.)
       const uint64_t t_start = global_timer_ns();
       const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + (lane % g.KC2);
       for (uint32_t i = 0;; ++i) {
-        if (__all_sync(0xFFFFFFFFu, load_relaxed_gpu(flag) != 0)) break;
+        if (__all_sync(0xFFFFFFFFu, load_acquire_gpu(flag) != 0)) break;
         if ((i & 7u) == 7u && global_timer_ns() - t_start > a.timeout_ns) {
           if (lane == 0) report(a.status, MOE_ERR_DEVICE_TIMEOUT);
           break;  // proceed with whatever the image holds
         }
       }
-      fence_acquire_gpu();
+      __syncwarp();
       // The image (codes of every K chunk, then their scale atoms) in one
       // batch of independent 16-byte loads per lane: a single L2 round trip.
       const uint4* src = reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes);
@@ -611,13 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           uint32_t others = 0;
           for (; c_end < G && st[c_end] <= item_last; ++c_end) others += st[c_end] < st[c_end + 1];
           const uint64_t t_wait = global_timer_ns();
-          for (uint32_t i = 0; load_relaxed_gpu(&a.item_counters[item]) < others; ++i) {
+          // Every thread acquires the count itself before it loads partials.
+          for (uint32_t i = 0; load_acquire_gpu(&a.item_counters[item]) < others; ++i) {
             if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
               report(a.status, MOE_ERR_DEVICE_TIMEOUT);
               break;
             }
           }
-          fence_acquire_gpu();
           // Sum the pieces in CTA order, the owner's own piece first; the
           // loads of up to four pieces are issued together.
           for (int c0 = cta + 1; c0 < c_end; c0 += 4) {
