@@ -29,6 +29,7 @@ struct moe_ctx {
   float* partials = nullptr;
   uint8_t* hidden = nullptr;
   int32_t* status = nullptr;
+  int32_t* status_host = nullptr;  // pinned host word: the status read-back stays asynchronous
   uint8_t* pair_kept = nullptr;  // [MOE_MAX_BATCH * 16]
   uint16_t* staged = nullptr;    // BF16 [MOE_MAX_BATCH * 16, H]: moe_run_combined's per-pair rows
   uint8_t* io = nullptr;  // device buffers of moe_run_host (x, ids, out), made on first use
@@ -103,6 +104,7 @@ void release(moe_ctx* h) {
   cudaFree(h->stages);
   cudaFree(h->workspace);
   cudaFree(h->io);
+  cudaFreeHost(h->status_host);
   cudaSetDevice(current);
   delete h;
 }
@@ -203,6 +205,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->status = reinterpret_cast<int32_t*>(w + offsets[9]);
   h->pair_kept = w + offsets[10];
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
+  MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   return encode_weight_map(h);
 }
 
@@ -344,11 +347,10 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
 int moe_sync_status(moe_handle h, void* stream) {
   if (h == nullptr) return MOE_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t status = 0;
-  MOE_CUDA(cudaMemcpyAsync(&status, h->status, 4, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(h->status_host, h->status, 4, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemsetAsync(h->status, 0, 4, s));
   MOE_CUDA(cudaStreamSynchronize(s));
-  return status;
+  return *h->status_host;
 }
 
 int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void* out_host,
