@@ -246,9 +246,28 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
  * moe_debug_withhold - test hook: the unit with this index never publishes
  * its hidden vector, so its consumers' waits run out (-1 = off, the
  * default). Used to check the bounded waits without faulting the GPU.
+ * moe_debug_paths - test hook: 1 (the default) lets calls of one or two
+ * tokens run on the cluster variant of the experts kernel (one cluster of
+ * up to 8 CTAs per unit, partial sums and hidden chunks exchanged through
+ * distributed shared memory) where the layer's shape allows it; 0 sends
+ * every call to the grid kernel. The two cut the FC1 K range into split-K
+ * pieces at different stages, so their FP32 sums are grouped differently
+ * and may differ in the last bits. MOE_ERR_ARG for other values.
  */
 int moe_set_timeout(moe_handle h, uint64_t nanoseconds);
 int moe_debug_withhold(moe_handle h, int unit);
+int moe_debug_paths(moe_handle h, int allow_cluster);
+
+/*
+ * moe_cluster_size - the CTAs per thread-block cluster that a call of
+ * `batch` tokens on this layer runs on: on the cluster variant the largest
+ * size up to 8 of which one cluster per possible unit (min(E, 16 batch)) is
+ * resident at once; 0 on the grid kernel (more than two tokens, shapes
+ * whose split-K pieces do not fit the variant's receive buffer, too few
+ * resident clusters, or moe_debug_paths(h, 0)). -MOE_ERR_ARG for a null handle or a
+ * batch outside [1, MOE_MAX_BATCH].
+ */
+int moe_cluster_size(moe_handle h, int batch);
 
 int moe_info(moe_handle h, moe_info_t* info);
 

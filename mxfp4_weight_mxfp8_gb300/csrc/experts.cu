@@ -79,7 +79,7 @@ struct Layout {
 struct Split {
   int T1, J, KC2, G, T;
   bool balanced;
-  __device__ Split(int units, const Geometry& g, int grid) {
+  __host__ __device__ Split(int units, const Geometry& g, int grid) {
     T1 = units * g.P1 * g.KC1;
     J = units * g.NQ;
     KC2 = g.KC2;
@@ -88,11 +88,11 @@ struct Split {
     balanced = T / G >= KC2 * ((J + G - 1) / G);
   }
   // 32-bit products: T < 1.2M stages and c <= 256 for every supported layer.
-  __device__ int fc2_begin(int c) const {
+  __host__ __device__ int fc2_begin(int c) const {
     const uint32_t cu = static_cast<uint32_t>(c);
     return static_cast<int>(cu * static_cast<uint32_t>(J) / static_cast<uint32_t>(G));
   }
-  __device__ int fc1_begin(int c) const {
+  __host__ __device__ int fc1_begin(int c) const {
     if (c >= G) return T1;
     const uint32_t cu = static_cast<uint32_t>(c), gu = static_cast<uint32_t>(G);
     if (!balanced) return static_cast<int>(cu * static_cast<uint32_t>(T1) / gu);
@@ -113,6 +113,23 @@ __device__ bool wait_bar(const Ctx& cx, uint64_t* bar, uint32_t parity) {
   const uint64_t start = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*cx.abort_flag) return false;
+      if (global_timer_ns() - start > cx.a->timeout_ns) {
+        *cx.abort_flag = 1;
+        report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// wait_bar for barriers that other CTAs of the cluster arrive on.
+__device__ bool wait_bar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const uint64_t start = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_cluster(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*cx.abort_flag) return false;
       if (global_timer_ns() - start > cx.a->timeout_ns) {
@@ -716,18 +733,502 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant for calls of one or two tokens, where every unit is one
+// expert with at most two rows. One thread-block cluster of C CTAs runs one
+// unit: its FC1 stages and FC2 jobs are cut over the cluster's CTAs as the
+// kernel above cuts a call's work over the grid (the same Split). Nothing
+// goes through global memory between the two GEMMs:
+// - a CTA holding a later piece of an FC1 item stores its FP32 partial sums
+//   straight into the shared memory of the item's owner (the CTA holding the
+//   item's first stage) and arrives on the owner's mbarrier;
+// - the owner sums the pieces in CTA order, applies SiLU(gate) * up and the
+//   MXFP8 requant into its own hidden-chunk buffer, then sends the chunk to
+//   every other CTA of the cluster with shared-to-shared bulk copies counted
+//   on their mbarriers. It also writes the chunk to the global hidden image,
+//   which moe_copy_hidden reads back.
+// The FC2 weights stream into the ring while FC1 is reduced.
+
+constexpr int kClusterMaxRows = 2;  // rows of a unit in a call of one or two tokens
+
+// Unit-relative work of CTA `rank` of a C-CTA cluster: FC1 stages [f0, f1)
+// (stage s = item * KC1 + chunk) and FC2 jobs [j0, j1).
+struct ClusterRange {
+  int f0, f1, j0, j1;
+  __host__ __device__ ClusterRange(const Geometry& g, int rank, int C) {
+    const Split sp(1, g, C);
+    f0 = sp.fc1_begin(rank);
+    f1 = sp.fc1_begin(rank + 1);
+    j0 = sp.fc2_begin(rank);
+    j1 = sp.fc2_begin(rank + 1);
+  }
+};
+
+// The owner of FC1 item p (the CTA whose range holds the item's first
+// stage), how many later CTAs hold pieces of it, and the piece index of CTA
+// `rank` among them (-1 if it holds none).
+struct ItemPieces {
+  int owner, pieces, slot;
+  __host__ __device__ ItemPieces(const Geometry& g, int C, int p, int rank) : owner(-1), pieces(0), slot(-1) {
+    const int lo = p * g.KC1, hi = lo + g.KC1;
+    for (int r = 0; r < C; ++r) {
+      const ClusterRange cr(g, r, C);
+      if (cr.f1 <= cr.f0 || cr.f0 >= hi || cr.f1 <= lo) continue;
+      if (cr.f0 <= lo) {
+        owner = r;
+      } else {
+        if (r == rank) slot = pieces;
+        ++pieces;
+      }
+    }
+  }
+};
+
+// Partial sums of one piece in the owner's `out` region: [2 tiles][rows][128].
+__host__ __device__ constexpr int cluster_piece_bytes(int rows) { return 2 * rows * kTileM * 4; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    cluster_kernel(const __grid_constant__ ExpertsArgs a, const __grid_constant__ ClusterPlan plan) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const Geometry& g = a.g;
+  const Layout L(g.KC2);
+  uint8_t* W = sm + L.w;
+  uint8_t* ACT = sm + L.act;
+  uint8_t* ASF = sm + L.asf;
+  uint8_t* HC = sm + L.hcodes;   // the unit's hidden codes, chunk c at c * 1 KB
+  uint8_t* HSF = sm + L.hsf;     // their scale atoms, chunk c at c * 512 B
+  float* RECV = reinterpret_cast<float*>(sm + L.out);  // partial sums sent to this CTA
+  uint8_t* BSF = sm + L.bsf;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + S;
+  uint64_t* accfull = empty + S;
+  uint64_t* accempty = accfull + NACC;
+  uint64_t* recv = accempty + NACC;  // the other pieces of the item this CTA owns
+  uint64_t* hidden = recv + 1;       // every chunk of the unit's hidden vector
+  int4* meta = reinterpret_cast<int4*>(sm + L.meta);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = static_cast<int>(cluster_ctarank()), u = static_cast<int>(cluster_id_x());
+  Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
+  const int C = plan.C;
+  struct {
+    int f0, f1, j0, j1;
+  } cr = {plan.fc1[rank], plan.fc1[rank + 1], plan.fc2[rank], plan.fc2[rank + 1]};
+  const int T1 = g.P1 * g.KC1;
+  // The item whose first stage this CTA holds (at most one: a range is at
+  // most KC1 stages long), and the number of pieces other CTAs send it.
+  const int first_item = (cr.f0 + g.KC1 - 1) / g.KC1;
+  const bool owns = cr.f1 > cr.f0 && first_item * g.KC1 < cr.f1 && first_item < g.P1;
+  const int owned_pieces = owns ? plan.pieces[first_item] : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1 + 32);
+      mbar_init(&empty[s], kMmaWarps);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&accfull[i], kMmaWarps + 1);
+      mbar_init(&accempty[i], 4);
+    }
+    mbar_init(recv, owned_pieces > 0 ? owned_pieces * 128 : 1);  // every epilogue thread of a piece
+    mbar_init(hidden, 1 + (owns ? 1 : 0));  // the byte count below + this CTA's own chunk
+    misc[1] = 0;
+    fence_mbar_init();
+    // Chunks from the other owners arrive as bytes.
+    mbar_arrive_expect_tx(hidden, (g.P1 - (owns ? 1 : 0)) * kHiddenChunkBytes);
+    prefetch_tensormap(&a.wmap);
+  }
+  for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == kMmaWarp0) {
+    tmem_alloc(&misc[0], kTmemColumns);
+    tmem_relinquish();
+  }
+  // The plan and unit table of the preceding prep grid.
+  grid_dependency_wait();
+  const int units = *a.unit_count;
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = misc[0];
+  if (u >= units) {  // a cluster without a unit (the same for all its CTAs)
+    if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+    return;
+  }
+  // Every CTA's barriers are initialised before any CTA of the cluster
+  // touches another's shared memory: all threads arrive now, and the
+  // epilogue, the only role that reaches into other CTAs, waits before it
+  // starts (the other roles wait at the end).
+  cluster_arrive();
+  const int fc1_stages = T1;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_first();
+      const int e = a.unit_expert[u];
+      int n = 0, slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      auto issue = [&](int stage, bool stand_in) {
+        if (n >= S && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
+        mbar_arrive_expect_tx(&full[slot], kStageWeightBytes + 2 * kScaleAtomBytes);
+        if (stand_in) mbar_arrive_count(&full[slot], 32);
+        tma_load_3d(W + slot * kStageSmemWeights, &a.wmap, 0, 0, e * g.SPE + stage, &full[slot],
+                    policy);
+        bulk_load(ASF + slot * 2 * kScaleAtomBytes,
+                  a.stages + static_cast<size_t>(e * g.SPE + stage) * kStageBytes + kStageWeightBytes,
+                  2 * kScaleAtomBytes, &full[slot], policy);
+        ++n;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+        return true;
+      };
+      for (int st = cr.f0; st < cr.f1 && ok; ++st) ok = issue(st, false);
+      for (int q = cr.j0; q < cr.j1 && ok; ++q)
+        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(fc1_stages + q * g.KC2 + c, true);
+      if (ok) {
+        for (int k = (n > S ? n - S : 0); k < n; ++k)
+          if (!wait_bar(cx, &empty[k % S], (k / S) & 1)) break;
+      } else {
+        __nanosleep(50000);  // in-flight copies land before the CTA exits
+      }
+    }
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
+    // --------------------------------------------------------- MMA issuers
+    if (lane == 0) {
+      const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
+      const bool lead = issuer == 0;
+      int n = 0, slot = 0, k = 0, first_c = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      auto acquire = [&](int set) {
+        return k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
+      };
+      auto advance = [&]() {
+        ++n;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+      };
+      for (int st = cr.f0; st < cr.f1 && ok; ++st) {
+        const int p = st / g.KC1, c = st - p * g.KC1;
+        const bool first = (st == cr.f0) || (c == 0);
+        const bool last = (st == cr.f1 - 1) || (c == g.KC1 - 1);
+        const int set = k % NACC;
+        if (first) {
+          if (!(ok = acquire(set))) break;
+          first_c = c;
+        }
+        if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
+        tc_fence_after_sync();
+        const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+        tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+        tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
+        const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
+        const uint64_t dx = desc_sw128(ACT + slot * kActImageBytes + k0 * 32);
+        const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
+        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+        tc_commit(&empty[slot]);
+        advance();
+        if (last) {
+          if (lead) meta[set] = make_int4(0, u * g.P1 + p, first_c == 0, c == g.KC1 - 1);
+          tc_commit(&accfull[set]);
+          if (lead) mbar_arrive(&accfull[set]);
+          ++k;
+        }
+      }
+      // FC2 reads the whole hidden vector of the unit, sent by the owners.
+      if (ok && cr.j0 < cr.j1) {
+        ok = wait_bar_cluster(cx, hidden, 0);
+        tc_fence_after_sync();
+      }
+      for (int q = cr.j0; q < cr.j1 && ok; ++q) {
+        const int set = k % NACC;
+        if (!(ok = acquire(set))) break;
+        bool started = false;
+        for (int c = 0; c < g.KC2 && ok; ++c) {
+          if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+          tc_fence_after_sync();
+          const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
+          if (k0 < ksteps) {
+            const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+            tc_copy_scales(sf + 4, desc_scales(HSF + c * kScaleAtomBytes));
+            const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
+            const uint64_t dh = desc_sw128(HC + c * kActImageBytes + k0 * 32);
+            const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sf + 4, started ? 1u : 0u);
+            if (k0 + 1 < ksteps)
+              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+            started = true;
+          }
+          tc_commit(&empty[slot]);
+          advance();
+        }
+        if (!ok) break;
+        if (lead) meta[set] = make_int4(1, u * g.NQ + q, 0, 0);
+        tc_commit(&accfull[set]);
+        if (lead) mbar_arrive(&accfull[set]);
+        ++k;
+      }
+      if (lead) {
+        const int set = k % NACC;
+        if (k >= NACC) wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
+        meta[set] = make_int4(2, 0, 0, 0);
+        mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+      }
+    }
+  } else if (warp == kGatherWarp) {
+    // ------------------------------------------------ activation gather (FC1)
+    int n = 0, slot = 0;
+    uint32_t phase = 0;
+    const int pc = a.unit_rows[u * kUnitRows + (lane >> 2)];
+    const int ps = a.unit_rows[u * kUnitRows + (lane & 7)];
+    const int tok_code = pc >= 0 ? (pc >> 4) : -1;
+    const int tok_scale = ps >= 0 ? (ps >> 4) : -1;
+    for (int st = cr.f0; st < cr.f1; ++st) {
+      const int c = st % g.KC1;
+      if (n >= S) {
+        bool freed = true;
+        if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
+        if (!__shfl_sync(0xFFFFFFFFu, freed, 0)) break;
+      }
+      const int r = lane >> 2, piece = lane & 3;
+      uint8_t* img = ACT + slot * kActImageBytes;
+      const uint8_t* row = a.plan_codes + static_cast<size_t>(tok_code < 0 ? 0 : tok_code) * g.H +
+                           c * kChunkK;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c16 = piece * 2 + h;
+        cp_async_16(img + swizzle128(r, c16), row + c16 * 16, tok_code < 0 ? 0u : 16u);
+      }
+      if (lane < 8) {
+        const uint8_t* src = a.plan_scales +
+                             static_cast<size_t>(tok_scale < 0 ? 0 : tok_scale) * (g.H / kBlock) +
+                             c * (kChunkK / kBlock);
+        cp_async_4(BSF + slot * kScaleAtomBytes + lane * 16, src, tok_scale < 0 ? 0u : 4u);
+      }
+      cp_async_arrive_noinc(&full[slot]);
+      ++n;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1;
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp >= kEpilogueWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int et = tid - kEpilogueWarp0 * 32;
+    const int m = q * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+    const bool fc2_upper_half = g.I > 2 * kBlock;
+    int rows[kClusterMaxRows];  // the unit's pair rows (at most two in these calls)
+    int valid = 0;
+#pragma unroll
+    for (int r = 0; r < kClusterMaxRows; ++r) {
+      rows[r] = a.unit_rows[u * kUnitRows + r];
+      valid += rows[r] >= 0;
+    }
+    const int stride = cluster_piece_bytes(a.B) / 4;  // floats per piece slot
+    cluster_wait();
+    int k = 0;
+    for (;;) {
+      const int set = k % NACC;
+      if (!wait_bar(cx, &accfull[set], (k / NACC) & 1)) break;
+      tc_fence_after_sync();
+      const int4 md = meta[set];
+      if (md.x == 2) break;
+      float v0[8], v1[8], x0[8], x1[8];
+      {
+        uint32_t r0[8], r1[8], r2[8], r3[8];
+        const uint32_t base = tmem + lanes + set * kAccSetColumns;
+        tmem_load_8_async(base + 0, r0);
+        tmem_load_8_async(base + 8, r1);
+        tmem_load_8_async(base + 16, r2);
+        tmem_load_8_async(base + 24, r3);
+        tmem_wait_loads();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          v0[t] = __uint_as_float(r0[t]);
+          x0[t] = __uint_as_float(r1[t]);
+          v1[t] = __uint_as_float(r2[t]);
+          x1[t] = __uint_as_float(r3[t]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[set]);
+      ++k;
+      if (md.x == 0 || fc2_upper_half) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          v0[t] += x0[t];
+          v1[t] += x1[t];
+        }
+      }
+      if (md.x == 0) {
+        // ---- FC1 piece of item p: gate = v0, up = v1 for rows 128p + m.
+        const int p = md.y - u * g.P1;
+        if (!md.z) {
+          // A later piece: into the owner's shared memory, then its barrier.
+          const int owner = plan.owner[p], slot = plan.slot[p][rank];
+          if (owner >= 0 && slot >= 0) {
+            float* slot_base = RECV + slot * stride;
+#pragma unroll
+            for (int t = 0; t < kClusterMaxRows; ++t) {
+              if (t >= valid) break;
+              st_cluster_f32(cluster_map(slot_base + t * kTileM + m, owner), v0[t]);
+              st_cluster_f32(cluster_map(slot_base + (a.B + t) * kTileM + m, owner), v1[t]);
+            }
+            // Each thread's arrival releases its own stores.
+            mbar_arrive_remote(cluster_map(recv, owner));
+          }
+          continue;
+        }
+        if (!md.w && owned_pieces > 0) {
+          // Sum the other pieces in CTA order, after the owner's own.
+          if (wait_bar_cluster(cx, recv, 0)) {
+            for (int j = 0; j < owned_pieces; ++j) {
+              const float* src = RECV + j * stride;
+#pragma unroll
+              for (int t = 0; t < kClusterMaxRows; ++t) {
+                if (t >= valid) break;
+                v0[t] += src[t * kTileM + m];
+                v1[t] += src[(a.B + t) * kTileM + m];
+              }
+            }
+          }
+        }
+        // SiLU(gate) * up, MXFP8 per 32 hidden values, into this CTA's chunk p.
+        if (p * kTileM + q * 32 < g.I) {
+#pragma unroll
+          for (int t = 0; t < kClusterMaxRows; ++t) {
+            if (t >= valid) break;
+            const float h = silu_times(v0[t], v1[t]);
+            float amax = fabsf(h);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+            const int E = mx_exponent(amax, g.floor_rule != 0);
+            HC[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
+            if (lane == 0) HSF[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
+          }
+        }
+        fence_proxy_async_shared();  // generic writes, read by tensor-core and bulk copies
+        epilogue_sync();
+        if (et == 0 && u != a.withhold_unit) {
+          mbar_arrive(hidden);
+          for (int d = 0; d < C; ++d) {
+            if (d == rank) continue;
+            const uint32_t bar = cluster_map(hidden, d);
+            bulk_copy_to_peer(cluster_map(HC + p * kActImageBytes, d), HC + p * kActImageBytes,
+                              kActImageBytes, bar);
+            bulk_copy_to_peer(cluster_map(HSF + p * kScaleAtomBytes, d), HSF + p * kScaleAtomBytes,
+                              kScaleAtomBytes, bar);
+          }
+        }
+        // The global hidden image, for read-back.
+        uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
+        if (et < kActImageBytes / 16)
+          reinterpret_cast<uint4*>(img + p * kActImageBytes)[et] =
+              reinterpret_cast<const uint4*>(HC + p * kActImageBytes)[et];
+        else if (et < kActImageBytes / 16 + kScaleAtomBytes / 16)
+          reinterpret_cast<uint4*>(img + g.KC2 * kActImageBytes + p * kScaleAtomBytes)[et - kActImageBytes / 16] =
+              reinterpret_cast<const uint4*>(HSF + p * kScaleAtomBytes)[et - kActImageBytes / 16];
+      } else {
+        // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
+        const int qq = md.y - u * g.NQ;
+#pragma unroll
+        for (int t = 0; t < kClusterMaxRows; ++t) {
+          if (t >= valid) break;
+          uint16_t* dst = a.out + static_cast<size_t>(rows[t]) * g.H + qq * 2 * kTileM;
+          dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
+          dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
+        }
+      }
+    }
+  }
+
+  // No other CTA writes into this one's shared memory after the hidden
+  // vector is complete (bounded: a CTA that gave up exits all the same).
+  if (tid == 0 && !*cx.abort_flag) wait_bar_cluster(cx, hidden, 0);
+  if (warp < kEpilogueWarp0) cluster_wait();  // the start-up barrier
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+}
+
 }  // namespace
 
 int experts_smem_bytes(const Geometry& g) { return Layout(g.KC2).bytes; }
 
 bool experts_layout_aligned(const Geometry& g) { return Layout(g.KC2).aligned(); }
 
+namespace {
+int g_resident_clusters[9] = {};  // clusters of this many CTAs resident at once (0: none)
+}
+
 cudaError_t experts_configure(const Geometry& g) {
   // The attribute belongs to the kernel, not to a handle: allow the largest
   // layout any handle can need (I = 512), so every prepared layer launches.
   (void)g;
-  return cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Layout(kMaxInterChunks).bytes);
+  const int bytes = Layout(kMaxInterChunks).bytes;
+  cudaError_t e = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int C = 2; C <= 8; ++C) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    const cudaError_t q = cudaOccupancyMaxActiveClusters(&clusters, cluster_kernel, &cfg);
+    g_resident_clusters[C] = q == cudaSuccess ? clusters : 0;
+    if (q != cudaSuccess) cudaGetLastError();  // the grid kernel serves these calls then
+  }
+  return cudaSuccess;
+}
+
+// The largest cluster (at most 8 CTAs) of which one per possible unit is
+// resident at once, and whose work split the cluster kernel supports: each
+// CTA's FC1 range holds at most one item start, and the later pieces of
+// every item fit the owner's 4 KB receive region.
+int cluster_size_for(const Geometry& g, int batch) {
+  if (batch > kClusterMaxRows) return 0;
+  const int max_units = g.E < batch * kTopK ? g.E : batch * kTopK;
+  for (int C = 8; C >= 2; --C) {
+    if (g_resident_clusters[C] < max_units) continue;
+    bool ok = true;
+    for (int r = 0; r < C && ok; ++r) {
+      const ClusterRange cr(g, r, C);
+      ok = cr.f1 - cr.f0 <= g.KC1;
+    }
+    for (int p = 0; p < g.P1 && ok; ++p) {
+      const ItemPieces ip(g, C, p, -1);
+      ok = ip.owner >= 0 && ip.pieces * cluster_piece_bytes(batch) <= kUnitRows * 2 * kTileM * 2;
+    }
+    if (ok) return C;
+  }
+  return 0;
 }
 
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
@@ -735,17 +1236,51 @@ cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
                                                        experts_smem_bytes(g));
 }
 
-cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
+cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
+                           bool allow_cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = experts_smem_bytes(a.g);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  const int C = allow_cluster ? cluster_size_for(a.g, a.B) : 0;
+  if (C > 0) {
+    // One cluster per possible unit: at most min(E, 16B) in these calls.
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = C;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+    cfg.numAttrs = n;
+    const int max_units = a.g.E < a.B * kTopK ? a.g.E : a.B * kTopK;
+    cfg.gridDim = dim3(max_units * C);
+    ClusterPlan plan = {};
+    plan.C = C;
+    for (int r = 0; r <= C; ++r) {
+      const ClusterRange cr(a.g, r < C ? r : C - 1, C);
+      plan.fc1[r] = r < C ? cr.f0 : cr.f1;
+      plan.fc2[r] = r < C ? cr.j0 : cr.j1;
+    }
+    for (int p = 0; p < a.g.P1; ++p) {
+      for (int r = 0; r < 8; ++r) plan.slot[p][r] = -1;
+      for (int r = 0; r < C; ++r) {
+        const ItemPieces ip(a.g, C, p, r);
+        plan.owner[p] = ip.owner;
+        plan.pieces[p] = ip.pieces;
+        plan.slot[p][r] = static_cast<int8_t>(ip.slot);
+      }
+    }
+    return cudaLaunchKernelEx(&cfg, cluster_kernel, a, plan);
+  }
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, experts_kernel, a);
 }
 

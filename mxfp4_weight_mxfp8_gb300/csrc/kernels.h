@@ -45,6 +45,7 @@ struct ExpertsArgs {
   uint8_t* hidden;            // [unit_cap, hidden_bytes]
   uint16_t* out;              // BF16 [B * 16, H]
   int32_t* status;
+  int B;                      // tokens of the call
   Geometry g;
   uint64_t timeout_ns;
   int withhold_unit;          // test hook: never publish this unit's hidden (-1 = off)
@@ -54,7 +55,22 @@ int experts_smem_bytes(const Geometry& g);
 bool experts_layout_aligned(const Geometry& g);
 cudaError_t experts_configure(const Geometry& g);
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);
-cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
+// Work split of the cluster variant, computed on the host per launch: CTA r
+// of a cluster runs FC1 stages [fc1[r], fc1[r + 1]) and FC2 jobs
+// [fc2[r], fc2[r + 1]) of its unit; FC1 item p is owned by CTA owner[p],
+// which receives pieces[p] partial sums, CTA r's into slot[p][r] (-1: none).
+struct ClusterPlan {
+  int C;
+  int fc1[9], fc2[9];
+  int owner[kMaxInterChunks], pieces[kMaxInterChunks];
+  int8_t slot[kMaxInterChunks][8];
+};
+
+// One- and two-token calls run on thread-block clusters (one per unit) when
+// allow_cluster and the layer's shape fits that variant; all others on the grid.
+cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
+                           bool allow_cluster);
+int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serves this call
 
 // Routing-weighted combine of each token's 16 rows (after the experts kernel).
 struct CombineArgs {

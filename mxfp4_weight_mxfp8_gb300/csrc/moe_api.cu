@@ -36,6 +36,7 @@ struct moe_ctx {
   CUtensorMap wmap{};
   uint64_t timeout_ns = 2000000000ull;
   int withhold = -1;
+  int allow_cluster = 1;  // one- and two-token calls may run on the cluster variant
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
 };
 
@@ -235,7 +236,7 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
 
 int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE_OK : MOE_ERR_ARG; }
 
-int launch_experts(moe_ctx* h, void* out, cudaStream_t stream) {
+int launch_experts(moe_ctx* h, void* out, int batch, cudaStream_t stream) {
   moe::ExpertsArgs a{};
   a.wmap = h->wmap;
   a.stages = h->stages;
@@ -250,10 +251,11 @@ int launch_experts(moe_ctx* h, void* out, cudaStream_t stream) {
   a.hidden = h->hidden;
   a.out = static_cast<uint16_t*>(out);
   a.status = h->status;
+  a.B = batch;
   a.g = h->g;
   a.timeout_ns = h->timeout_ns;
   a.withhold_unit = h->withhold;
-  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true));
+  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->allow_cluster != 0));
   return MOE_OK;
 }
 
@@ -307,7 +309,7 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(moe::launch_prep(
       prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
-  const int rc = launch_experts(h, out_bf16, s);
+  const int rc = launch_experts(h, out_bf16, batch, s);
   if (rc != MOE_OK) return rc;
   h->plan_batch = batch;
   h->group_batch = batch;
@@ -339,7 +341,7 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
   if (h == nullptr || out_bf16 == nullptr || !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
   if (h->plan_batch != batch || h->group_batch != batch) return MOE_ERR_STATE;
-  const int rc = launch_experts(h, out_bf16, static_cast<cudaStream_t>(stream));
+  const int rc = launch_experts(h, out_bf16, batch, static_cast<cudaStream_t>(stream));
   if (rc == MOE_OK) h->ran = 1;
   return rc;
 }
@@ -439,6 +441,17 @@ int moe_debug_withhold(moe_handle h, int unit) {
   if (h == nullptr || unit < -1) return MOE_ERR_ARG;
   h->withhold = unit;
   return MOE_OK;
+}
+
+int moe_debug_paths(moe_handle h, int allow_cluster) {
+  if (h == nullptr || allow_cluster < 0 || allow_cluster > 1) return MOE_ERR_ARG;
+  h->allow_cluster = allow_cluster;
+  return MOE_OK;
+}
+
+int moe_cluster_size(moe_handle h, int batch) {
+  if (h == nullptr || check_batch(batch)) return -MOE_ERR_ARG;
+  return h->allow_cluster ? moe::cluster_size_for(h->g, batch) : 0;
 }
 
 int moe_info(moe_handle h, moe_info_t* info) {
@@ -583,10 +596,11 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.hidden = w + offsets[8];
   ea.out = static_cast<uint16_t*>(out_bf16);
   ea.status = h->status;  // read and cleared by moe_sync_status, as for moe_run
+  ea.B = batch;
   ea.g = g;
   ea.timeout_ns = h->timeout_ns;
   ea.withhold_unit = -1;
-  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true));
+  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->allow_cluster != 0));
   return MOE_OK;
 }
 

@@ -83,6 +83,8 @@ def test_calls_reject_null_handles_and_bad_batches(lib):
     assert raw.moe_copy_hidden(None, p, p, 1) == lib.MOE_ERR_ARG
     assert raw.moe_set_timeout(None, 5) == lib.MOE_ERR_ARG
     assert raw.moe_debug_withhold(None, 0) == lib.MOE_ERR_ARG
+    assert raw.moe_debug_paths(None, 1) == lib.MOE_ERR_ARG
+    assert raw.moe_cluster_size(None, 1) == -lib.MOE_ERR_ARG
     info = lib.MoeInfo()
     assert raw.moe_info(None, ctypes.byref(info)) == lib.MOE_ERR_ARG
     raw.moe_destroy(None)  # no-op

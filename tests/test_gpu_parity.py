@@ -377,19 +377,75 @@ def test_out_of_range_ids_are_reported_and_skipped(moe):
     check_rows(got[keep], ref["out"], "tiny with bad ids")
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(moe):
+@pytest.mark.parametrize("allow_cluster", [1, 0], ids=["cluster", "grid"])
+def test_bounded_wait_reports_timeout_and_context_survives(moe, allow_cluster):
     weights, x, ids = cached_inputs("tiny")
     layer = layer_for(moe, weights)
-    moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
-    moe.moe_debug_withhold(layer.handle, 0)        # unit 0 never publishes its hidden vector
-    _, status = run_layer(moe, layer, x, ids)
-    assert status == moe.MOE_ERR_DEVICE_TIMEOUT
-    moe.moe_debug_withhold(layer.handle, -1)
-    moe.moe_set_timeout(layer.handle, 0)
-    got, status = run_layer(moe, layer, x, ids)
-    assert status == moe.MOE_OK
+    moe.moe_debug_paths(layer.handle, allow_cluster)
+    try:
+        assert (moe.moe_cluster_size(layer.handle, x.shape[0]) > 0) == bool(allow_cluster)
+        moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
+        moe.moe_debug_withhold(layer.handle, 0)        # unit 0 never publishes its hidden vector
+        _, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_ERR_DEVICE_TIMEOUT
+        moe.moe_debug_withhold(layer.handle, -1)
+        moe.moe_set_timeout(layer.handle, 0)
+        got, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+    finally:
+        moe.moe_debug_withhold(layer.handle, -1)
+        moe.moe_set_timeout(layer.handle, 0)
+        moe.moe_debug_paths(layer.handle, 1)
     xq, xs = oracle.quantize_x(x)
     check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
+
+
+@pytest.mark.parametrize("name", ["tiny", "tp8_b1"])
+def test_cluster_and_grid_paths_for_one_and_two_tokens(moe, name):
+    """One- and two-token calls run on thread-block clusters (one per unit,
+    split-K partials and hidden chunks exchanged in distributed shared
+    memory); the grid kernel still serves them when that variant is off.
+    Both meet the oracle's tolerances, and they agree with each other up to
+    the rounding of their different split-K groupings."""
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    B = x.shape[0]
+    pairs, ref = oracle_run(name)
+    assert moe.moe_cluster_size(layer.handle, B) >= 2
+    clus, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    check_rows(clus[pairs], ref["out"], f"{name} cluster path")
+    moe.moe_debug_paths(layer.handle, 0)
+    try:
+        assert moe.moe_cluster_size(layer.handle, B) == 0
+        grid, status = run_layer(moe, layer, x, ids)
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
+    assert status == moe.MOE_OK
+    check_rows(grid[pairs], ref["out"], f"{name} grid path")
+    a = bf16_to_float(grid).astype(np.float64)
+    b = bf16_to_float(clus).astype(np.float64)
+    rel = np.linalg.norm(a - b) / max(np.linalg.norm(a), 1e-300)
+    print(f"[{name}] cluster vs grid: rel L2 {rel:.3e}")
+    assert rel <= 2e-3
+
+
+def test_cluster_path_at_two_tokens_with_shared_experts(moe):
+    """Two tokens routed to the same experts: every unit holds two rows, so
+    each split-K piece carries two rows of partial sums."""
+    weights, x, _ = cached_inputs("tp8_b1")
+    rng = np.random.default_rng(11)
+    x2 = np.concatenate([x, x[:1] ^ np.uint16(0x0001)], axis=0)  # a second, slightly different row
+    row = rng.permutation(weights[0].shape[0])[:16].astype(np.int32)
+    ids = np.stack([row, row[::-1]]).astype(np.int32)
+    layer = layer_for(moe, weights)
+    assert moe.moe_cluster_size(layer.handle, 2) >= 2
+    got, status = run_layer(moe, layer, x2, ids)
+    assert status == moe.MOE_OK
+    experts, rows = units_of(moe, layer, 2)
+    assert len(experts) == 16 and np.all(rows[:, 1] >= 0)
+    xq, xs = oracle.quantize_x(x2)
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tp8 two tokens, shared experts")
 
 
 @pytest.mark.parametrize("name", CONFIGS)
