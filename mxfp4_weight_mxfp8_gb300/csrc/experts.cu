@@ -847,9 +847,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&misc[0], kTmemColumns);
     tmem_relinquish();
   }
-  // The plan and unit table of the preceding prep grid.
+  // The plan and unit table of the preceding prep grid. The unit's expert
+  // (producer) and rows (gather warp) are read together with the unit count:
+  // one round trip. The table holds min(E, 16B) units, so these reads stay in
+  // bounds for every cluster.
   grid_dependency_wait();
   const int units = *a.unit_count;
+  int pre0 = 0, pre1 = 0;
+  if (warp == kProducerWarp) {
+    pre0 = a.unit_expert[u];
+  } else if (warp == kGatherWarp) {
+    pre0 = a.unit_rows[u * kUnitRows + (lane >> 2)];
+    pre1 = a.unit_rows[u * kUnitRows + (lane & 7)];
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -869,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      const int e = a.unit_expert[u];
+      const int e = pre0;
       int n = 0, slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -991,10 +1001,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ activation gather (FC1)
     int n = 0, slot = 0;
     uint32_t phase = 0;
-    const int pc = a.unit_rows[u * kUnitRows + (lane >> 2)];
-    const int ps = a.unit_rows[u * kUnitRows + (lane & 7)];
-    const int tok_code = pc >= 0 ? (pc >> 4) : -1;
-    const int tok_scale = ps >= 0 ? (ps >> 4) : -1;
+    const int tok_code = pre0 >= 0 ? (pre0 >> 4) : -1;
+    const int tok_scale = pre1 >= 0 ? (pre1 >> 4) : -1;
     for (int st = cr.f0; st < cr.f1; ++st) {
       const int c = st % g.KC1;
       if (n >= S) {
