@@ -16,7 +16,8 @@ L2, so no call finds its weights in the 126 MiB L2. The K timed calls are
 replayed from a CUDA graph (no host launch gaps), bracketed by a barrier and
 a device synchronize, timed with CUDA events. The experts kernel is timed
 alone (events around moe_experts, after moe_quantize + moe_group) for the
-roofline. e2e: moe_run_host with pinned host buffers (host->device copies of
+roofline: at one or two tokens that is the cluster variant (one thread-block
+cluster per unit), otherwise the persistent grid kernel. e2e: moe_run_host with pinned host buffers (host->device copies of
 x and ids, the call, the device->host copy of out, a synchronize) per step.
 
 --impl reference times the float64 CPU oracle (oracle/) on the host cores on
@@ -45,7 +46,7 @@ import workload  # noqa: E402
 MAIN_CONFIG = "tp8_b1"
 EXTRA_CONFIGS = ["tp16_b8", "tp8_b64", "tp8_b256"]
 L2_FALLBACK_BYTES = 126 * 2 ** 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "experts_kernel_tp8_b1.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "cluster_kernel_tp8_b1.md")
 KERNEL_SOURCES = ["experts.cu", "ptx.cuh", "common.cuh", "kernels.h"]
 
 
@@ -276,6 +277,13 @@ class OurArm:
         torch.cuda.synchronize()
         return start.elapsed_time(end) / calls
 
+    def kernel_label(self):
+        C = self.moe.moe_cluster_size(self.layers[0].handle, self.cfg.batch)
+        if C:
+            return (f"cluster_kernel (experts kernel on thread-block clusters of {C} CTAs, "
+                    "one per unit; tcgen05 block-scaled MMA)")
+        return "experts_kernel (persistent, tcgen05 block-scaled MMA)"
+
     def experts_kernel_ms(self, calls):
         """Mean device time of the experts kernel alone: moe_quantize and
         moe_group run first; CUDA events bracket only moe_experts. Every call is
@@ -417,7 +425,7 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(kernel_gbs / peak, 4),
             "traffic": traffic,
-            "kernel": "experts_kernel (persistent, tcgen05 block-scaled MMA)",
+            "kernel": arm.kernel_label(),
             "kernel_us": round(kernel_ms * 1e3, 3),
             "algorithmic_bytes": arm.touched,
             "peak_kind": f"{peak_kind} (copy bandwidth)",
