@@ -8,7 +8,9 @@
 // (nearest even).
 //
 // One thread per 8 consecutive outputs of a token: a 16-byte load of each
-// slot's row, eight FP32 accumulators, one 16-byte store.
+// slot's row (all issued together), eight FP32 accumulators, one 16-byte
+// store. The kept flags and weights of a token are 16-byte aligned (the
+// call checks the weights' alignment; the flags live in the workspace).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -23,20 +25,36 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
   const int i = blockIdx.x * kCombineThreads + threadIdx.x;
   if (i >= a.B * per_token) return;
   const int t = i / per_token, n = (i - t * per_token) * 8;
+  // Every load of the token's 16 slots is issued at once (one round trip):
+  // the kept flags, the weights and the rows. A dropped pair's row is stale
+  // and is never used: its slot is skipped, not multiplied by zero.
+  const uint4 kept4 = __ldg(reinterpret_cast<const uint4*>(a.kept + t * kTopK));
+  const float4* w4 = reinterpret_cast<const float4*>(a.weights + t * kTopK);
+  float w[kTopK];
+#pragma unroll
+  for (int j = 0; j < kTopK / 4; ++j) {
+    const float4 v = __ldg(w4 + j);
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  uint4 row[kTopK];
+#pragma unroll
+  for (int s = 0; s < kTopK; ++s)
+    row[s] = __ldg(reinterpret_cast<const uint4*>(a.rows + static_cast<size_t>(t * kTopK + s) * a.H + n));
+  const uint32_t kept_words[4] = {kept4.x, kept4.y, kept4.z, kept4.w};
   float acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll 4
+#pragma unroll
   for (int s = 0; s < kTopK; ++s) {
-    const int p = t * kTopK + s;
-    if (!a.kept[p]) continue;
-    const float w = a.weights[p];
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.rows + static_cast<size_t>(p) * a.H + n));
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    if (((kept_words[s >> 2] >> (8 * (s & 3))) & 0xFFu) == 0) continue;
+    const uint32_t words[4] = {row[s].x, row[s].y, row[s].z, row[s].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      acc[2 * k] = fmaf(__uint_as_float(words[k] << 16), w, acc[2 * k]);
-      acc[2 * k + 1] = fmaf(__uint_as_float(words[k] & 0xFFFF0000u), w, acc[2 * k + 1]);
+      acc[2 * k] = fmaf(__uint_as_float(words[k] << 16), w[s], acc[2 * k]);
+      acc[2 * k + 1] = fmaf(__uint_as_float(words[k] & 0xFFFF0000u), w[s], acc[2 * k + 1]);
     }
   }
   uint32_t packed[4];
