@@ -312,6 +312,60 @@ def test_supported_limits(moe, E, H, I, B, dist):
     layer.close()
 
 
+@pytest.mark.parametrize("E,H,I,B", [
+    (16, 512, 96, 1),      # partial tiles (I = 96), clusters of 6
+    (16, 512, 96, 2),      # two-row units; the piece layout allows only small clusters
+    (8, 3584, 384, 1),     # fewer experts than slots: 8 units, clusters of 8
+    (1024, 256, 512, 2),   # the widest I with the smallest H
+    (16, 16384, 512, 1),   # the largest H and I
+])
+def test_cluster_path_shapes(moe, E, H, I, B):
+    """The cluster variant over the shapes it accepts, against the oracle."""
+    weights = workload.make_weights(E, H, I, seed13=31, seed2=32)
+    import torch
+
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
+    C = moe.moe_cluster_size(layer.handle, B)
+    print(f"[E={E} H={H} I={I} B={B}] clusters of {C}")
+    assert C >= 2
+    x = workload.make_x(B, H, seed=33)
+    ids = workload.make_ids(B, E, seed=34) if E >= 16 else np.stack(
+        [np.random.default_rng(35 + t).permutation(16) % E for t in range(B)]).astype(np.int32)
+    got, status = run_layer(moe, layer, x, ids)
+    xq, xs = oracle.quantize_x(x)
+    if E >= 16:
+        assert status == moe.MOE_OK
+        ref = oracle.pairs_forward(weights, xq, xs, ids)
+        check_rows(got, ref["out"], f"cluster E={E} H={H} I={I} B={B}")
+    else:
+        # 16 slots over 8 experts: each expert twice per token, the higher slot dropped.
+        assert status == moe.MOE_ERR_DEVICE_IDS
+        keep = np.array([t * 16 + s for t in range(B) for s in range(16)
+                         if s == min(np.nonzero(ids[t] == ids[t, s])[0])], np.int32)
+        ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=keep)
+        check_rows(got[keep], ref["out"], f"cluster E={E} H={H} I={I} B={B}")
+    layer.close()
+
+
+def test_cluster_path_with_bad_and_repeated_ids(moe):
+    """One token whose ids include a repeat and an out-of-range id: 14 units,
+    so the last two clusters find no unit and leave at once."""
+    weights, x, ids = cached_inputs("tp8_b1")
+    layer = layer_for(moe, weights)
+    assert moe.moe_cluster_size(layer.handle, 1) >= 2
+    bad = ids.copy()
+    bad[0, 9] = bad[0, 4]   # a repeat: slot 9 is dropped
+    bad[0, 12] = 384        # out of range: slot 12 is dropped
+    got, status = run_layer(moe, layer, x, bad)
+    assert status == moe.MOE_ERR_DEVICE_IDS
+    experts, _ = units_of(moe, layer, 1)
+    assert len(experts) == 14
+    keep = np.array([s for s in range(16) if s not in (9, 12)], np.int32)
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, bad, pairs=keep)
+    check_rows(got[keep], ref["out"], "tp8 B1 with bad ids (cluster path)")
+
+
 def test_repeated_expert_is_reported_and_others_kept(moe):
     weights, x, ids = cached_inputs("tiny")
     layer = layer_for(moe, weights)
