@@ -162,8 +162,10 @@ int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
  * output epilogue, on the plan and unit table that moe_quantize and
  * moe_group (called in that order, with the same batch, on the same stream)
  * left in the handle. moe_quantize + moe_group + moe_experts computes
- * exactly what moe_run does. Source: [runtime] PersistentExperts.group / run
- * (a unit-table kernel launched ahead of the experts kernel).
+ * exactly what moe_run does. Each moe_experts call needs a moe_group of its
+ * own before it: the grouping clears the per-call counters and flags that
+ * the experts kernel consumes. Source: [runtime] PersistentExperts.group /
+ * run (a unit-table kernel launched ahead of the experts kernel).
  *   out_bf16  device BF16 [batch, 16, H], 16-byte aligned
  * Errors: MOE_ERR_ARG, MOE_ERR_STATE (no plan or unit table of this batch),
  * MOE_ERR_CUDA.

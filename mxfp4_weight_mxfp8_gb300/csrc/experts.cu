@@ -558,8 +558,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     auto unit_valid = [&](int u) -> int {
       const int i = cached(u);
       if (i >= 0) return cache_valid[i];
+      // Rows of a unit are its pairs, then -1 padding: one 16-byte load.
+      const int4 r4 = __ldcg(reinterpret_cast<const int4*>(a.unit_rows) + u);
+      const uint32_t w4[4] = {static_cast<uint32_t>(r4.x), static_cast<uint32_t>(r4.y),
+                              static_cast<uint32_t>(r4.z), static_cast<uint32_t>(r4.w)};
       int v = 0;
-      while (v < kUnitRows && a.unit_rows[u * kUnitRows + v] >= 0) ++v;
+#pragma unroll
+      for (int r = 0; r < kUnitRows; ++r) v += static_cast<int16_t>(w4[r >> 1] >> (16 * (r & 1))) >= 0;
       return v;
     };
     int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;

@@ -178,19 +178,14 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   int32_t* key = reinterpret_cast<int32_t*>(smem);  // [256]: expert of a kept pair, else INT_MAX
   int32_t* nun = key + kPrepThreads;                // [256]: units of the expert, on its first pair
   const int e = tid < pairs ? a.ids[tid] : -1;
-  key[tid] = e;
-  __syncthreads();
-  bool kept = false;
-  if (tid < pairs) {
-    if (e < 0 || e >= a.E) {
-      report(a.status, MOE_ERR_DEVICE_IDS);
-    } else {
-      kept = true;
-      for (int q = tid & ~(kTopK - 1); q < tid; ++q) kept = kept && key[q] != e;
-      if (!kept) report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within the token
-    }
-  }
-  __syncthreads();
+  // Lanes 0-15 and 16-31 of a warp hold the 16 slots of one token: a pair is
+  // kept when its id is in range and no lower lane of its token has the same
+  // id (out-of-range ids get a key of their own).
+  const int lane = tid & 31;
+  const bool valid = tid < pairs && e >= 0 && e < a.E;
+  const unsigned same = __match_any_sync(0xFFFFFFFFu, valid ? 2 * e + ((lane >> 4) & 1) : -1 - lane);
+  const bool kept = valid && __ffs(same) - 1 == lane;
+  if (tid < pairs && !kept) report(a.status, MOE_ERR_DEVICE_IDS);  // out of range or repeated
   if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   key[tid] = kept ? e : 0x7FFFFFFF;
   __syncthreads();
@@ -199,6 +194,7 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   const int4* nun4 = reinterpret_cast<const int4*>(nun);
   int n = 0, before = 0;
   if (kept)
+#pragma unroll 4
     for (int q = 0; q < pairs; q += 4) {
       const int4 k = key4[q >> 2];
       const int s0 = k.x == e, s1 = k.y == e, s2 = k.z == e, s3 = k.w == e;
@@ -208,6 +204,7 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   nun[tid] = (kept && before == 0) ? (n + 7) >> 3 : 0;
   __syncthreads();
   int units = 0, ubefore = 0;
+#pragma unroll 4
   for (int q = 0; q < pairs; q += 4) {
     const int4 v = nun4[q >> 2], k = key4[q >> 2];
     units += v.x + v.y + v.z + v.w;
