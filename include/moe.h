@@ -205,10 +205,13 @@ int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* topk_ids, v
                     int batch, void* stream);
 
 /*
- * moe_run_host - moe_run on host buffers: copies x and ids to handle-owned
- * device buffers, runs the layer and copies out back, all on `stream`, then
- * synchronizes the stream and returns moe_sync_status's result. Pinned host
- * memory makes the copies asynchronous DMA transfers.
+ * moe_run_host - moe_run on host buffers, on `stream`; synchronizes the
+ * stream and returns the call's device status (as moe_sync_status). Pinned,
+ * 16-byte aligned buffers on a GPU with native atomics on host memory (a
+ * coherent GPU-CPU link, as on Grace) are used in place: the prep grid reads
+ * x and ids from them and the experts kernel writes out into them, with no
+ * copies. Otherwise x and ids are copied to handle-owned device buffers and
+ * out is copied back.
  *   x_host BF16 [batch, H], ids_host int32 [batch, 16], out_host BF16
  *   [batch, 16, H]. Errors: as moe_run, plus device-side status.
  */

@@ -30,6 +30,8 @@ struct moe_ctx {
   uint8_t* hidden = nullptr;
   int32_t* status = nullptr;
   int32_t* status_host = nullptr;  // pinned host word: the status read-back stays asynchronous
+  int32_t* status_dev = nullptr;   // the word the kernels report into: status, or status_host
+  int host_atomics = 0;            // the GPU's atomics on host memory are native (coherent link)
   uint8_t* pair_kept = nullptr;  // [MOE_MAX_BATCH * 16]
   uint16_t* staged = nullptr;    // BF16 [MOE_MAX_BATCH * 16, H]: moe_run_combined's per-pair rows
   uint8_t* io = nullptr;  // device buffers of moe_run_host (x, ids, out), made on first use
@@ -141,6 +143,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     return MOE_ERR_UNSUPPORTED;
   }
   h->sms = prop.multiProcessorCount;
+  MOE_CUDA(cudaDeviceGetAttribute(&h->host_atomics, cudaDevAttrHostNativeAtomicSupported, h->device));
   MOE_CUDA(moe::experts_configure(g));
   int per_sm = 0;
   MOE_CUDA(moe::experts_occupancy(g, &per_sm));
@@ -207,6 +210,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->pair_kept = w + offsets[10];
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
+  h->status_dev = h->status;
   return encode_weight_map(h);
 }
 
@@ -228,7 +232,7 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
   a.item_counters = h->item_counters;
   a.hidden_flags = h->hidden_flags;
   a.pair_kept = h->pair_kept;
-  a.status = h->status;
+  a.status = h->status_dev;
   a.roles = roles;
   a.quant_blocks = moe::prep_quant_blocks(batch, h->g.H);
   return a;
@@ -250,7 +254,7 @@ int launch_experts(moe_ctx* h, void* out, int batch, cudaStream_t stream) {
   a.partials = h->partials;
   a.hidden = h->hidden;
   a.out = static_cast<uint16_t*>(out);
-  a.status = h->status;
+  a.status = h->status_dev;
   a.B = batch;
   a.g = h->g;
   a.timeout_ns = h->timeout_ns;
@@ -355,14 +359,37 @@ int moe_sync_status(moe_handle h, void* stream) {
   return *h->status_host;
 }
 
+bool is_pinned_host(const void* p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeHost && attr.devicePointer == p;
+}
+
 int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void* out_host,
                  int batch, void* stream) {
   if (h == nullptr || !x_host || !ids_host || !out_host || check_batch(batch)) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->host_atomics && aligned16(x_host) && aligned16(ids_host) && aligned16(out_host) &&
+      is_pinned_host(x_host) && is_pinned_host(ids_host) && is_pinned_host(out_host)) {
+    // Pinned buffers are mapped into the GPU's address space (the same
+    // pointers; coherent over the GPU-CPU link): the prep grid reads x and ids
+    // from them, the epilogue writes the rows into them, and the kernels
+    // report into a pinned status word, so the call makes no copies at all.
+    *reinterpret_cast<volatile int32_t*>(h->status_host) = 0;
+    h->status_dev = h->status_host;
+    const int rc = moe_run(h, x_host, ids_host, out_host, batch, stream);
+    h->status_dev = h->status;
+    if (rc != MOE_OK) return rc;
+    MOE_CUDA(cudaStreamSynchronize(s));
+    return *reinterpret_cast<volatile int32_t*>(h->status_host);
+  }
   const size_t xb = round256(static_cast<size_t>(MOE_MAX_BATCH) * h->g.H * 2);
   const size_t ib = round256(static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * 4);
   const size_t ob = static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * h->g.H * 2;
   if (h->io == nullptr) MOE_CUDA(cudaMalloc(&h->io, xb + ib + ob));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* dx = h->io;
   int32_t* dids = reinterpret_cast<int32_t*>(h->io + xb);
   uint8_t* dout = h->io + xb + ib;
@@ -595,7 +622,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.partials = reinterpret_cast<float*>(w + offsets[7]);
   ea.hidden = w + offsets[8];
   ea.out = static_cast<uint16_t*>(out_bf16);
-  ea.status = h->status;  // read and cleared by moe_sync_status, as for moe_run
+  ea.status = h->status_dev;  // read and cleared by moe_sync_status, as for moe_run
   ea.B = batch;
   ea.g = g;
   ea.timeout_ns = h->timeout_ns;

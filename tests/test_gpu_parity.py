@@ -392,6 +392,36 @@ def test_run_host_equals_device_run(moe):
     np.testing.assert_array_equal(outh.numpy().view(np.uint16).reshape(-1, 256), got)
 
 
+def test_run_host_in_place_and_copied(moe):
+    """moe_run_host on pinned buffers (used in place by the kernels) and on
+    pageable arrays (copied), each against moe_run; then a bad id through the
+    pinned path reports its status from the host-side status word."""
+    import torch
+
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    for step, batch in enumerate([8, 3, 1]):
+        x = workload.make_x(batch, 256, seed=400 + step)
+        ids = workload.make_ids(batch, 32, seed=500 + step)
+        want, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        idsh = torch.from_numpy(ids).pin_memory()
+        outh = torch.zeros((batch, 16, 256), dtype=torch.int16).pin_memory()
+        moe.moe_run_host(layer.handle, xh, idsh, outh, batch)
+        np.testing.assert_array_equal(outh.numpy().view(np.uint16).reshape(-1, 256), want)
+        out = np.zeros((batch, 16, 256), np.uint16)
+        moe.moe_run_host(layer.handle, x, ids, out, batch)
+        np.testing.assert_array_equal(out.reshape(-1, 256), want)
+    bad = ids.copy()
+    bad[0, 0] = 99
+    idsh = torch.from_numpy(bad).pin_memory()
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_run_host(layer.handle, xh, idsh, outh, 1)
+    assert err.value.code == moe.MOE_ERR_DEVICE_IDS
+    moe.moe_run_host(layer.handle, xh, torch.from_numpy(ids).pin_memory(), outh, 1)
+
+
 def test_quantize_group_experts_equals_run(moe):
     weights, x, ids = cached_inputs("tp16_b8")
     layer = layer_for(moe, weights)
