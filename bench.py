@@ -17,8 +17,13 @@ replayed from a CUDA graph (no host launch gaps), bracketed by a barrier and
 a device synchronize, timed with CUDA events. The experts kernel is timed
 alone (events around moe_experts, after moe_quantize + moe_group) for the
 roofline: at one or two tokens that is the cluster variant (one thread-block
-cluster per unit), otherwise the persistent grid kernel. e2e: moe_run_host with pinned host buffers (host->device copies of
-x and ids, the call, the device->host copy of out, a synchronize) per step.
+cluster per unit), otherwise the persistent grid kernel.
+
+e2e: moe_run_host with pinned host buffers per step. On a GPU with native
+atomics on host memory (Grace's coherent link) the kernels read x and ids from
+those buffers and write out into them in place; elsewhere the call copies
+them. Either way the input and output bytes cross between host and device
+inside the timed region, and a synchronize ends every step.
 
 --impl reference times the float64 CPU oracle (oracle/) on the host cores on
 the same workload: each step is one whole call.
