@@ -108,10 +108,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
                : "memory");
 }
 
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 // The two halves of a cluster barrier; every thread of every CTA arrives,
 // and waits before it arrives again.
 __device__ __forceinline__ void cluster_arrive() {
@@ -171,12 +167,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // --------------------------------------------------------------- cp.async
 // 16-byte gather; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
@@ -222,24 +212,6 @@ __device__ __forceinline__ uint32_t load_acquire_gpu(const uint32_t* p) {
 
 __device__ __forceinline__ void store_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint4 load_cg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 load_cg_f4(const void* p) {
-  float4 v;
-  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
 }
 
 // ------------------------------------------------------------------ TMEM
@@ -326,20 +298,6 @@ __device__ __forceinline__ void tmem_load_8_async(uint32_t taddr, uint32_t (&r)[
 
 __device__ __forceinline__ void tmem_wait_loads() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Eight consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_load_8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A = E2M1 (5),
