@@ -852,24 +852,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&misc[0], kTmemColumns);
     tmem_relinquish();
   }
-  // The plan and unit table of the preceding prep grid. The unit's expert
-  // (producer) and rows (gather warp) are read together with the unit count:
-  // one round trip. The table holds min(E, 16B) units, so these reads stay in
-  // bounds for every cluster.
-  grid_dependency_wait();
-  const int units = *a.unit_count;
-  int pre0 = 0, pre1 = 0;
-  if (warp == kProducerWarp) {
-    pre0 = a.unit_expert[u];
-  } else if (warp == kGatherWarp) {
-    pre0 = a.unit_rows[u * kUnitRows + (lane >> 2)];
-    pre1 = a.unit_rows[u * kUnitRows + (lane & 7)];
-  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = misc[0];
-  if (u >= units) {  // a cluster without a unit (the same for all its CTAs)
+  // Each warp waits for the prep grid only for what it reads itself: the
+  // unit count, and the unit's expert (producer) or rows (gather warp), in
+  // one round trip (the table holds min(E, 16B) units, so the reads stay in
+  // bounds for every cluster). Given the routing ids, the producer derives
+  // the unit count and its expert from them instead (one unit per distinct
+  // kept expert, ascending: the canonical table of one or two tokens) and
+  // streams weights while the prep grid still runs.
+  int units = 0, pre0 = 0, pre1 = 0;
+  if (warp == kProducerWarp && a.ids != nullptr) {
+    unsigned* bits = reinterpret_cast<unsigned*>(sm + L.table);  // kept experts, E <= 1024 bits
+    const int pairs = a.B * kTopK;  // 16 or 32: one pair per lane
+    const int e = lane < pairs ? a.ids[lane] : -1;
+    bits[lane] = 0;
+    const bool valid = lane < pairs && e >= 0 && e < g.E;
+    // Kept: the lowest slot of its token with that id (lanes 0-15, 16-31).
+    const unsigned in_token = __match_any_sync(0xFFFFFFFFu, valid ? 2 * e + (lane >> 4) : -1 - lane);
+    __syncwarp();
+    if (valid && __ffs(in_token) - 1 == lane) atomicOr(&bits[e >> 5], 1u << (e & 31));
+    __syncwarp();
+    // Unit u is the u-th set bit: a prefix count over the words, then the
+    // bit inside the word that holds it.
+    const unsigned word = bits[lane];
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int other = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += other;
+    }
+    units = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const unsigned who = __ballot_sync(0xFFFFFFFFu, u >= incl - cnt && u < incl);
+    const int w = who ? __ffs(who) - 1 : 0;
+    const int below = __shfl_sync(0xFFFFFFFFu, incl - cnt, w);
+    const unsigned ww = __shfl_sync(0xFFFFFFFFu, word, w);
+    pre0 = who ? w * 32 + static_cast<int>(__fns(ww, 0, u - below + 1)) : 0;
+  } else {
+    grid_dependency_wait();
+    units = *a.unit_count;
+    if (warp == kProducerWarp) {
+      pre0 = a.unit_expert[u];
+    } else if (warp == kGatherWarp) {
+      pre0 = a.unit_rows[u * kUnitRows + (lane >> 2)];
+      pre1 = a.unit_rows[u * kUnitRows + (lane & 7)];
+    }
+  }
+  if (u >= units) {  // a cluster without a unit (the same for all its CTAs and warps)
     if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
     return;
   }

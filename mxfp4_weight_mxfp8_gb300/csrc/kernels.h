@@ -34,6 +34,8 @@ int prep_group_smem_bytes(int experts);
 struct ExpertsArgs {
   CUtensorMap wmap;           // 3-D map over the stage blocks (first: 64-byte aligned)
   const uint8_t* stages;      // [E * SPE] blocks of kStageBytes
+  const int32_t* ids;         // [B, 16] routing ids of the call, or null: lets the cluster
+                              // variant's producer find its unit without the prep grid
   const uint8_t* plan_codes;  // [B, H]
   const uint8_t* plan_scales; // [B, H / 32]
   const int32_t* unit_count;

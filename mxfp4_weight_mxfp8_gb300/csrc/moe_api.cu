@@ -240,10 +240,13 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
 
 int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE_OK : MOE_ERR_ARG; }
 
-int launch_experts(moe_ctx* h, void* out, int batch, cudaStream_t stream) {
+// ids: the call's routing ids when the same call's prep grid runs just
+// before on this stream, else null.
+int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream) {
   moe::ExpertsArgs a{};
   a.wmap = h->wmap;
   a.stages = h->stages;
+  a.ids = ids;
   a.plan_codes = h->plan_codes;
   a.plan_scales = h->plan_scales;
   a.unit_count = h->unit_count;
@@ -313,7 +316,7 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(moe::launch_prep(
       prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
-  const int rc = launch_experts(h, out_bf16, batch, s);
+  const int rc = launch_experts(h, out_bf16, batch, topk_ids, s);
   if (rc != MOE_OK) return rc;
   h->plan_batch = batch;
   h->group_batch = batch;
@@ -345,7 +348,7 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
   if (h == nullptr || out_bf16 == nullptr || !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
   if (h->plan_batch != batch || h->group_batch != batch) return MOE_ERR_STATE;
-  const int rc = launch_experts(h, out_bf16, batch, static_cast<cudaStream_t>(stream));
+  const int rc = launch_experts(h, out_bf16, batch, nullptr, static_cast<cudaStream_t>(stream));
   if (rc == MOE_OK) h->ran = 1;
   return rc;
 }
@@ -612,6 +615,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   moe::ExpertsArgs ea{};
   ea.wmap = h->wmap;
   ea.stages = h->stages;
+  ea.ids = topk_ids;
   ea.plan_codes = pa.plan_codes;
   ea.plan_scales = pa.plan_scales;
   ea.unit_count = pa.unit_count;
