@@ -21,15 +21,20 @@
 //   warps 6-9  epilogue: FC1 -> split-K reduction, SiLU(gate) * up, MXFP8
 //              hidden requant, publish; FC2 -> BF16 rows with 16-byte stores
 //
-// Work split: the units are cut into two halves, A and B. Within each half,
-// FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256 output rows)
-// are cut into contiguous per-CTA ranges of near-equal bytes, and every CTA
-// runs FC1(A), FC1(B), FC2(A), FC2(B): half A's hidden vectors are reduced
-// and published while half B's FC1 weights stream.
+// Work split: FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256
+// output rows) are cut into contiguous per-CTA ranges of near-equal bytes,
+// and every CTA runs its FC1 range, then its FC2 range. Above 256 units the
+// units are cut into two halves, A and B, run as FC1(A), FC1(B), FC2(A),
+// FC2(B): half A's hidden vectors are reduced and published while half B's
+// FC1 weights stream.
 // An FC1 item split across CTAs is reduced by the CTA holding its first
 // stage: the others store FP32 partial sums and release-increment a counter
 // that the owner acquires; a fixed CTA order keeps the sum deterministic.
 // Every wait is bounded by a time limit.
+//
+// Calls of one or two tokens run on cluster_kernel (below) instead: one
+// thread-block cluster per unit, the same roles and stages, and the two
+// hand-offs through distributed shared memory.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -752,7 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 //   every other CTA of the cluster with shared-to-shared bulk copies counted
 //   on their mbarriers. It also writes the chunk to the global hidden image,
 //   which moe_copy_hidden reads back.
-// The FC2 weights stream into the ring while FC1 is reduced.
+// The FC2 weights stream into the ring while FC1 is reduced. The host computes
+// the per-rank work split (ClusterPlan). Given the routing ids, the producer
+// derives its unit from them and starts streaming before the prep grid ends;
+// every other warp waits for the prep grid only for what it reads itself.
 
 constexpr int kClusterMaxRows = 2;  // rows of a unit in a call of one or two tokens
 
