@@ -64,7 +64,7 @@ struct Layout {
     bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
     hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
     table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
-    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4) * 8;
+    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4 + kMmaWarps) * 8;
     meta = o = up(o, 16);  o += NACC * 16;
     misc = o = up(o, 16);  o += 16;
     rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
@@ -148,6 +148,40 @@ __device__ bool wait_bar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity) 
 
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// The epilogue warps' common decision on an accumulator: true only if every
+// one of the 128 threads passed its wait, so that no warp goes on into a
+// named barrier that another warp has left.
+__device__ __forceinline__ bool epilogue_all(bool ok) {
+  uint32_t r;
+  __syncwarp();
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait on a completion that is bound to come (this thread's own
+// tensor-core work), taken after a failure as well: the abort flag does not
+// end it.
+__device__ void wait_own(const Ctx& cx, uint64_t* bar, uint32_t parity) {
+  const uint64_t start = global_timer_ns();
+  for (uint32_t i = 1; !mbar_test(bar, parity); ++i) {
+    if ((i & 63u) == 0 && global_timer_ns() - start > cx.a->timeout_ns) {
+      report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// After a failed wait nobody waits for the copies still in flight into (or
+// out of) this CTA's shared memory: give them 50 us to land before it exits.
+__device__ void settle_copies() {
+  const uint64_t start = global_timer_ns();
+  while (global_timer_ns() - start < 50000) __nanosleep(1000);
+}
+
 // Release increment (no result): the caller's earlier stores, and those of
 // the threads it synchronized with, are visible to whoever acquires the count.
 __device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
@@ -223,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   uint64_t* accempty = accfull + NACC;
   uint64_t* hfull = accempty + NACC;
   uint64_t* hempty = hfull + 2;
+  uint64_t* drained = hempty + 2;  // [issuer]: its tensor-core work has finished
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort, last flag
 
@@ -243,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       mbar_init(&hfull[b], 1);
       mbar_init(&hempty[b], kMmaWarps);
     }
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
@@ -317,13 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
           for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
         }
-      if (ok) {
-        // Drain: every issued stage consumed and released before exit.
-        for (int k = (n > S ? n - S : 0); k < n; ++k)
-          if (!wait_bar(cx, &empty[k % S], (k / S) & 1)) break;
-      } else {
-        __nanosleep(50000);  // in-flight copies land before the CTA exits
-      }
+      // Drain: every issued stage consumed and released before exit.
+      if (ok)
+        for (int k = (n > S ? n - S : 0); k < n && ok; ++k) ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
+      if (!ok) settle_copies();
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
     // --------------------------------------------------------- MMA issuers
@@ -415,13 +448,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lead) mbar_arrive(&accfull[set]);
         ++k;
       }
-      // End marker for the epilogue (also after a timeout, so it exits).
-      if (lead) {
+      // End marker for the epilogue, only when every wait of this CTA has
+      // succeeded: after a failure the issuers may have stopped at different
+      // jobs, and a full-count arrival could overrun a barrier that another
+      // issuer's commit has reached. The epilogue then ends on the abort flag.
+      if (lead && ok && !*cx.abort_flag) {
         const int set = k % NACC;
-        if (k >= NACC) wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
-        meta[set] = make_int4(2, 0, 0, 0);
-        mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+        if (k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1)) {
+          meta[set] = make_int4(2, 0, 0, 0);
+          mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+        }
       }
+      // The tensor memory is freed only after every MMA and scale copy of
+      // this thread has finished (after a failure nobody else waits on them).
+      tc_commit(&drained[issuer]);
+      wait_own(cx, &drained[issuer], 0);
     }
   } else if (warp == kGatherWarp) {
     // ------------------------------- activation gather (FC1), hidden loader (FC2)
@@ -575,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;
     for (;;) {
       const int set = k % NACC;
-      if (!wait_bar(cx, &accfull[set], (k / NACC) & 1)) break;
+      if (!epilogue_all(wait_bar(cx, &accfull[set], (k / NACC) & 1))) break;
       tc_fence_after_sync();
       const int4 md = meta[set];
       if (md.x == 2) break;
@@ -820,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accempty = accfull + NACC;
   uint64_t* recv = accempty + NACC;  // the other pieces of the item this CTA owns
   uint64_t* hidden = recv + 1;       // every chunk of the unit's hidden vector
+  uint64_t* drained = hidden + 1;    // [issuer]: its tensor-core work has finished
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort
 
@@ -848,6 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(recv, owned_pieces > 0 ? owned_pieces * 128 : 1);  // every epilogue thread of a piece
     mbar_init(hidden, 1 + (owns ? 1 : 0));  // the byte count below + this CTA's own chunk
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
     misc[1] = 0;
     fence_mbar_init();
     // Chunks from the other owners arrive as bytes.
@@ -947,12 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = cr.f0; st < cr.f1 && ok; ++st) ok = issue(st, false);
       for (int q = cr.j0; q < cr.j1 && ok; ++q)
         for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(fc1_stages + q * g.KC2 + c, true);
-      if (ok) {
-        for (int k = (n > S ? n - S : 0); k < n; ++k)
-          if (!wait_bar(cx, &empty[k % S], (k / S) & 1)) break;
-      } else {
-        __nanosleep(50000);  // in-flight copies land before the CTA exits
-      }
+      if (ok)  // drain, as in the grid kernel
+        for (int k = (n > S ? n - S : 0); k < n && ok; ++k) ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
+      if (!ok) settle_copies();
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
     // --------------------------------------------------------- MMA issuers
@@ -1035,12 +1075,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lead) mbar_arrive(&accfull[set]);
         ++k;
       }
-      if (lead) {
+      if (lead && ok && !*cx.abort_flag) {  // as in the grid kernel
         const int set = k % NACC;
-        if (k >= NACC) wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
-        meta[set] = make_int4(2, 0, 0, 0);
-        mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+        if (k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1)) {
+          meta[set] = make_int4(2, 0, 0, 0);
+          mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+        }
       }
+      tc_commit(&drained[issuer]);
+      wait_own(cx, &drained[issuer], 0);
     }
   } else if (warp == kGatherWarp) {
     // ------------------------------------------------ activation gather (FC1)
@@ -1097,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0;
     for (;;) {
       const int set = k % NACC;
-      if (!wait_bar(cx, &accfull[set], (k / NACC) & 1)) break;
+      if (!epilogue_all(wait_bar(cx, &accfull[set], (k / NACC) & 1))) break;
       tc_fence_after_sync();
       const int4 md = meta[set];
       if (md.x == 2) break;
@@ -1217,8 +1260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kEpilogueWarp0) cluster_wait();  // the start-up barrier
   tc_fence_before_sync();
   __syncthreads();
+  // A CTA that gave up tells the others, so that every CTA of the cluster
+  // lets the copies between them land before it exits.
+  if (tid == 0 && *cx.abort_flag)
+    for (int d = 0; d < C; ++d) st_cluster_u32(cluster_map(&misc[1], d), 1u);
   cluster_sync();
   tc_fence_after_sync();
+  if (tid == 0 && *cx.abort_flag) settle_copies();
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
 }
 
