@@ -47,12 +47,13 @@ constexpr int S = kRingStages;
 constexpr int NACC = kAccSets;
 constexpr int kHalvesFrom = 256;  // more units than this: split them into halves A and B
 constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memory
+constexpr int kAgreeSlots = 2 * NACC;  // epilogue decisions in flight after an abort
 
 // Shared-memory carve-up. The swizzled operand images (weights, activation
 // and hidden codes) start on 1024-byte boundaries, every other region on a
 // 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
 struct Layout {
-  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, bytes;
+  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, bytes;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
   __host__ __device__ explicit Layout(int kc2) {
     int o = 0;
@@ -68,12 +69,13 @@ struct Layout {
     meta = o = up(o, 16);  o += NACC * 16;
     misc = o = up(o, 16);  o += 16;
     rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
+    agree = o = up(o, 16); o += kAgreeSlots * 4;
     bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }
   __host__ __device__ bool aligned() const {
     return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
            out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
-           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0;
+           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0 && agree % 16 == 0;
   }
 };
 
@@ -148,23 +150,9 @@ __device__ bool wait_bar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity) 
 
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// The epilogue warps' common decision on an accumulator: true only if every
-// one of the 128 threads passed its wait, so that no warp goes on into a
-// named barrier that another warp has left.
-__device__ __forceinline__ bool epilogue_all(bool ok) {
-  uint32_t r;
-  __syncwarp();
-  asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok))
-      : "memory");
-  return r != 0;
-}
-
 // Bounded wait on a completion that is bound to come (this thread's own
-// tensor-core work), taken after a failure as well: the abort flag does not
-// end it.
+// tensor-core work, or a barrier another thread has seen complete), taken
+// after a failure as well: the abort flag does not end it.
 __device__ void wait_own(const Ctx& cx, uint64_t* bar, uint32_t parity) {
   const uint64_t start = global_timer_ns();
   for (uint32_t i = 1; !mbar_test(bar, parity); ++i) {
@@ -173,6 +161,29 @@ __device__ void wait_own(const Ctx& cx, uint64_t* bar, uint32_t parity) {
       return;
     }
   }
+}
+
+// The epilogue threads' common decision on accumulator k (true: process it).
+// A thread that saw the barrier complete and then the abort flag still clear
+// goes on: the barrier completed before any abort. Any other thread calls
+// this: it tests the barrier once more and proposes to go on if it has
+// completed, to stop if not; the first proposal for k, kept by
+// compare-and-swap, decides for every such thread. The two kinds agree, as a
+// proposal to stop shows that the barrier had not completed when the abort
+// came. So no epilogue warp goes on into a named barrier that another has
+// left. A thread runs at most NACC accumulators ahead of another, so
+// 2 * NACC slots keep the decisions in flight apart.
+__device__ __noinline__ bool epilogue_agree(const Ctx& cx, uint64_t* bar, uint32_t parity, int k, int* agree) {
+  const int proposal = (k << 2) | (mbar_test(bar, parity) ? 1 : 2);
+  int* slot = agree + (k & (kAgreeSlots - 1));
+  int v = *reinterpret_cast<volatile int*>(slot);
+  while ((v >> 2) != k) {
+    const int w = atomicCAS(slot, v, proposal);
+    v = w == v ? proposal : w;
+  }
+  if ((v & 3) != 1) return false;
+  wait_own(cx, bar, parity);  // completed already: some thread saw it
+  return true;
 }
 
 // After a failed wait nobody waits for the copies still in flight into (or
@@ -258,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   uint64_t* hfull = accempty + NACC;
   uint64_t* hempty = hfull + 2;
   uint64_t* drained = hempty + 2;  // [issuer]: its tensor-core work has finished
+  int* agree = reinterpret_cast<int*>(sm + L.agree);
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort, last flag
 
@@ -278,11 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       mbar_init(&hfull[b], 1);
       mbar_init(&hempty[b], kMmaWarps);
     }
-    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
     prefetch_tensormap(&a.wmap);
+  } else if (warp == kMmaWarp0 + 1 && lane == 0) {
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
+    for (int i = 0; i < kAgreeSlots; ++i) agree[i] = -1;
+    fence_mbar_init();
   }
   for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
@@ -616,9 +631,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;
     for (;;) {
       const int set = k % NACC;
-      if (!epilogue_all(wait_bar(cx, &accfull[set], (k / NACC) & 1))) break;
+      // The metadata and the abort flag are read together, after the wait.
+      const bool seen = wait_bar(cx, &accfull[set], (k / NACC) & 1);
       tc_fence_after_sync();
-      const int4 md = meta[set];
+      int4 md = meta[set];
+      if (!seen || *cx.abort_flag) {
+        if (!epilogue_agree(cx, &accfull[set], (k / NACC) & 1, k, agree)) break;
+        tc_fence_after_sync();
+        md = meta[set];
+      }
       if (md.x == 2) break;
       float v0[8], v1[8], x0[8], x1[8];
       {
@@ -862,6 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* recv = accempty + NACC;  // the other pieces of the item this CTA owns
   uint64_t* hidden = recv + 1;       // every chunk of the unit's hidden vector
   uint64_t* drained = hidden + 1;    // [issuer]: its tensor-core work has finished
+  int* agree = reinterpret_cast<int*>(sm + L.agree);
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort
 
@@ -890,12 +912,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(recv, owned_pieces > 0 ? owned_pieces * 128 : 1);  // every epilogue thread of a piece
     mbar_init(hidden, 1 + (owns ? 1 : 0));  // the byte count below + this CTA's own chunk
-    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
     misc[1] = 0;
     fence_mbar_init();
     // Chunks from the other owners arrive as bytes.
     mbar_arrive_expect_tx(hidden, (g.P1 - (owns ? 1 : 0)) * kHiddenChunkBytes);
     prefetch_tensormap(&a.wmap);
+  } else if (warp == kMmaWarp0 + 1 && lane == 0) {
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
+    for (int i = 0; i < kAgreeSlots; ++i) agree[i] = -1;
+    fence_mbar_init();
   }
   for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
@@ -1140,9 +1165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0;
     for (;;) {
       const int set = k % NACC;
-      if (!epilogue_all(wait_bar(cx, &accfull[set], (k / NACC) & 1))) break;
+      // The metadata and the abort flag are read together, after the wait.
+      const bool seen = wait_bar(cx, &accfull[set], (k / NACC) & 1);
       tc_fence_after_sync();
-      const int4 md = meta[set];
+      int4 md = meta[set];
+      if (!seen || *cx.abort_flag) {
+        if (!epilogue_agree(cx, &accfull[set], (k / NACC) & 1, k, agree)) break;
+        tc_fence_after_sync();
+        md = meta[set];
+      }
       if (md.x == 2) break;
       float v0[8], v1[8], x0[8], x1[8];
       {
@@ -1255,15 +1286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // No other CTA writes into this one's shared memory after the hidden
-  // vector is complete (bounded: a CTA that gave up exits all the same).
-  if (tid == 0 && !*cx.abort_flag) wait_bar_cluster(cx, hidden, 0);
+  // vector is complete (bounded). A CTA that gave up on it tells the others,
+  // after the start-up barrier, so that every CTA of the cluster lets the
+  // copies between them land before it exits.
+  bool gave_up = false;
+  if (tid == 0) gave_up = *cx.abort_flag || !wait_bar_cluster(cx, hidden, 0);
   if (warp < kEpilogueWarp0) cluster_wait();  // the start-up barrier
+  if (gave_up)
+    for (int d = 0; d < C; ++d) st_cluster_u32(cluster_map(&misc[1], d), 1u);
   tc_fence_before_sync();
   __syncthreads();
-  // A CTA that gave up tells the others, so that every CTA of the cluster
-  // lets the copies between them land before it exits.
-  if (tid == 0 && *cx.abort_flag)
-    for (int d = 0; d < C; ++d) st_cluster_u32(cluster_map(&misc[1], d), 1u);
   cluster_sync();
   tc_fence_after_sync();
   if (tid == 0 && *cx.abort_flag) settle_copies();
