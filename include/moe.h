@@ -251,6 +251,11 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
  * moe_debug_withhold - test hook: the unit with this index never publishes
  * its hidden vector, so its consumers' waits run out (-1 = off, the
  * default). Used to check the bounded waits without faulting the GPU.
+ * moe_debug_withhold_image - test hook for the grid kernel: the hidden
+ * loader never hands this unit's hidden image to the MMA issuers, so their
+ * mbarrier wait runs out and the CTA gives up (-1 = off, the default).
+ * Checks the abort path: the call records MOE_ERR_DEVICE_TIMEOUT, finishes,
+ * and the next call is unaffected. MOE_ERR_ARG below -1.
  * moe_debug_paths - test hook: 1 (the default) lets calls of one or two
  * tokens run on the cluster variant of the experts kernel (one cluster of
  * up to 8 CTAs per unit, partial sums and hidden chunks exchanged through
@@ -261,6 +266,7 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
  */
 int moe_set_timeout(moe_handle h, uint64_t nanoseconds);
 int moe_debug_withhold(moe_handle h, int unit);
+int moe_debug_withhold_image(moe_handle h, int unit);
 int moe_debug_paths(moe_handle h, int allow_cluster);
 
 /*

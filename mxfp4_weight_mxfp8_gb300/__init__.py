@@ -18,7 +18,8 @@ __all__ = [
     "MoeError", "MoeInfo", "MoeLayer", "library", "moe_prepare", "moe_quantize", "moe_group",
     "moe_run", "moe_experts", "moe_run_noalloc", "moe_run_combined", "moe_run_host",
     "moe_sync_status", "moe_copy_plan", "moe_copy_units", "moe_copy_hidden", "moe_set_timeout",
-    "moe_debug_withhold", "moe_debug_paths", "moe_cluster_size", "moe_info", "moe_destroy", "moe_error_string",
+    "moe_debug_withhold", "moe_debug_withhold_image", "moe_debug_paths", "moe_cluster_size", "moe_info",
+    "moe_destroy", "moe_error_string",
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
     "MAX_BATCH",
@@ -63,6 +64,7 @@ def _load():
         "moe_copy_hidden": ([vp, vp, vp, i32], i32),
         "moe_set_timeout": ([vp, u64], i32),
         "moe_debug_withhold": ([vp, i32], i32),
+        "moe_debug_withhold_image": ([vp, i32], i32),
         "moe_debug_paths": ([vp, i32], i32),
         "moe_cluster_size": ([vp, i32], i32),
         "moe_info": ([vp, ctypes.POINTER(MoeInfo)], i32),
@@ -195,6 +197,10 @@ def moe_set_timeout(handle, nanoseconds: int):
 
 def moe_debug_withhold(handle, unit: int):
     return _check(_lib.moe_debug_withhold(handle, unit), "moe_debug_withhold")
+
+
+def moe_debug_withhold_image(handle, unit: int):
+    return _check(_lib.moe_debug_withhold_image(handle, unit), "moe_debug_withhold_image")
 
 
 def moe_debug_paths(handle, allow_cluster: int):

@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       }
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&hfull[b]);
+      if (lane == 0 && cur.u != a.withhold_image) mbar_arrive(&hfull[b]);
     }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue

@@ -51,6 +51,8 @@ struct ExpertsArgs {
   Geometry g;
   uint64_t timeout_ns;
   int withhold_unit;          // test hook: never publish this unit's hidden (-1 = off)
+  int withhold_image;         // test hook (grid kernel): never deliver this unit's hidden
+                              // image to shared memory (-1 = off)
 };
 
 int experts_smem_bytes(const Geometry& g);

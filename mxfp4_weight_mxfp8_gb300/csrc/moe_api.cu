@@ -38,6 +38,7 @@ struct moe_ctx {
   CUtensorMap wmap{};
   uint64_t timeout_ns = 2000000000ull;
   int withhold = -1;
+  int withhold_image = -1;
   int allow_cluster = 1;  // one- and two-token calls may run on the cluster variant
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
 };
@@ -262,6 +263,7 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.g = h->g;
   a.timeout_ns = h->timeout_ns;
   a.withhold_unit = h->withhold;
+  a.withhold_image = h->withhold_image;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->allow_cluster != 0));
   return MOE_OK;
 }
@@ -473,6 +475,12 @@ int moe_debug_withhold(moe_handle h, int unit) {
   return MOE_OK;
 }
 
+int moe_debug_withhold_image(moe_handle h, int unit) {
+  if (h == nullptr || unit < -1) return MOE_ERR_ARG;
+  h->withhold_image = unit;
+  return MOE_OK;
+}
+
 int moe_debug_paths(moe_handle h, int allow_cluster) {
   if (h == nullptr || allow_cluster < 0 || allow_cluster > 1) return MOE_ERR_ARG;
   h->allow_cluster = allow_cluster;
@@ -631,6 +639,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.g = g;
   ea.timeout_ns = h->timeout_ns;
   ea.withhold_unit = -1;
+  ea.withhold_image = -1;
   MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->allow_cluster != 0));
   return MOE_OK;
 }

@@ -484,6 +484,33 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe, allow_cluster):
     check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
 
 
+@pytest.mark.parametrize("name", ["tiny", "tp16_b8"])
+def test_mbarrier_timeout_aborts_and_context_survives(moe, name):
+    """The grid kernel's abort path, made to run deterministically: the
+    hidden loader never hands unit 0's image to the MMA issuers, so their
+    bounded mbarrier wait runs out and every CTA with a job of that unit gives
+    up (the other roles stop, MMAs drain, copies settle). The call reports
+    the timeout and ends; the next call is exact."""
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    moe.moe_debug_paths(layer.handle, 0)
+    try:
+        moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
+        moe.moe_debug_withhold_image(layer.handle, 0)
+        _, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_ERR_DEVICE_TIMEOUT
+        moe.moe_debug_withhold_image(layer.handle, -1)
+        moe.moe_set_timeout(layer.handle, 0)
+        got, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+    finally:
+        moe.moe_debug_withhold_image(layer.handle, -1)
+        moe.moe_set_timeout(layer.handle, 0)
+        moe.moe_debug_paths(layer.handle, 1)
+    xq, xs = oracle.quantize_x(x)
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], f"{name} after an abort")
+
+
 @pytest.mark.parametrize("name", ["tiny", "tp8_b1"])
 def test_cluster_and_grid_paths_for_one_and_two_tokens(moe, name):
     """One- and two-token calls run on thread-block clusters (one per unit,
