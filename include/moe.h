@@ -210,8 +210,11 @@ int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* topk_ids, v
  * 16-byte aligned buffers on a GPU with native atomics on host memory (a
  * coherent GPU-CPU link, as on Grace) are used in place: the prep grid reads
  * x and ids from them and the experts kernel writes out into them, with no
- * copies. Otherwise x and ids are copied to handle-owned device buffers and
- * out is copied back.
+ * copies. The first such call on a set of buffers and a batch captures the
+ * two launches into a CUDA graph owned by the handle. Later calls with the
+ * same buffers, batch and settings replay it as one graph launch. A new
+ * set, or a changed timeout or test hook, captures again. Otherwise x and
+ * ids are copied to handle-owned device buffers and out is copied back.
  *   x_host BF16 [batch, H], ids_host int32 [batch, 16], out_host BF16
  *   [batch, 16, H]. Errors: as moe_run, plus device-side status.
  */

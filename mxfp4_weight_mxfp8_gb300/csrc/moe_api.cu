@@ -41,6 +41,16 @@ struct moe_ctx {
   int withhold_image = -1;
   int allow_cluster = 1;  // one- and two-token calls may run on the cluster variant
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
+  uint64_t settings = 0;  // bumped by every setter that changes kernel arguments
+  // moe_run_host in place: the call's two launches, captured once per set of
+  // host buffers, batch and settings, and replayed as one graph launch.
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t host_exec = nullptr;
+  const void* host_x = nullptr;
+  const void* host_ids = nullptr;
+  const void* host_out = nullptr;
+  int host_batch = 0;
+  uint64_t host_settings = 0;
 };
 
 namespace {
@@ -109,6 +119,8 @@ void release(moe_ctx* h) {
   cudaFree(h->workspace);
   cudaFree(h->io);
   cudaFreeHost(h->status_host);
+  if (h->host_exec) cudaGraphExecDestroy(h->host_exec);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   cudaSetDevice(current);
   delete h;
 }
@@ -268,6 +280,38 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   return MOE_OK;
 }
 
+// Captures moe_run on host buffers, with the kernels reporting into the
+// pinned status word, into the handle's replay graph.
+int capture_host_run(moe_ctx* h, const void* x_host, const int32_t* ids_host, void* out_host,
+                     int batch) {
+  if (h->host_exec) {
+    cudaGraphExecDestroy(h->host_exec);
+    h->host_exec = nullptr;
+  }
+  if (h->capture_stream == nullptr)
+    MOE_CUDA(cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking));
+  MOE_CUDA(cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal));
+  h->status_dev = h->status_host;
+  const int rc = moe_run(h, x_host, ids_host, out_host, batch, h->capture_stream);
+  h->status_dev = h->status;
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(h->capture_stream, &graph);
+  if (rc != MOE_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  MOE_CUDA(ce);
+  const cudaError_t ie = cudaGraphInstantiate(&h->host_exec, graph, 0);
+  cudaGraphDestroy(graph);
+  MOE_CUDA(ie);
+  h->host_x = x_host;
+  h->host_ids = ids_host;
+  h->host_out = out_host;
+  h->host_batch = batch;
+  h->host_settings = h->settings;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -383,11 +427,20 @@ int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void
     // pointers; coherent over the GPU-CPU link): the prep grid reads x and ids
     // from them, the epilogue writes the rows into them, and the kernels
     // report into a pinned status word, so the call makes no copies at all.
+    // The two launches are captured into a graph on first use (and again
+    // when the buffers, the batch or a setting change); each call is then a
+    // single graph launch.
     *reinterpret_cast<volatile int32_t*>(h->status_host) = 0;
-    h->status_dev = h->status_host;
-    const int rc = moe_run(h, x_host, ids_host, out_host, batch, stream);
-    h->status_dev = h->status;
-    if (rc != MOE_OK) return rc;
+    if (h->host_exec == nullptr || h->host_x != x_host || h->host_ids != ids_host ||
+        h->host_out != out_host || h->host_batch != batch || h->host_settings != h->settings) {
+      const int rc = capture_host_run(h, x_host, ids_host, out_host, batch);
+      if (rc != MOE_OK) return rc;
+    }
+    MOE_CUDA(cudaGraphLaunch(h->host_exec, s));
+    h->plan_batch = batch;  // what moe_run records, for the read-back calls
+    h->group_batch = batch;
+    h->grouped = 1;
+    h->ran = 1;
     MOE_CUDA(cudaStreamSynchronize(s));
     return *reinterpret_cast<volatile int32_t*>(h->status_host);
   }
@@ -466,24 +519,28 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units) {
 int moe_set_timeout(moe_handle h, uint64_t nanoseconds) {
   if (h == nullptr) return MOE_ERR_ARG;
   h->timeout_ns = nanoseconds ? nanoseconds : 2000000000ull;
+  ++h->settings;
   return MOE_OK;
 }
 
 int moe_debug_withhold(moe_handle h, int unit) {
   if (h == nullptr || unit < -1) return MOE_ERR_ARG;
   h->withhold = unit;
+  ++h->settings;
   return MOE_OK;
 }
 
 int moe_debug_withhold_image(moe_handle h, int unit) {
   if (h == nullptr || unit < -1) return MOE_ERR_ARG;
   h->withhold_image = unit;
+  ++h->settings;
   return MOE_OK;
 }
 
 int moe_debug_paths(moe_handle h, int allow_cluster) {
   if (h == nullptr || allow_cluster < 0 || allow_cluster > 1) return MOE_ERR_ARG;
   h->allow_cluster = allow_cluster;
+  ++h->settings;
   return MOE_OK;
 }
 
