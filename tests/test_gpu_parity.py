@@ -422,6 +422,40 @@ def test_run_host_in_place_and_copied(moe):
     moe.moe_run_host(layer.handle, xh, torch.from_numpy(ids).pin_memory(), outh, 1)
 
 
+def test_run_host_replay_graph_follows_buffers_batch_and_settings(moe):
+    """The in-place moe_run_host replays a captured graph. The same pinned
+    buffers with new contents are read afresh, and a smaller batch, a
+    cluster-path switch or a new timeout captures again. Each call equals
+    moe_run on device copies."""
+    import torch
+
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    xh = torch.zeros((4, 256), dtype=torch.int16).pin_memory()
+    idsh = torch.zeros((4, 16), dtype=torch.int32).pin_memory()
+    outh = torch.zeros((4, 16, 256), dtype=torch.int16).pin_memory()
+    steps = [(4, None), (4, None), (2, None), (2, ("paths", 0)), (4, ("timeout", 50_000_000)), (4, None)]
+    try:
+        for step, (batch, setting) in enumerate(steps):
+            if setting and setting[0] == "paths":
+                moe.moe_debug_paths(layer.handle, setting[1])
+            if setting and setting[0] == "timeout":
+                moe.moe_set_timeout(layer.handle, setting[1])
+            x = workload.make_x(batch, 256, seed=600 + step)
+            ids = workload.make_ids(batch, 32, seed=700 + step)
+            want, status = run_layer(moe, layer, x, ids)
+            assert status == moe.MOE_OK
+            xh[:batch].copy_(torch.from_numpy(x.view(np.int16)))
+            idsh[:batch].copy_(torch.from_numpy(ids))
+            outh.zero_()
+            moe.moe_run_host(layer.handle, xh, idsh, outh, batch)
+            got = outh[:batch].numpy().view(np.uint16).reshape(-1, 256)
+            np.testing.assert_array_equal(got, want, err_msg=f"step {step}")
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
+        moe.moe_set_timeout(layer.handle, 0)
+
+
 def test_quantize_group_experts_equals_run(moe):
     weights, x, ids = cached_inputs("tp16_b8")
     layer = layer_for(moe, weights)
