@@ -78,6 +78,19 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device):
+    """The largest of one float per rank (every rank gets it); with one rank,
+    the value itself. Each rank times its own replica, so the job's time per
+    call is the slowest rank's."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def describe(cfg):
     return (f"{cfg.name}: E={cfg.experts} H={cfg.hidden} I={cfg.inter} B={cfg.batch} top-16 "
             f"{cfg.ids} ids" + (f", {cfg.outlier_fraction:.0%} rows x50" if cfg.outlier_fraction else ""))
@@ -388,10 +401,7 @@ def run_ours(args, rank, world, local):
     sampler.stop()
     arm.check_status()
     clocks = sampler.summary(t_warm, t1)
-    if world > 1:
-        t = torch.tensor([ms_per_call], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_call = float(t.item())
+    ms_per_call = max_over_ranks(ms_per_call, world, device)
 
     kernel_ms = arm.experts_kernel_ms(min(200, max(20, args.steps // 10)))
     arm.check_status()
