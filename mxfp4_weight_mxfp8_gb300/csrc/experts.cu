@@ -828,14 +828,18 @@ constexpr int kClusterMaxRows = 2;  // rows of a unit in a call of one or two to
 
 // Unit-relative work of CTA `rank` of a C-CTA cluster: FC1 stages [f0, f1)
 // (stage s = item * KC1 + chunk) and FC2 jobs [j0, j1).
+// FC1 stages and FC2 jobs are each cut evenly over the cluster. FC2 starts
+// only once every hidden chunk has landed, so the longest FC1 range sets when
+// it starts: balancing FC1 + FC2 stages per CTA (as the grid kernel's Split
+// does) would lengthen the longest FC1 range by the FC2 jobs' unevenness.
 struct ClusterRange {
   int f0, f1, j0, j1;
   __host__ __device__ ClusterRange(const Geometry& g, int rank, int C) {
-    const Split sp(1, g, C);
-    f0 = sp.fc1_begin(rank);
-    f1 = sp.fc1_begin(rank + 1);
-    j0 = sp.fc2_begin(rank);
-    j1 = sp.fc2_begin(rank + 1);
+    const int T1 = g.P1 * g.KC1;
+    f0 = rank * T1 / C;
+    f1 = (rank + 1) * T1 / C;
+    j0 = rank * g.NQ / C;
+    j1 = (rank + 1) * g.NQ / C;
   }
 };
 
