@@ -82,9 +82,8 @@ struct Layout {
 // Per-call split of the work over the grid: FC1 stages and FC2 jobs are each
 // cut evenly over the CTAs. A unit's FC2 waits for its hidden vector, which is
 // complete only when the FC1 ranges holding its items are done, so the FC1
-// ranges are kept equal rather than evening out FC1 + FC2 stages per CTA
-// (measured slightly faster at every batch size). Every CTA computes the
-// same table.
+// ranges are kept equal rather than evening out FC1 + FC2 stages per CTA.
+// Every CTA computes the same table.
 struct Split {
   int T1, J, G;
   __host__ __device__ Split(int units, const Geometry& g, int grid) {
