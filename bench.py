@@ -37,6 +37,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -106,11 +107,25 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_hash():
+def code_only(text):
+    """C++ source without its comments and with whitespace runs collapsed, so
+    that editing a comment does not count as changing the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_hash(read=None):
+    """sha256[:16] of the experts kernel's code (comments and whitespace
+    ignored), as recorded in the ncu summaries."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "mxfp4_weight_mxfp8_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        if read is None:
+            with open(os.path.join(ROOT, "mxfp4_weight_mxfp8_gb300", "csrc", name), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(name)
+        h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,8 +22,8 @@
 //              hidden requant, publish; FC2 -> BF16 rows with 16-byte stores
 //
 // Work split: FC1 stages (unit, tile pair, K chunk) and FC2 jobs (unit, 256
-// output rows) are cut into contiguous per-CTA ranges of near-equal bytes,
-// and every CTA runs its FC1 range, then its FC2 range. Above 256 units the
+// output rows) are each cut evenly into contiguous per-CTA ranges, and every
+// CTA runs its FC1 range, then its FC2 range. Above 256 units the
 // units are cut into two halves, A and B, run as FC1(A), FC1(B), FC2(A),
 // FC2(B): half A's hidden vectors are reduced and published while half B's
 // FC1 weights stream.
@@ -825,8 +825,8 @@ constexpr int kClusterMaxRows = 2;  // rows of a unit in a call of one or two to
 // (stage s = item * KC1 + chunk) and FC2 jobs [j0, j1).
 // FC1 stages and FC2 jobs are each cut evenly over the cluster. FC2 starts
 // only once every hidden chunk has landed, so the longest FC1 range sets when
-// it starts: balancing FC1 + FC2 stages per CTA (as the grid kernel's Split
-// does) would lengthen the longest FC1 range by the FC2 jobs' unevenness.
+// it starts: balancing FC1 + FC2 stages per CTA instead would lengthen the
+// longest FC1 range by the FC2 jobs' unevenness.
 struct ClusterRange {
   int f0, f1, j0, j1;
   __host__ __device__ ClusterRange(const Geometry& g, int rank, int C) {
