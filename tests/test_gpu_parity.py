@@ -316,6 +316,7 @@ def test_supported_limits(moe, E, H, I, B, dist):
     (16, 512, 96, 1),      # partial tiles (I = 96), clusters of 6
     (16, 512, 96, 2),      # two-row units; the piece layout allows only small clusters
     (8, 3584, 384, 1),     # fewer experts than slots: 8 units, clusters of 8
+    (32, 3584, 384, 2),    # the TP8 shard's shape at two tokens: clusters of 4, FC2 stages past the ring
     (1024, 256, 512, 2),   # the widest I with the smallest H
     (16, 16384, 512, 1),   # the largest H and I
 ])
