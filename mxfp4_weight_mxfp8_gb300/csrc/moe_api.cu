@@ -301,9 +301,11 @@ int capture_host_run(moe_ctx* h, const void* x_host, const int32_t* ids_host, vo
     return rc;
   }
   MOE_CUDA(ce);
-  const cudaError_t ie = cudaGraphInstantiate(&h->host_exec, graph, 0);
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
   cudaGraphDestroy(graph);
   MOE_CUDA(ie);
+  h->host_exec = exec;
   h->host_x = x_host;
   h->host_ids = ids_host;
   h->host_out = out_host;
