@@ -576,6 +576,43 @@ def test_cluster_and_grid_paths_for_one_and_two_tokens(moe, name):
     assert rel <= 2e-3
 
 
+@pytest.mark.parametrize("allow_cluster", [1, 0])
+def test_floor_rule_pair_golden_on_the_gpu(moe, allow_cluster):
+    """The hand-worked pair of golden/floor_rule_pair.json (I = 384: the floor
+    rule saturates its hidden block) through the kernels: its hidden codes,
+    scales and output bits are the golden's, on both paths, and every other
+    pair (an all-zero expert) gives +0.0 rows."""
+    import torch
+    from conftest import floor_rule_pair_case
+
+    weights, x, ids, spec = floor_rule_pair_case()
+    dev = torch.device("cuda:0")
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights))
+    try:
+        moe.moe_debug_paths(layer.handle, allow_cluster)
+        got, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        H, I = spec["hidden"], spec["inter"]
+        out = np.full(H, spec["out_bits_default"], np.uint16)
+        for n, v in spec["out_bits"].items():
+            out[int(n)] = v
+        np.testing.assert_array_equal(got[0], out)
+        assert not got[1:].any()
+        experts, _ = units_of(moe, layer, 1)
+        hq = np.zeros((len(experts), 8, I), np.uint8)
+        hs = np.zeros((len(experts), 8, I // 32), np.uint8)
+        moe.moe_copy_hidden(layer.handle, hq, hs, len(experts))
+        assert experts[0] == 0
+        expect_hs = np.full(I // 32, spec["hidden_scale_default"], np.uint8)
+        expect_hs[0] = spec["hidden_scales"]["0"]
+        expect_hq = np.full(I, spec["hidden_code_default"], np.uint8)
+        expect_hq[0] = spec["hidden_codes"]["0"]
+        np.testing.assert_array_equal(hs[0, 0], expect_hs)
+        np.testing.assert_array_equal(hq[0, 0], expect_hq)
+    finally:
+        layer.close()
+
+
 def test_cluster_path_at_two_tokens_with_shared_experts(moe):
     """Two tokens routed to the same experts: every unit holds two rows, so
     each split-K piece carries two rows of partial sums."""

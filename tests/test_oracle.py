@@ -327,28 +327,75 @@ def naive_pair(w13, s13, w2, s2, xq, xs, e, t, floor_rule):
     return np.array(y), np.array(hq, np.uint8), np.array(hs, np.uint8), np.array(o)
 
 
-@pytest.mark.parametrize("inter", [32, 64, 256])
+@pytest.mark.parametrize("inter", [32, 64, 256, 384])
 def test_pairs_against_naive_triple_loop(inter):
-    """inter = 256 > H: FC2 rows are longer than FC1 rows."""
+    """inter = 256 > H: FC2 rows are longer than FC1 rows. inter = 384 is the
+    TP8 shard's (2I = 768): the hidden requant takes the floor rule there
+    (ExpertsKernel.store_hidden, floor = tp == 8; PersistentExperts.__init__,
+    tp = 8 iff w13 has 768 rows), every other inter the ceil rule. The loop
+    below is told the rule from the pages' definition, not from the oracle, and
+    the test checks that the other rule would have given different codes, so
+    an oracle that ignored or misrouted the rule fails here."""
     rng = np.random.default_rng(inter)
-    E, H, B = 4, 64, 2
+    E, H, B = 16, 64, 2  # 16 distinct experts per token: 32 distinct hidden rows
+    floor_rule = 2 * inter == 768
     weights = random_weights(rng, E, H, inter)
     x = rng.standard_normal((B, H)).astype(np.float32)
     bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     xq, xs = oracle.quantize_x(bits)
-    ids = np.stack([np.concatenate([rng.permutation(E), rng.permutation(E), rng.permutation(E),
-                                    rng.permutation(E)]) for _ in range(B)]).astype(np.int32)
-    pairs = np.array([0, 5, 16, 31], np.int32)
+    ids = np.stack([rng.permutation(E) for _ in range(B)]).astype(np.int32)
+    # Short hidden rows have few 32-blocks: take every pair there, so that some
+    # block falls between the two rules.
+    pairs = np.arange(B * 16, dtype=np.int32) if inter <= 64 else np.array([0, 5, 16, 31], np.int32)
     res = oracle.pairs_forward(weights, xq, xs, ids, pairs=pairs, want_hidden=True,
                                want_fc1=True, threads=2)
+    other_rule_differs = False
     for i, p in enumerate(pairs):
-        y, hq, hs, o = naive_pair(*weights, xq, xs, ids.reshape(-1)[p], p // 16, False)
+        y, hq, hs, o = naive_pair(*weights, xq, xs, ids.reshape(-1)[p], p // 16, floor_rule)
         np.testing.assert_allclose(res["y"][i], y, rtol=1e-12, atol=1e-300)
         np.testing.assert_array_equal(res["hq"][i], hq)
         np.testing.assert_array_equal(res["hs"][i], hs)
-        expect = torch.from_numpy(o.astype(np.float32)).to(torch.bfloat16)
+        # Bit for bit: o is rounded once, from float64, exactly as the oracle does.
+        expect = torch.from_numpy(o).to(torch.bfloat16)
         got = torch.from_numpy(res["out"][i].view(np.int16)).view(torch.bfloat16)
         assert torch.equal(got, expect)
+        _, hq2, hs2, _ = naive_pair(*weights, xq, xs, ids.reshape(-1)[p], p // 16, not floor_rule)
+        other_rule_differs |= not (np.array_equal(hq2, hq) and np.array_equal(hs2, hs))
+    assert other_rule_differs, "the data does not tell the two scale rules apart"
+
+
+def test_floor_rule_pair_golden():
+    """The hand-worked pair of golden/floor_rule_pair.json (I = 384, floor rule)
+    reproduces its codes, scales and output bits through the oracle."""
+    from conftest import floor_rule_pair_case
+
+    weights, x, ids, spec = floor_rule_pair_case()
+    xq, xs = oracle.quantize_x(x)
+    assert (xs == spec["x_scale"]).all() and (xq == spec["x_code"]).all()
+    res = oracle.pairs_forward(weights, xq, xs, ids, pairs=np.array([0], np.int32),
+                               want_hidden=True, threads=1)
+    I, H = spec["inter"], spec["hidden"]
+    hs = np.full(I // 32, spec["hidden_scale_default"], np.uint8)
+    for b, v in spec["hidden_scales"].items():
+        hs[int(b)] = v
+    hq = np.full(I, spec["hidden_code_default"], np.uint8)
+    for j, v in spec["hidden_codes"].items():
+        hq[int(j)] = v
+    out = np.full(H, spec["out_bits_default"], np.uint16)
+    for n, v in spec["out_bits"].items():
+        out[int(n)] = v
+    np.testing.assert_array_equal(res["hs"][0], hs)
+    np.testing.assert_array_equal(res["hq"][0], hq)
+    np.testing.assert_array_equal(res["out"][0], out)
+    # The hidden block alone, under each rule, as the golden's derivation states.
+    h0 = 2.125 / (1.0 + math.exp(-2.125))
+    block = np.zeros(32)
+    block[0] = h0
+    codes, scale = oracle.mxfp8_block(block, True)
+    assert (int(scale), int(codes[0])) == (spec["hidden_scales"]["0"], spec["hidden_codes"]["0"])
+    codes, scale = oracle.mxfp8_block(block, False)
+    alt = spec["ceil_rule_would_give"]
+    assert (int(scale), int(codes[0])) == (alt["hidden_scale_0"], alt["hidden_code_0"])
 
 
 def test_fc2_only_entry_reproduces_pair_outputs():
