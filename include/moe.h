@@ -25,7 +25,9 @@
  *    workspace) until moe_destroy.
  *  - A handle is bound to the device that was current at moe_prepare and
  *    serves one stream at a time: calls that overlap on the GPU race on its
- *    workspace.
+ *    workspace. Every call that launches, copies or synchronizes returns
+ *    MOE_ERR_ARG (nothing queued; moe_last_error_detail names both devices)
+ *    when another device is current.
  */
 #ifndef MXFP4_WEIGHT_MXFP8_GB300_MOE_H
 #define MXFP4_WEIGHT_MXFP8_GB300_MOE_H
@@ -48,7 +50,7 @@ extern "C" {
 enum moe_status {
   MOE_OK = 0,
   MOE_ERR_ARG = 1,            /* null/misaligned pointer, size out of range */
-  MOE_ERR_UNSUPPORTED = 2,    /* no sm_103/sm_100-family device, grid not co-resident */
+  MOE_ERR_UNSUPPORTED = 2,    /* not an sm_103 (GB300) device, grid not co-resident */
   MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
   MOE_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
   MOE_ERR_DEVICE_IDS = 5,     /* an id out of [0, E) or repeated within a token */
@@ -89,8 +91,9 @@ typedef struct moe_info_t {
  * pre-tiled for the tensor core), allocates the plan, unit table and
  * workspace for batches up to MOE_MAX_BATCH, builds the TMA descriptor and
  * checks that the persistent grid fits one CTA per SM.
- * Errors: MOE_ERR_ARG (null out/pointers, sizes), MOE_ERR_UNSUPPORTED (not an
- * sm_100-family GPU with >= 227 KB shared memory per block), MOE_ERR_CUDA.
+ * Errors: MOE_ERR_ARG (null out/pointers, sizes), MOE_ERR_UNSUPPORTED (the
+ * current device fails moe_device_supported: the library holds sm_103a code
+ * only), MOE_ERR_CUDA.
  * On error *out is NULL and nothing is leaked.
  */
 int moe_prepare(moe_handle* out, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -197,6 +200,11 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream);
  *   - Every call on a device shares the one array, and the counters that
  *     must start at zero are cleared inside each call: calls that overlap on
  *     the GPU (other streams, other handles) race and corrupt each other.
+ *   - Of the handle it reads the weights and settings and writes only the
+ *     status word that moe_sync_status reads.
+ *   - The array's address is looked up once per device and kept for the
+ *     life of the process: a cudaDeviceReset (or any other teardown of the
+ *     device's primary context) after the first call is not supported.
  * Asynchronous on `stream`; device-side errors surface through
  * moe_sync_status on the same handle. Errors: as moe_run, and
  * MOE_ERR_UNSUPPORTED on a device ordinal of 64 or more.
@@ -291,9 +299,21 @@ void moe_destroy(moe_handle h);
 /* Static description of a status code. */
 const char* moe_error_string(int status);
 
-/* Text of the last CUDA failure seen by this thread (for MOE_ERR_CUDA /
- * MOE_ERR_UNSUPPORTED diagnostics); empty if none. */
+/* Text of the last failure seen by this thread (for MOE_ERR_CUDA,
+ * MOE_ERR_UNSUPPORTED and some MOE_ERR_ARG diagnostics); empty if none. */
 const char* moe_last_error_detail(void);
+
+/*
+ * moe_device_supported - whether a device with these properties runs this
+ * library: compute capability 10.3 (sm_103, GB300; the library carries
+ * sm_103a code only, and sm_100 parts lack it) with at least the experts
+ * kernel's dynamic shared memory per block (cudaDeviceProp::
+ * sharedMemPerBlockOptin). MOE_OK or MOE_ERR_UNSUPPORTED; pure, no CUDA
+ * call. moe_prepare applies it to the current device. Source: [runtime]
+ * PersistentExperts (one co-resident CTA per SM with the kernel's shared
+ * memory) and the pages' sm_100-family tcgen05 kernels, here built for sm_103a.
+ */
+int moe_device_supported(int cc_major, int cc_minor, size_t smem_per_block_optin);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ __all__ = [
     "moe_destroy", "moe_error_string",
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
-    "MAX_BATCH",
+    "MAX_BATCH", "moe_device_supported",
 ]
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
@@ -71,6 +71,7 @@ def _load():
         "moe_destroy": ([vp], None),
         "moe_error_string": ([i32], ctypes.c_char_p),
         "moe_last_error_detail": ([], ctypes.c_char_p),
+        "moe_device_supported": ([i32, i32, ctypes.c_size_t], i32),
     }
     for name, (args, res) in signatures.items():
         fn = getattr(lib, name)
@@ -223,6 +224,12 @@ def moe_info(handle) -> MoeInfo:
 
 def moe_destroy(handle):
     _lib.moe_destroy(handle)
+
+
+def moe_device_supported(cc_major: int, cc_minor: int, smem_per_block_optin: int) -> int:
+    """MOE_OK if a device with these properties runs the library (sm_103 with
+    enough shared memory per block), else MOE_ERR_UNSUPPORTED."""
+    return _lib.moe_device_supported(cc_major, cc_minor, smem_per_block_optin)
 
 
 def moe_error_string(code: int) -> str:

@@ -149,10 +149,12 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     std::snprintf(g_detail, sizeof g_detail, "internal: misaligned shared-memory layout");
     return MOE_ERR_UNSUPPORTED;
   }
-  if (prop.major != 10 ||
-      static_cast<int>(prop.sharedMemPerBlockOptin) < moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER))) {
-    std::snprintf(g_detail, sizeof g_detail, "needs an sm_100-family GPU with %d B shared memory",
-                  h->smem_bytes);
+  if (moe_device_supported(prop.major, prop.minor, prop.sharedMemPerBlockOptin) != MOE_OK) {
+    std::snprintf(g_detail, sizeof g_detail,
+                  "needs an sm_103 GPU (GB300) with %d B of shared memory per block; found sm_%d%d "
+                  "with %zu B (the library carries sm_103a code only)",
+                  moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)), prop.major,
+                  prop.minor, static_cast<size_t>(prop.sharedMemPerBlockOptin));
     return MOE_ERR_UNSUPPORTED;
   }
   h->sms = prop.multiProcessorCount;
@@ -253,6 +255,26 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
 
 int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE_OK : MOE_ERR_ARG; }
 
+// A handle's buffers, tensor map and kernels belong to the device that was
+// current at moe_prepare: every call that launches, copies or synchronizes
+// refuses to run with another device current.
+int check_device(const moe_ctx* h) {
+  int current = -1;
+  MOE_CUDA(cudaGetDevice(&current));
+  if (current != h->device) {
+    std::snprintf(g_detail, sizeof g_detail,
+                  "handle prepared on device %d used with device %d current", h->device, current);
+    return MOE_ERR_ARG;
+  }
+  return MOE_OK;
+}
+
+#define MOE_CHECK_DEVICE(h)                     \
+  do {                                          \
+    const int moe_rc_ = check_device(h);        \
+    if (moe_rc_ != MOE_OK) return moe_rc_;      \
+  } while (0)
+
 // ids: the call's routing ids when the same call's prep grid runs just
 // before on this stream, else null.
 int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream) {
@@ -340,6 +362,7 @@ int moe_prepare(moe_handle* out, const void* w13, const void* s13, const void* w
 
 int moe_quantize(moe_handle h, const void* x_bf16, int batch, void* stream) {
   if (h == nullptr || x_bf16 == nullptr || !aligned16(x_bf16) || check_batch(batch)) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   MOE_CUDA(moe::launch_prep(prep_args(h, x_bf16, nullptr, batch, moe::kPrepQuantize),
                             static_cast<cudaStream_t>(stream)));
   h->plan_batch = batch;
@@ -349,6 +372,7 @@ int moe_quantize(moe_handle h, const void* x_bf16, int batch, void* stream) {
 int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream) {
   if (h == nullptr || topk_ids == nullptr || !aligned16(topk_ids) || check_batch(batch))
     return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   MOE_CUDA(moe::launch_prep(prep_args(h, nullptr, topk_ids, batch, moe::kPrepGroup),
                             static_cast<cudaStream_t>(stream)));
   h->grouped = 1;
@@ -361,6 +385,7 @@ int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out
   if (h == nullptr || !x_bf16 || !topk_ids || !out_bf16) return MOE_ERR_ARG;
   if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(moe::launch_prep(
       prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
@@ -379,6 +404,7 @@ int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
   if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(topk_weights) ||
       !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   const int rc = moe_run(h, x_bf16, topk_ids, h->staged, batch, stream);
   if (rc != MOE_OK) return rc;
   moe::CombineArgs c{};
@@ -395,6 +421,7 @@ int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
 int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
   if (h == nullptr || out_bf16 == nullptr || !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   if (h->plan_batch != batch || h->group_batch != batch) return MOE_ERR_STATE;
   const int rc = launch_experts(h, out_bf16, batch, nullptr, static_cast<cudaStream_t>(stream));
   if (rc == MOE_OK) h->ran = 1;
@@ -403,6 +430,7 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
 
 int moe_sync_status(moe_handle h, void* stream) {
   if (h == nullptr) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(cudaMemcpyAsync(h->status_host, h->status, 4, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemsetAsync(h->status, 0, 4, s));
@@ -422,6 +450,7 @@ bool is_pinned_host(const void* p) {
 int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void* out_host,
                  int batch, void* stream) {
   if (h == nullptr || !x_host || !ids_host || !out_host || check_batch(batch)) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (h->host_atomics && aligned16(x_host) && aligned16(ids_host) && aligned16(out_host) &&
       is_pinned_host(x_host) && is_pinned_host(ids_host) && is_pinned_host(out_host)) {
@@ -466,6 +495,7 @@ int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void
 
 int moe_copy_plan(moe_handle h, uint8_t* codes, uint8_t* scales, int batch) {
   if (h == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   if (h->plan_batch == 0) return MOE_ERR_STATE;
   if (batch < 1 || batch > h->plan_batch) return MOE_ERR_ARG;
   MOE_CUDA(cudaDeviceSynchronize());
@@ -478,6 +508,7 @@ int moe_copy_plan(moe_handle h, uint8_t* codes, uint8_t* scales, int batch) {
 
 int moe_copy_units(moe_handle h, int32_t* count, int32_t* experts, int16_t* rows, int capacity) {
   if (h == nullptr || count == nullptr) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   if (!h->grouped) return MOE_ERR_STATE;
   MOE_CUDA(cudaDeviceSynchronize());
   MOE_CUDA(cudaMemcpy(count, h->unit_count, 4, cudaMemcpyDeviceToHost));
@@ -493,6 +524,7 @@ int moe_copy_units(moe_handle h, int32_t* count, int32_t* experts, int16_t* rows
 
 int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units) {
   if (h == nullptr || codes == nullptr || scales == nullptr || units < 0) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
   if (!h->ran) return MOE_ERR_STATE;
   if (units > h->unit_cap) return MOE_ERR_ARG;
   const Geometry& g = h->g;
@@ -585,6 +617,12 @@ const char* moe_error_string(int status) {
 
 const char* moe_last_error_detail(void) { return g_detail; }
 
+int moe_device_supported(int cc_major, int cc_minor, size_t smem_per_block_optin) {
+  if (cc_major != 10 || cc_minor != 3) return MOE_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)));
+  return smem_per_block_optin >= need ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -658,10 +696,9 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
                   batch, total, MOE_NOALLOC_SCRATCH_BYTES);
     return MOE_ERR_ARG;
   }
-  int device = 0;
-  MOE_CUDA(cudaGetDevice(&device));
+  MOE_CHECK_DEVICE(h);
   uint8_t* w = nullptr;
-  const int rc = noalloc_scratch(device, &w);
+  const int rc = noalloc_scratch(h->device, &w);
   if (rc != MOE_OK) return rc;
 
   // The grouping block of the prep kernel clears the counters and flags the
@@ -676,6 +713,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.unit_rows = reinterpret_cast<int16_t*>(w + offsets[4]);
   pa.item_counters = reinterpret_cast<uint32_t*>(w + offsets[5]);
   pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
+  pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(moe::launch_prep(pa, s));
 
@@ -703,6 +741,3 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   return MOE_OK;
 }
 
-extern "C" {
-
-}  // extern "C"

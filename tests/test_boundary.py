@@ -42,9 +42,27 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(raw, name), name
 
 
-def test_library_is_built_for_sm103a(lib):
-    data = open(lib.library()._name, "rb").read()
-    assert b"sm_103a" in data or b"sm_103" in data
+def test_library_is_built_for_sm103a_only(lib):
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "_moe_build_check", os.path.join(ROOT, "mxfp4_weight_mxfp8_gb300", "build.py"))
+    build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build)
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert os.path.exists(lib.library()._name)
+
+
+def test_device_support_check_without_a_gpu(lib):
+    """moe_prepare's device check on faked properties: sm_103 with the
+    kernel's shared memory is accepted; sm_100 (no sm_103a code), other
+    majors and too little shared memory are refused."""
+    ok = 232448  # cudaDeviceProp::sharedMemPerBlockOptin of a GB300
+    assert lib.moe_device_supported(10, 3, ok) == lib.MOE_OK
+    assert lib.moe_device_supported(10, 0, ok) == lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_device_supported(12, 0, ok) == lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_device_supported(9, 0, ok) == lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_device_supported(10, 3, 100 * 1024) == lib.MOE_ERR_UNSUPPORTED
 
 
 def test_error_strings(lib):

@@ -1,11 +1,11 @@
 """moe_run_noalloc against moe_run, through the C ABI.
 
 moe_run_noalloc takes all per-call scratch from the library's static device
-buffer instead of the handle's workspace. Its rows must agree with moe_run's
-within the output bars of the parity tests (relative L2 <= 1e-2 over all rows,
-|err| <= 3e-2 * rms(row) per element), on consecutive calls that share the
-buffer, and a batch whose scratch would not fit must be refused before any
-launch. The file is named so that pytest collects it last; it also passes on
+buffer instead of the handle's workspace. It runs the same kernels with the
+same work split as moe_run, and every sum of both (split-K pieces in CTA
+order, one fixed cut per call) is deterministic, so its rows must equal
+moe_run's bit for bit, on consecutive calls that share the buffer. A batch
+whose scratch would not fit must be refused before any launch. The file is named so that pytest collects it last; it also passes on
 its own in a fresh process.
 """
 from __future__ import annotations
@@ -89,6 +89,9 @@ def check_close(got, ref, label):
     rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
     worst = float(np.max(np.abs(got - ref) / np.maximum(rms, 1e-300)))
     print(f"{label}: rel_l2 {rel:.3e} worst/rms {worst:.3e} identical {np.array_equal(got, ref)}")
+    # The same kernels and split as moe_run: identical rows. (Had the paths
+    # summed in different orders, the parity bars below would be the bar.)
+    np.testing.assert_array_equal(got, ref, err_msg=label)
     assert rel <= REL_L2, (label, rel)
     assert worst <= ROW_TOL, (label, worst)
 
