@@ -281,6 +281,25 @@ int moe_debug_withhold_image(moe_handle h, int unit);
 int moe_debug_paths(moe_handle h, int allow_cluster);
 
 /*
+ * moe_debug_kernel_span - measurement hook: with enable = 1, every later
+ * launch of the experts kernel (cluster variant or grid) on this handle has
+ * each CTA store its start and end time (%globaltimer, nanoseconds) into a
+ * handle-owned array, overwriting the previous launch's (plain stores, no
+ * synchronization between CTAs). 0 turns it off. Synchronizes the device and
+ * clears the array when turned on.
+ * moe_read_kernel_span - synchronizes the device and returns, in *span_ns,
+ * the last recorded launch's span: the latest CTA end minus the earliest CTA
+ * start. The launch overlaps the preceding prep grid (programmatic launch),
+ * so its span starts while that grid still runs. Clears the array.
+ * MOE_ERR_STATE if no launch was recorded since the last read.
+ * Source: [runtime] PersistentExperts (one persistent launch per call; the
+ * pages time it as part of the decode step). MOE_ERR_ARG for a null handle
+ * or output, or another value of enable.
+ */
+int moe_debug_kernel_span(moe_handle h, int enable);
+int moe_read_kernel_span(moe_handle h, uint64_t* span_ns);
+
+/*
  * moe_cluster_size - the CTAs per thread-block cluster that a call of
  * `batch` tokens on this layer runs on: on the cluster variant the largest
  * size up to 8 of which one cluster per possible unit (min(E, 16 batch)) is

@@ -22,7 +22,7 @@ __all__ = [
     "moe_destroy", "moe_error_string",
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
-    "MAX_BATCH", "moe_device_supported",
+    "MAX_BATCH", "moe_device_supported", "moe_debug_kernel_span", "moe_read_kernel_span",
 ]
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
@@ -72,6 +72,8 @@ def _load():
         "moe_error_string": ([i32], ctypes.c_char_p),
         "moe_last_error_detail": ([], ctypes.c_char_p),
         "moe_device_supported": ([i32, i32, ctypes.c_size_t], i32),
+        "moe_debug_kernel_span": ([vp, i32], i32),
+        "moe_read_kernel_span": ([vp, ctypes.POINTER(u64)], i32),
     }
     for name, (args, res) in signatures.items():
         fn = getattr(lib, name)
@@ -206,6 +208,17 @@ def moe_debug_withhold_image(handle, unit: int):
 
 def moe_debug_paths(handle, allow_cluster: int):
     return _check(_lib.moe_debug_paths(handle, allow_cluster), "moe_debug_paths")
+
+
+def moe_debug_kernel_span(handle, enable: int):
+    return _check(_lib.moe_debug_kernel_span(handle, enable), "moe_debug_kernel_span")
+
+
+def moe_read_kernel_span(handle):
+    """Span (ns) of the last experts-kernel launch recorded by the launch clock."""
+    span = ctypes.c_uint64()
+    _check(_lib.moe_read_kernel_span(handle, ctypes.byref(span)), "moe_read_kernel_span")
+    return span.value
 
 
 def moe_cluster_size(handle, batch: int) -> int:

@@ -14,8 +14,11 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-BUILD = os.path.join(HERE, "_build")
-LIBRARY = os.path.join(BUILD, "libmoe_gb300.so")
+# MOE_BUILD_DIR / MOE_NVCC_DEFINES build a variant elsewhere (for example
+# with -DMOE_TRACE); MOE_LIBRARY makes the binding load a given build.
+BUILD = os.environ.get("MOE_BUILD_DIR", os.path.join(HERE, "_build"))
+LIBRARY = os.environ.get("MOE_LIBRARY", os.path.join(BUILD, "libmoe_gb300.so"))
+DEFINES = os.environ.get("MOE_NVCC_DEFINES", "").split()
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]
@@ -45,7 +48,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+        cmd = [NVCC, *ARCH, *FLAGS, *DEFINES, *extra, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{res.stderr}")

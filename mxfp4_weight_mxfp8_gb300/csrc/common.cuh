@@ -40,6 +40,7 @@ constexpr int kEpilogueWarp0 = 6;         // warps 6..9: the epilogue warpgroup
 constexpr int kThreads = 320;             // 10 warps
 constexpr int kMaxInterChunks = MOE_MAX_INTER / kChunkK;  // 4
 constexpr int kMaxGrid = 256;             // partition table capacity (CTAs)
+constexpr int kMaxSpanCtas = 512;         // launch-clock slots: CTAs of any experts launch
 
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `r` (0..7) in a
 // 1024-byte, 128-byte-swizzled 8-row image.

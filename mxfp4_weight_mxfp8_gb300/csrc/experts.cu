@@ -194,6 +194,37 @@ __device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Launch clock (moe_debug_kernel_span): CTA c stores its start and end times
+// (%globaltimer) into words 2c and 2c + 1; plain stores, so the clock costs
+// the launch nothing measurable. The host reduces them to the launch's span.
+__device__ __forceinline__ void span_enter(uint64_t* span) {
+  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x] = global_timer_ns();
+}
+
+__device__ __forceinline__ void span_leave(uint64_t* span) {
+  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x + 1] = global_timer_ns();
+}
+
+// Phase stamps for timing studies, compiled in only with -DMOE_TRACE: slot k
+// of this CTA's 16-word record gets the time the CTA passed point k.
+#ifdef MOE_TRACE
+#define MOE_STAMP(k)                                                                        \
+  do {                                                                                      \
+    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
+  } while (0)
+#define MOE_STAMP_VALUE(k, v)                                                              \
+  do {                                                                                     \
+    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 16 + (k)] = (v);     \
+  } while (0)
+#else
+#define MOE_STAMP(k) \
+  do {               \
+  } while (0)
+#define MOE_STAMP_VALUE(k, v) \
+  do {                        \
+  } while (0)
+#endif
+
 __device__ __forceinline__ float silu_times(float gate, float up) {
   return gate / (1.0f + expf(-gate)) * up;
 }
@@ -273,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
 
   if (tid == 0) {
+    span_enter(a.span);
+    MOE_STAMP(0);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
       mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
@@ -304,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   // The plan, unit table and cleared counters of the preceding prep grid.
   grid_dependency_wait();
   const int units = *a.unit_count;
+  if (tid == 0) MOE_STAMP(3);
   // Half A = units [0, units_a). Small calls keep one half: their chain of
   // reductions is latency-bound and more pieces per item only lengthen it.
   const int units_a = units > kHalvesFrom ? (units + 1) / 2 : units;
@@ -343,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         bulk_load(ASF + slot * 2 * kScaleAtomBytes,
                   a.stages + static_cast<size_t>(stage) * kStageBytes + kStageWeightBytes,
                   2 * kScaleAtomBytes, &full[slot], policy);
+        if (n == 0) MOE_STAMP(1);
+        MOE_STAMP(2);
         ++n;
         if (++slot == S) {
           slot = 0;
@@ -363,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
           for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
         }
+      MOE_STAMP_VALUE(15, static_cast<uint64_t>(n));
       // Drain: every issued stage consumed and released before exit.
       if (ok)
         for (int k = (n > S ? n - S : 0); k < n && ok; ++k) ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
@@ -376,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
+      bool fc2_seen = false;
+      (void)fc2_seen;
       auto acquire = [&](int set) {
         return k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
       };
@@ -396,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           first_c = cur.c;
         }
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        if (lead && n == 0) MOE_STAMP(4);
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
         tc_fence_after_sync();
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
@@ -407,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         // Descriptor start addresses count 16-byte units: +2 is the next K-step.
         tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
         tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+        if (lead) MOE_STAMP(5);
         tc_commit(&empty[slot]);
         advance();
         if (last) {
@@ -432,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         bool started = false;
         for (int c = 0; c < g.KC2 && ok; ++c) {
           if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+          if (lead && !fc2_seen) {
+            MOE_STAMP(10);
+            fc2_seen = true;
+          }
           tc_fence_after_sync();
           // K-steps of this chunk: 4, or fewer in the last chunk when I % 128 != 0.
           const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
@@ -449,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
               tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
             started = true;
           }
+          if (lead) MOE_STAMP(11);
           tc_commit(&empty[slot]);
           advance();
         }
@@ -546,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         }
       }
       __syncwarp();
+      if (lane == 0 && ordinal == 0) MOE_STAMP(9);
       // The image (codes of every K chunk, then their scale atoms) in one
       // batch of independent 16-byte loads per lane: a single L2 round trip.
       const uint4* src = reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes);
@@ -656,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[set]);
+      if (et == 0 && md.x == 0) MOE_STAMP(6);
       ++k;
       if (md.x == 0 || fc2_upper_half) {
 #pragma unroll
@@ -703,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
               break;
             }
           }
+          if (et == 0) MOE_STAMP(7);
           // Sum the pieces in CTA order, the owner's own piece first; the
           // loads of up to four pieces are issued together.
           for (int c0 = cta + 1; c0 < c_end; c0 += 4) {
@@ -753,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         epilogue_sync();
         if (et == 0 && u != a.withhold_unit)
           store_release_gpu(&a.hidden_flags[u * g.KC2 + p], 1u);
+        if (et == 0) MOE_STAMP(8);
       } else {
         // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
@@ -771,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
             dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
           }
+          if (et == 0) MOE_STAMP(12);
           continue;
         }
 #pragma unroll
@@ -790,14 +841,20 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           }
         }
         epilogue_sync();
+        if (et == 0) MOE_STAMP(12);
       }
     }
   }
 
+  if (tid == 0) MOE_STAMP(13);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+  if (tid == 0) {
+    MOE_STAMP(14);
+    span_leave(a.span);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -890,6 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = static_cast<int>(cluster_ctarank()), u = static_cast<int>(cluster_id_x());
   Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
   const int C = plan.C;
+  if (tid == 0) {
+    span_enter(a.span);
+    MOE_STAMP(0);
+  }
   struct {
     int f0, f1, j0, j1;
   } cr = {plan.fc1[rank], plan.fc1[rank + 1], plan.fc2[rank], plan.fc2[rank + 1]};
@@ -974,10 +1035,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kGatherWarp) {
       pre0 = a.unit_rows[u * kUnitRows + (lane >> 2)];
       pre1 = a.unit_rows[u * kUnitRows + (lane & 7)];
+      if (lane == 0) MOE_STAMP(3);
     }
   }
   if (u >= units) {  // a cluster without a unit (the same for all its CTAs and warps)
     if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+    if (tid == 0) span_leave(a.span);
     return;
   }
   // Every CTA's barriers are initialised before any CTA of the cluster
@@ -1004,6 +1067,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(ASF + slot * 2 * kScaleAtomBytes,
                   a.stages + static_cast<size_t>(e * g.SPE + stage) * kStageBytes + kStageWeightBytes,
                   2 * kScaleAtomBytes, &full[slot], policy);
+        if (n == 0) MOE_STAMP(1);
+        MOE_STAMP(2);
         ++n;
         if (++slot == S) {
           slot = 0;
@@ -1014,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = cr.f0; st < cr.f1 && ok; ++st) ok = issue(st, false);
       for (int q = cr.j0; q < cr.j1 && ok; ++q)
         for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(fc1_stages + q * g.KC2 + c, true);
+      MOE_STAMP_VALUE(15, static_cast<uint64_t>(n));
       if (ok)  // drain, as in the grid kernel
         for (int k = (n > S ? n - S : 0); k < n && ok; ++k) ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
       if (!ok) settle_copies();
@@ -1026,6 +1092,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0, slot = 0, k = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
+      bool fc2_seen = false;
+      (void)fc2_seen;
       auto acquire = [&](int set) {
         return k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
       };
@@ -1046,6 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           first_c = c;
         }
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        if (lead && n == 0) MOE_STAMP(4);
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
         tc_fence_after_sync();
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
@@ -1056,6 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
         tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
         tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+        if (lead) MOE_STAMP(5);
         tc_commit(&empty[slot]);
         advance();
         if (last) {
@@ -1068,6 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // FC2 reads the whole hidden vector of the unit, sent by the owners.
       if (ok && cr.j0 < cr.j1) {
         ok = wait_bar_cluster(cx, hidden, 0);
+        if (lead) MOE_STAMP(9);
         tc_fence_after_sync();
       }
       for (int q = cr.j0; q < cr.j1 && ok; ++q) {
@@ -1076,6 +1147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool started = false;
         for (int c = 0; c < g.KC2 && ok; ++c) {
           if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+          if (lead && !fc2_seen) {
+            MOE_STAMP(10);
+            fc2_seen = true;
+          }
           tc_fence_after_sync();
           const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
           if (k0 < ksteps) {
@@ -1090,6 +1165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
             started = true;
           }
+          if (lead) MOE_STAMP(11);
           tc_commit(&empty[slot]);
           advance();
         }
@@ -1194,6 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[set]);
+      if (et == 0 && md.x == 0) MOE_STAMP(6);
       ++k;
       if (md.x == 0 || fc2_upper_half) {
 #pragma unroll
@@ -1219,11 +1296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Each thread's arrival releases its own stores.
             mbar_arrive_remote(cluster_map(recv, owner));
           }
+          if (et == 0) MOE_STAMP(7);
           continue;
         }
         if (!md.w && owned_pieces > 0) {
           // Sum the other pieces in CTA order, after the owner's own.
           if (wait_bar_cluster(cx, recv, 0)) {
+            if (et == 0) MOE_STAMP(7);
             for (int j = 0; j < owned_pieces; ++j) {
               const float* src = RECV + j * stride;
 #pragma unroll
@@ -1251,6 +1330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_shared();  // generic writes, read by tensor-core and bulk copies
         epilogue_sync();
+        if (et == 0) MOE_STAMP(8);
         if (et == 0 && u != a.withhold_unit) {
           mbar_arrive(hidden);
           for (int d = 0; d < C; ++d) {
@@ -1280,6 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
           dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
         }
+        if (et == 0) MOE_STAMP(12);
       }
     }
   }
@@ -1293,12 +1374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kEpilogueWarp0) cluster_wait();  // the start-up barrier
   if (gave_up)
     for (int d = 0; d < C; ++d) st_cluster_u32(cluster_map(&misc[1], d), 1u);
+  if (tid == 0) MOE_STAMP(13);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();
   tc_fence_after_sync();
   if (tid == 0 && *cx.abort_flag) settle_copies();
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+  if (tid == 0) {
+    MOE_STAMP(14);
+    span_leave(a.span);
+  }
 }
 
 }  // namespace

@@ -53,6 +53,8 @@ struct ExpertsArgs {
   int withhold_unit;          // test hook: never publish this unit's hidden (-1 = off)
   int withhold_image;         // test hook (grid kernel): never deliver this unit's hidden
                               // image to shared memory (-1 = off)
+  uint64_t* span;             // or null: launch clock, [CTA][start, end] (moe_debug_kernel_span)
+  uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
 };
 
 int experts_smem_bytes(const Geometry& g);

@@ -40,6 +40,9 @@ struct moe_ctx {
   int withhold = -1;
   int withhold_image = -1;
   int allow_cluster = 1;  // one- and two-token calls may run on the cluster variant
+  uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
+  int span_on = 0;
+  uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
   uint64_t settings = 0;  // bumped by every setter that changes kernel arguments
   // moe_run_host in place: the call's two launches, captured once per set of
@@ -202,9 +205,10 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       4,                                                        // status
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
+      static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8,           // launch clock
   };
-  size_t offsets[12], total = 0;
-  for (int i = 0; i < 12; ++i) {
+  size_t offsets[13], total = 0;
+  for (int i = 0; i < 13; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -224,6 +228,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->status = reinterpret_cast<int32_t*>(w + offsets[9]);
   h->pair_kept = w + offsets[10];
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
+  h->span = reinterpret_cast<uint64_t*>(w + offsets[12]);
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
   return encode_weight_map(h);
@@ -298,6 +303,8 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.timeout_ns = h->timeout_ns;
   a.withhold_unit = h->withhold;
   a.withhold_image = h->withhold_image;
+  a.span = h->span_on ? h->span : nullptr;
+  a.trace = h->trace;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->allow_cluster != 0));
   return MOE_OK;
 }
@@ -577,6 +584,46 @@ int moe_debug_paths(moe_handle h, int allow_cluster) {
   ++h->settings;
   return MOE_OK;
 }
+
+int moe_debug_kernel_span(moe_handle h, int enable) {
+  if (h == nullptr || enable < 0 || enable > 1) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
+  if (enable && !h->span_on) {
+    MOE_CUDA(cudaDeviceSynchronize());
+    MOE_CUDA(cudaMemset(h->span, 0, static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8));
+  }
+  h->span_on = enable;
+  ++h->settings;
+  return MOE_OK;
+}
+
+int moe_read_kernel_span(moe_handle h, uint64_t* span_ns) {
+  if (h == nullptr || span_ns == nullptr) return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
+  std::vector<uint64_t> words(static_cast<size_t>(moe::kMaxSpanCtas) * 2);
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(words.data(), h->span, words.size() * 8, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(h->span, 0, words.size() * 8));
+  uint64_t first = ~0ull, last = 0;
+  for (size_t c = 0; c < words.size() / 2; ++c) {
+    if (words[2 * c] == 0) continue;  // no CTA of that index in the last launch
+    if (words[2 * c] < first) first = words[2 * c];
+    if (words[2 * c + 1] > last) last = words[2 * c + 1];
+  }
+  if (first == ~0ull || last < first) return MOE_ERR_STATE;
+  *span_ns = last - first;
+  return MOE_OK;
+}
+
+#ifdef MOE_TRACE
+// Trace builds only: per-CTA phase stamps (16 words per CTA) into `buffer`.
+int moe_debug_trace(moe_handle h, void* buffer) {
+  if (h == nullptr) return MOE_ERR_ARG;
+  h->trace = static_cast<uint64_t*>(buffer);
+  ++h->settings;
+  return MOE_OK;
+}
+#endif
 
 int moe_cluster_size(moe_handle h, int batch) {
   if (h == nullptr || check_batch(batch)) return -MOE_ERR_ARG;

@@ -660,3 +660,30 @@ def test_run_combined_leaves_out_dropped_pairs(moe):
     xq, xs = oracle.quantize_x(x)
     rows = oracle.pairs_forward(weights, xq, xs, bad)["out"]
     check_rows(got, oracle.combine(rows, rw, kept), "tiny combined with a repeated id")
+
+
+@pytest.mark.parametrize("name", ["tp8_b1", "tp16_b8"])
+def test_kernel_span_records_the_last_launch(moe, name):
+    """The launch clock (moe_debug_kernel_span) gives a positive span for the
+    last launch, on the cluster variant and on the grid kernel, leaves the rows
+    unchanged, reads each launch once, and records nothing when off."""
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    ref, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    moe.moe_debug_kernel_span(layer.handle, 1)
+    try:
+        for _ in range(3):
+            got, status = run_layer(moe, layer, x, ids)
+            assert status == moe.MOE_OK
+            np.testing.assert_array_equal(got, ref)
+            span = moe.moe_read_kernel_span(layer.handle)
+            assert 0 < span < 5_000_000, span
+            print(f"[{name}] span {span / 1e3:.2f} us")
+        with pytest.raises(moe.MoeError):
+            moe.moe_read_kernel_span(layer.handle)  # read already: nothing recorded since
+    finally:
+        moe.moe_debug_kernel_span(layer.handle, 0)
+    run_layer(moe, layer, x, ids)
+    with pytest.raises(moe.MoeError):
+        moe.moe_read_kernel_span(layer.handle)
