@@ -68,7 +68,7 @@ MAIN_CONFIG = "tp8_b1"
 EXTRA_CONFIGS = ["tp16_b8", "tp8_b64", "tp8_b256"]
 L2_FALLBACK_BYTES = 126 * 2 ** 20
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "cluster_kernel_tp8_b1.md")
-KERNEL_SOURCES = ["experts.cu", "ptx.cuh", "common.cuh", "kernels.h"]
+KERNEL_SOURCES = ["experts.cu", "small.cu", "pipeline.cuh", "ptx.cuh", "common.cuh", "kernels.h"]
 
 
 def parse():
@@ -408,8 +408,13 @@ class OurArm:
         return start.elapsed_time(end) / calls
 
     def kernel_label(self):
-        C = self.moe.moe_cluster_size(self.layers[0].handle, self.cfg.batch)
-        if C:
+        handle, B = self.layers[0].handle, self.cfg.batch
+        path = self.moe.moe_kernel_path(handle, B)
+        if path == self.moe.PATH_SMALL:
+            return ("small_kernel (one CTA per SM; unit table derived from the routing ids in the "
+                    "kernel; FC1 partial sums summed by every FC2 CTA; tcgen05 block-scaled MMA)")
+        if path == self.moe.PATH_CLUSTER:
+            C = self.moe.moe_cluster_size(handle, B)
             return (f"cluster_kernel (experts kernel on thread-block clusters of {C} CTAs, "
                     "one per unit; tcgen05 block-scaled MMA)")
         return "experts_kernel (persistent, tcgen05 block-scaled MMA)"

@@ -267,18 +267,27 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
  * mbarrier wait runs out and the CTA gives up (-1 = off, the default).
  * Checks the abort path: the call records MOE_ERR_DEVICE_TIMEOUT, finishes,
  * and the next call is unaffected. MOE_ERR_ARG below -1.
- * moe_debug_paths - test hook: 1 (the default) lets calls of one or two
- * tokens run on the cluster variant of the experts kernel (one cluster of
- * up to 8 CTAs per unit, partial sums and hidden chunks exchanged through
- * distributed shared memory) where the layer's shape allows it; 0 sends
- * every call to the grid kernel. The two cut the FC1 K range into split-K
- * pieces at different stages, so their FP32 sums are grouped differently
- * and may differ in the last bits. MOE_ERR_ARG for other values.
+ * moe_debug_paths - which experts kernel calls of one or two tokens run on:
+ * 1 (the default) the small-batch kernel (one CTA per SM, the unit table
+ * derived from the routing ids in the kernel, every FC2 CTA summing the FC1
+ * partial sums of its units itself) where the layer's shape fits it;
+ * 0 the persistent grid kernel; 2 the cluster variant (one thread-block
+ * cluster of up to 8 CTAs per unit, partial sums and hidden chunks through
+ * distributed shared memory) where the shape fits it. Calls of more tokens,
+ * and calls whose path does not fit, run on the grid kernel. The kernels
+ * cut the FC1 K range into split-K pieces at different stages, so their FP32
+ * sums are grouped differently and may differ in the last bits.
+ * MOE_ERR_ARG for other values.
+ * moe_kernel_path - the kernel a call of `batch` tokens runs on under the
+ * current setting: 0 grid, 1 small-batch, 2 cluster variant (calls through
+ * moe_experts, which has no routing ids, never take path 1).
+ * -MOE_ERR_ARG for a null handle or a batch outside [1, MOE_MAX_BATCH].
  */
 int moe_set_timeout(moe_handle h, uint64_t nanoseconds);
 int moe_debug_withhold(moe_handle h, int unit);
 int moe_debug_withhold_image(moe_handle h, int unit);
-int moe_debug_paths(moe_handle h, int allow_cluster);
+int moe_debug_paths(moe_handle h, int path);
+int moe_kernel_path(moe_handle h, int batch);
 
 /*
  * moe_debug_kernel_span - measurement hook: with enable = 1, every later
@@ -303,9 +312,9 @@ int moe_read_kernel_span(moe_handle h, uint64_t* span_ns);
  * moe_cluster_size - the CTAs per thread-block cluster that a call of
  * `batch` tokens on this layer runs on: on the cluster variant the largest
  * size up to 8 of which one cluster per possible unit (min(E, 16 batch)) is
- * resident at once; 0 on the grid kernel (more than two tokens, shapes
- * whose split-K pieces do not fit the variant's receive buffer, too few
- * resident clusters, or moe_debug_paths(h, 0)). -MOE_ERR_ARG for a null handle or a
+ * resident at once; 0 when the call does not run on it (more than two
+ * tokens, shapes whose split-K pieces do not fit the variant's receive
+ * buffer, too few resident clusters, or any moe_debug_paths setting but 2). -MOE_ERR_ARG for a null handle or a
  * batch outside [1, MOE_MAX_BATCH].
  */
 int moe_cluster_size(moe_handle h, int batch);

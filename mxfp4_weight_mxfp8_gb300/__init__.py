@@ -23,6 +23,7 @@ __all__ = [
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
     "MAX_BATCH", "moe_device_supported", "moe_debug_kernel_span", "moe_read_kernel_span",
+    "moe_kernel_path", "PATH_GRID", "PATH_SMALL", "PATH_CLUSTER",
 ]
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
@@ -67,6 +68,7 @@ def _load():
         "moe_debug_withhold_image": ([vp, i32], i32),
         "moe_debug_paths": ([vp, i32], i32),
         "moe_cluster_size": ([vp, i32], i32),
+        "moe_kernel_path": ([vp, i32], i32),
         "moe_info": ([vp, ctypes.POINTER(MoeInfo)], i32),
         "moe_destroy": ([vp], None),
         "moe_error_string": ([i32], ctypes.c_char_p),
@@ -206,8 +208,20 @@ def moe_debug_withhold_image(handle, unit: int):
     return _check(_lib.moe_debug_withhold_image(handle, unit), "moe_debug_withhold_image")
 
 
-def moe_debug_paths(handle, allow_cluster: int):
-    return _check(_lib.moe_debug_paths(handle, allow_cluster), "moe_debug_paths")
+PATH_GRID, PATH_SMALL, PATH_CLUSTER = 0, 1, 2
+
+
+def moe_debug_paths(handle, path: int):
+    """0 grid kernel, 1 small-batch kernel (default), 2 cluster variant."""
+    return _check(_lib.moe_debug_paths(handle, path), "moe_debug_paths")
+
+
+def moe_kernel_path(handle, batch: int) -> int:
+    """The experts kernel a call of `batch` tokens runs on (PATH_*)."""
+    n = _lib.moe_kernel_path(handle, batch)
+    if n < 0:
+        raise MoeError(-n, "moe_kernel_path")
+    return n
 
 
 def moe_debug_kernel_span(handle, enable: int):

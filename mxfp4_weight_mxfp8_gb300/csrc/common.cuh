@@ -32,7 +32,13 @@ constexpr int kAccSets = 4;               // TMEM accumulator sets
 constexpr int kAccSetColumns = kMmaWarps * 8;       // one N = 8 accumulator per issuer
 constexpr int kTmemScaleBase = kAccSets * kAccSetColumns;  // 128: per-slot scale columns
 constexpr int kSlotScaleColumns = kMmaWarps * 8;    // per issuer: A atom (4) + B atom (4)
+// FC2 hidden-vector scale atoms, copied once per unit: per issuer, 2 image
+// buffers x kMaxInterChunks chunks x 4 columns, after the per-slot columns.
+constexpr int kTmemHiddenScaleBase = kTmemScaleBase + kRingStages * kSlotScaleColumns;  // 320
+constexpr int kHiddenScaleColumns = 2 * 4 * 4;  // per issuer
 constexpr int kTmemColumns = 512;
+static_assert(kTmemHiddenScaleBase + kMmaWarps * kHiddenScaleColumns <= kTmemColumns,
+              "TMEM columns: accumulators, slot scales and hidden scales fit");
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp0 = 1;              // warps 1..4
 constexpr int kGatherWarp = 5;

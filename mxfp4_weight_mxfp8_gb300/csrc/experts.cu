@@ -35,244 +35,12 @@
 // Calls of one or two tokens run on cluster_kernel (below) instead: one
 // thread-block cluster per unit, the same roles and stages, and the two
 // hand-offs through distributed shared memory.
-#include "kernels.h"
-#include "ptx.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace {
 
 using namespace ptx;
-
-constexpr int S = kRingStages;
-constexpr int NACC = kAccSets;
-constexpr int kHalvesFrom = 256;  // more units than this: split them into halves A and B
-constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memory
-constexpr int kAgreeSlots = 2 * NACC;  // epilogue decisions in flight after an abort
-
-// Shared-memory carve-up. The swizzled operand images (weights, activation
-// and hidden codes) start on 1024-byte boundaries, every other region on a
-// 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
-struct Layout {
-  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, bytes;
-  __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
-  __host__ __device__ explicit Layout(int kc2) {
-    int o = 0;
-    w = o;                 o += S * kStageSmemWeights;
-    act = o = up(o, 1024); o += S * kActImageBytes;
-    hcodes = o = up(o, 1024); o += 2 * kc2 * kActImageBytes;
-    asf = o = up(o, 16);   o += S * 2 * kScaleAtomBytes;
-    out = o = up(o, 16);   o += kUnitRows * 2 * kTileM * 2;
-    bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
-    hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
-    table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
-    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4 + kMmaWarps) * 8;
-    meta = o = up(o, 16);  o += NACC * 16;
-    misc = o = up(o, 16);  o += 16;
-    rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
-    agree = o = up(o, 16); o += kAgreeSlots * 4;
-    bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
-  }
-  __host__ __device__ bool aligned() const {
-    return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
-           out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
-           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0 && agree % 16 == 0;
-  }
-};
-
-// Per-call split of the work over the grid: FC1 stages and FC2 jobs are each
-// cut evenly over the CTAs. A unit's FC2 waits for its hidden vector, which is
-// complete only when the FC1 ranges holding its items are done, so the FC1
-// ranges are kept equal rather than evening out FC1 + FC2 stages per CTA.
-// Every CTA computes the same table.
-struct Split {
-  int T1, J, G;
-  __host__ __device__ Split(int units, const Geometry& g, int grid) {
-    T1 = units * g.P1 * g.KC1;
-    J = units * g.NQ;
-    G = grid;
-  }
-  // 32-bit products: T1 <= 2M stages and c <= 256 for every supported layer.
-  __host__ __device__ int fc2_begin(int c) const {
-    const uint32_t cu = static_cast<uint32_t>(c);
-    return static_cast<int>(cu * static_cast<uint32_t>(J) / static_cast<uint32_t>(G));
-  }
-  __host__ __device__ int fc1_begin(int c) const {
-    if (c >= G) return T1;
-    const uint32_t cu = static_cast<uint32_t>(c);
-    return static_cast<int>(cu * static_cast<uint32_t>(T1) / static_cast<uint32_t>(G));
-  }
-};
-
-struct Ctx {
-  const ExpertsArgs* a;
-  volatile uint32_t* abort_flag;
-};
-
-// Bounded mbarrier wait: false after the time limit (recording the error)
-// or once another role of this CTA has given up.
-__device__ bool wait_bar(const Ctx& cx, uint64_t* bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t start = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*cx.abort_flag) return false;
-      if (global_timer_ns() - start > cx.a->timeout_ns) {
-        *cx.abort_flag = 1;
-        report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// wait_bar for barriers that other CTAs of the cluster arrive on.
-__device__ bool wait_bar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity) {
-  if (mbar_test_cluster(bar, parity)) return true;
-  const uint64_t start = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test_cluster(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*cx.abort_flag) return false;
-      if (global_timer_ns() - start > cx.a->timeout_ns) {
-        *cx.abort_flag = 1;
-        report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Bounded wait on a completion that is bound to come (this thread's own
-// tensor-core work, or a barrier another thread has seen complete), taken
-// after a failure as well: the abort flag does not end it.
-__device__ void wait_own(const Ctx& cx, uint64_t* bar, uint32_t parity) {
-  const uint64_t start = global_timer_ns();
-  for (uint32_t i = 1; !mbar_test(bar, parity); ++i) {
-    if ((i & 63u) == 0 && global_timer_ns() - start > cx.a->timeout_ns) {
-      report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
-      return;
-    }
-  }
-}
-
-// The epilogue threads' common decision on accumulator k (true: process it).
-// A thread that saw the barrier complete and then the abort flag still clear
-// goes on: the barrier completed before any abort. Any other thread calls
-// this: it tests the barrier once more and proposes to go on if it has
-// completed, to stop if not; the first proposal for k, kept by
-// compare-and-swap, decides for every such thread. The two kinds agree, as a
-// proposal to stop shows that the barrier had not completed when the abort
-// came. So no epilogue warp goes on into a named barrier that another has
-// left. A thread runs at most NACC accumulators ahead of another, so
-// 2 * NACC slots keep the decisions in flight apart.
-__device__ __noinline__ bool epilogue_agree(const Ctx& cx, uint64_t* bar, uint32_t parity, int k, int* agree) {
-  const int proposal = (k << 2) | (mbar_test(bar, parity) ? 1 : 2);
-  int* slot = agree + (k & (kAgreeSlots - 1));
-  int v = *reinterpret_cast<volatile int*>(slot);
-  while ((v >> 2) != k) {
-    const int w = atomicCAS(slot, v, proposal);
-    v = w == v ? proposal : w;
-  }
-  if ((v & 3) != 1) return false;
-  wait_own(cx, bar, parity);  // completed already: some thread saw it
-  return true;
-}
-
-// After a failed wait nobody waits for the copies still in flight into (or
-// out of) this CTA's shared memory: give them 50 us to land before it exits.
-__device__ void settle_copies() {
-  const uint64_t start = global_timer_ns();
-  while (global_timer_ns() - start < 50000) __nanosleep(1000);
-}
-
-// Release increment (no result): the caller's earlier stores, and those of
-// the threads it synchronized with, are visible to whoever acquires the count.
-__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Launch clock (moe_debug_kernel_span): CTA c stores its start and end times
-// (%globaltimer) into words 2c and 2c + 1; plain stores, so the clock costs
-// the launch nothing measurable. The host reduces them to the launch's span.
-__device__ __forceinline__ void span_enter(uint64_t* span) {
-  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x] = global_timer_ns();
-}
-
-__device__ __forceinline__ void span_leave(uint64_t* span) {
-  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x + 1] = global_timer_ns();
-}
-
-// Phase stamps for timing studies, compiled in only with -DMOE_TRACE: slot k
-// of this CTA's 16-word record gets the time the CTA passed point k.
-#ifdef MOE_TRACE
-#define MOE_STAMP(k)                                                                        \
-  do {                                                                                      \
-    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
-  } while (0)
-#define MOE_STAMP_VALUE(k, v)                                                              \
-  do {                                                                                     \
-    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 16 + (k)] = (v);     \
-  } while (0)
-#else
-#define MOE_STAMP(k) \
-  do {               \
-  } while (0)
-#define MOE_STAMP_VALUE(k, v) \
-  do {                        \
-  } while (0)
-#endif
-
-__device__ __forceinline__ float silu_times(float gate, float up) {
-  return gate / (1.0f + expf(-gate)) * up;
-}
-
-__device__ __forceinline__ uint64_t desc_sw128(const void* p) {
-  return smem_desc(smem_addr(p), 16, 1024, 2);
-}
-__device__ __forceinline__ uint64_t desc_scales(const void* p) {
-  return smem_desc(smem_addr(p), 128, 128, 0);
-}
-
-// FC1 stage cursor: stage s = (item * KC1 + c), item = u * P1 + p.
-struct Fc1Cursor {
-  int s, item, c, u, p;
-  __device__ Fc1Cursor(int s0, const Geometry& g) : s(s0) {
-    item = s0 / g.KC1;
-    c = s0 - item * g.KC1;
-    u = item / g.P1;
-    p = item - u * g.P1;
-  }
-  __device__ void next(const Geometry& g) {
-    ++s;
-    if (++c == g.KC1) {
-      c = 0;
-      ++item;
-      if (++p == g.P1) {
-        p = 0;
-        ++u;
-      }
-    }
-  }
-};
-
-// FC2 job cursor: job j = u * NQ + q.
-struct Fc2Cursor {
-  int j, u, q;
-  __device__ Fc2Cursor(int j0, const Geometry& g) : j(j0) {
-    u = j0 / g.NQ;
-    q = j0 - u * g.NQ;
-  }
-  __device__ void next(const Geometry& g) {
-    ++j;
-    if (++q == g.NQ) {
-      q = 0;
-      ++u;
-    }
-  }
-};
 
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ ExpertsArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -352,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (tid == 0) MOE_STAMP(16);
   const uint32_t tmem = misc[0];
   int f0[2], f1[2], j0[2], j1[2];
   for (int h = 0; h < 2; ++h) {
@@ -410,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (lane == 0) {
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
+      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase + issuer * kHiddenScaleColumns;
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -466,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           hb = ordinal & 1;
           if (!(ok = wait_bar(cx, &hfull[hb], (ordinal >> 1) & 1))) break;
           tc_fence_after_sync();
+          // The unit's hidden scale atoms, once for all its jobs.
+          for (int c = 0; c < g.KC2; ++c)
+            tc_copy_scales(hsf_cols + hb * 16 + c * 4, desc_scales(HSF + (hb * g.KC2 + c) * kScaleAtomBytes));
           cu = cur.u;
         }
         const int set = k % NACC;
@@ -483,15 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           if (k0 < ksteps) {
             const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
             const int hc = hb * g.KC2 + c;
+            const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-            tc_copy_scales(sf + 4, desc_scales(HSF + hc * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
             const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
             // Descriptor start addresses count 16-byte units: +2 is the next K-step.
-            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sf + 4, started ? 1u : 0u);
+            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
             if (k0 + 1 < ksteps)
-              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sfh, 1u);
             started = true;
           }
           if (lead) MOE_STAMP(11);
@@ -577,15 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lane == 0) freed = wait_bar(cx, &hempty[b], ((ordinal >> 1) - 1) & 1);
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
-      // Wait (bounded) for every K chunk of the unit's hidden vector: lane l
-      // polls chunk l % KC2 with acquire loads, so all chunks are polled at
-      // once; the warp barrier then orders every lane's image loads behind
-      // all of the lanes' acquires. (An acquire load costs less than a
-      // relaxed poll followed by a fence.)
+      // Wait (bounded) for every K chunk of the unit's hidden vector: lane
+      // l < KC2 polls chunk l with acquire loads (a short back-off between
+      // polls), so all chunks are polled at once; the warp barrier then
+      // orders every lane's image loads behind all of the acquires.
       const uint64_t t_start = global_timer_ns();
-      const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + (lane % g.KC2);
+      const uint32_t* flag = a.hidden_flags + cur.u * g.KC2 + (lane < g.KC2 ? lane : 0);
       for (uint32_t i = 0;; ++i) {
-        if (__all_sync(0xFFFFFFFFu, load_acquire_gpu(flag) != 0)) break;
+        if (__all_sync(0xFFFFFFFFu, lane >= g.KC2 || load_acquire_gpu(flag) != 0)) break;
+        __nanosleep(32);
         if ((i & 7u) == 7u && global_timer_ns() - t_start > a.timeout_ns) {
           if (lane == 0) report(a.status, MOE_ERR_DEVICE_TIMEOUT);
           break;  // proceed with whatever the image holds
@@ -743,14 +516,20 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           int c_end = cta + 1;
           uint32_t others = 0;
           for (; c_end < G && st[c_end] <= item_last; ++c_end) others += st[c_end] < st[c_end + 1];
-          const uint64_t t_wait = global_timer_ns();
-          // Every thread acquires the count itself before it loads partials.
-          for (uint32_t i = 0; load_acquire_gpu(&a.item_counters[item]) < others; ++i) {
-            if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
-              report(a.status, MOE_ERR_DEVICE_TIMEOUT);
-              break;
+          // One thread acquires the count (with a short back-off, so that the
+          // polls of many owners do not crowd the counters' L2 lines); the
+          // epilogue barrier orders every thread's partial-sum loads after it.
+          if (et == 0) {
+            const uint64_t t_wait = global_timer_ns();
+            for (uint32_t i = 0; load_acquire_gpu(&a.item_counters[item]) < others; ++i) {
+              __nanosleep(64);
+              if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
+                report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                break;
+              }
             }
           }
+          epilogue_sync();
           if (et == 0) MOE_STAMP(7);
           // Sum the pieces in CTA order, the owner's own piece first; the
           // loads of up to four pieces are issued together.
@@ -789,9 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           for (int t = 0; t < 8; ++t) {
             if (t >= valid) break;
             const float h = silu_times(v0[t], v1[t]);
-            float amax = fabsf(h);
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+            const float amax = warp_amax(h);
             const int E = mx_exponent(amax, g.floor_rule != 0);
             img[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
             if (lane == 0)
@@ -991,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (tid == 0) MOE_STAMP(16);
   const uint32_t tmem = misc[0];
   // Each warp waits for the prep grid only for what it reads itself: the
   // unit count, and the unit's expert (producer) or rows (gather warp), in
@@ -1027,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int below = __shfl_sync(0xFFFFFFFFu, incl - cnt, w);
     const unsigned ww = __shfl_sync(0xFFFFFFFFu, word, w);
     pre0 = who ? w * 32 + static_cast<int>(__fns(ww, 0, u - below + 1)) : 0;
+    if (lane == 0) MOE_STAMP(17);
   } else {
     grid_dependency_wait();
     units = *a.unit_count;
@@ -1048,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // epilogue, the only role that reaches into other CTAs, waits before it
   // starts (the other roles wait at the end).
   cluster_arrive();
+  if (tid == 0) MOE_STAMP(18);
   const int fc1_stages = T1;
 
   if (warp == kProducerWarp) {
@@ -1089,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;
+      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase + issuer * kHiddenScaleColumns;
       int n = 0, slot = 0, k = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -1140,6 +921,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar_cluster(cx, hidden, 0);
         if (lead) MOE_STAMP(9);
         tc_fence_after_sync();
+        // The unit's hidden scale atoms, once for all its jobs.
+        for (int c = 0; c < g.KC2 && ok; ++c)
+          tc_copy_scales(hsf_cols + c * 4, desc_scales(HSF + c * kScaleAtomBytes));
       }
       for (int q = cr.j0; q < cr.j1 && ok; ++q) {
         const int set = k % NACC;
@@ -1155,14 +939,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
           if (k0 < ksteps) {
             const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            const uint32_t sfh = hsf_cols + c * 4;
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-            tc_copy_scales(sf + 4, desc_scales(HSF + c * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + c * kActImageBytes + k0 * 32);
             const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
-            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sf + 4, started ? 1u : 0u);
+            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
             if (k0 + 1 < ksteps)
-              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sfh, 1u);
             started = true;
           }
           if (lead) MOE_STAMP(11);
@@ -1320,9 +1104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < kClusterMaxRows; ++t) {
             if (t >= valid) break;
             const float h = silu_times(v0[t], v1[t]);
-            float amax = fabsf(h);
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+            const float amax = warp_amax(h);
             const int E = mx_exponent(amax, g.floor_rule != 0);
             HC[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
             if (lane == 0) HSF[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
@@ -1406,6 +1188,8 @@ cudaError_t experts_configure(const Geometry& g) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  e = small_configure();
+  if (e != cudaSuccess) return e;
   for (int C = 2; C <= 8; ++C) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);
@@ -1455,7 +1239,9 @@ cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
 }
 
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
-                           bool allow_cluster) {
+                           int path, bool small_ok) {
+  if (path == kPathSmall && small_ok && a.ids != nullptr && a.B <= 2)
+    return launch_small(a, grid, stream, pdl);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1469,7 +1255,7 @@ cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, 
     ++n;
   }
   cfg.attrs = attr;
-  const int C = allow_cluster ? cluster_size_for(a.g, a.B) : 0;
+  const int C = path == kPathCluster ? cluster_size_for(a.g, a.B) : 0;
   if (C > 0) {
     // One cluster per possible unit: at most min(E, 16B) in these calls.
     attr[n].id = cudaLaunchAttributeClusterDimension;

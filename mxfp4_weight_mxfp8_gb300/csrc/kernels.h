@@ -72,11 +72,18 @@ struct ClusterPlan {
   int8_t slot[kMaxInterChunks][8];
 };
 
-// One- and two-token calls run on thread-block clusters (one per unit) when
-// allow_cluster and the layer's shape fits that variant; all others on the grid.
+// Which experts kernel serves a call: kPathGrid always the persistent grid
+// kernel; kPathSmall (default) the small-batch kernel for calls of one or two
+// tokens whose routing ids are given and whose split fits it (small_fits),
+// else the grid kernel; kPathCluster the cluster variant for one or two
+// tokens where the shape fits it, else the grid kernel.
+enum ExpertsPath : int { kPathGrid = 0, kPathSmall = 1, kPathCluster = 2 };
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
-                           bool allow_cluster);
+                           int path, bool small_ok);
 int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serves this call
+bool small_fits(const Geometry& g, int batch, int grid);
+cudaError_t small_configure();
+cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
 
 // Routing-weighted combine of each token's 16 rows (after the experts kernel).
 struct CombineArgs {

@@ -39,7 +39,8 @@ struct moe_ctx {
   uint64_t timeout_ns = 2000000000ull;
   int withhold = -1;
   int withhold_image = -1;
-  int allow_cluster = 1;  // one- and two-token calls may run on the cluster variant
+  int path = moe::kPathSmall;  // which experts kernel one- and two-token calls run on
+  int small_ok[3] = {0, 0, 0};  // [batch]: the small-batch kernel's split fits this layer
   uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
@@ -170,6 +171,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     return MOE_ERR_UNSUPPORTED;
   }
   h->grid = h->sms < moe::kMaxGrid ? h->sms : moe::kMaxGrid;  // one co-resident CTA per SM
+  for (int b = 1; b <= 2; ++b) h->small_ok[b] = moe::small_fits(g, b, h->grid) ? 1 : 0;
 
   // Weights: one 17 KB block per stage.
   h->stage_bytes = static_cast<size_t>(g.E) * g.SPE * moe::kStageBytes;
@@ -305,7 +307,7 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.withhold_image = h->withhold_image;
   a.span = h->span_on ? h->span : nullptr;
   a.trace = h->trace;
-  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->allow_cluster != 0));
+  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
   return MOE_OK;
 }
 
@@ -578,9 +580,9 @@ int moe_debug_withhold_image(moe_handle h, int unit) {
   return MOE_OK;
 }
 
-int moe_debug_paths(moe_handle h, int allow_cluster) {
-  if (h == nullptr || allow_cluster < 0 || allow_cluster > 1) return MOE_ERR_ARG;
-  h->allow_cluster = allow_cluster;
+int moe_debug_paths(moe_handle h, int path) {
+  if (h == nullptr || path < moe::kPathGrid || path > moe::kPathCluster) return MOE_ERR_ARG;
+  h->path = path;
   ++h->settings;
   return MOE_OK;
 }
@@ -627,7 +629,14 @@ int moe_debug_trace(moe_handle h, void* buffer) {
 
 int moe_cluster_size(moe_handle h, int batch) {
   if (h == nullptr || check_batch(batch)) return -MOE_ERR_ARG;
-  return h->allow_cluster ? moe::cluster_size_for(h->g, batch) : 0;
+  return h->path == moe::kPathCluster ? moe::cluster_size_for(h->g, batch) : 0;
+}
+
+int moe_kernel_path(moe_handle h, int batch) {
+  if (h == nullptr || check_batch(batch)) return -MOE_ERR_ARG;
+  if (batch <= 2 && h->path == moe::kPathSmall && h->small_ok[batch]) return moe::kPathSmall;
+  if (h->path == moe::kPathCluster && moe::cluster_size_for(h->g, batch) > 0) return moe::kPathCluster;
+  return moe::kPathGrid;
 }
 
 int moe_info(moe_handle h, moe_info_t* info) {
@@ -784,7 +793,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.timeout_ns = h->timeout_ns;
   ea.withhold_unit = -1;
   ea.withhold_image = -1;
-  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->allow_cluster != 0));
+  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->path, batch <= 2 && h->small_ok[batch]));
   return MOE_OK;
 }
 

@@ -1,0 +1,257 @@
+// Device-side building blocks shared by the experts kernels (the persistent
+// grid kernel, its cluster variant and the small-batch kernel): the
+// shared-memory carve-up, the per-call work split, bounded mbarrier waits and
+// the epilogue's abort agreement, the launch clock and phase stamps, and the
+// FC1 / FC2 work cursors. Each translation unit that includes it gets its own
+// copy (internal linkage).
+#pragma once
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int S = kRingStages;
+constexpr int NACC = kAccSets;
+constexpr int kHalvesFrom = 256;  // more units than this: split them into halves A and B
+constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memory
+constexpr int kAgreeSlots = 2 * NACC;  // epilogue decisions in flight after an abort
+constexpr uint32_t kWaitHintNs = 20000;  // longest suspension of one mbarrier wait step
+
+// Shared-memory carve-up. The swizzled operand images (weights, activation
+// and hidden codes) start on 1024-byte boundaries, every other region on a
+// 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
+struct Layout {
+  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, bytes;
+  __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
+  __host__ __device__ explicit Layout(int kc2) {
+    int o = 0;
+    w = o;                 o += S * kStageSmemWeights;
+    act = o = up(o, 1024); o += S * kActImageBytes;
+    hcodes = o = up(o, 1024); o += 2 * kc2 * kActImageBytes;
+    asf = o = up(o, 16);   o += S * 2 * kScaleAtomBytes;
+    out = o = up(o, 16);   o += kUnitRows * 2 * kTileM * 2;
+    bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
+    hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
+    table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
+    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4 + kMmaWarps) * 8;
+    meta = o = up(o, 16);  o += NACC * 16;
+    misc = o = up(o, 16);  o += 16;
+    rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
+    agree = o = up(o, 16); o += kAgreeSlots * 4;
+    bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
+  }
+  __host__ __device__ bool aligned() const {
+    return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
+           out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
+           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0 && agree % 16 == 0;
+  }
+};
+
+// Per-call split of the work over the grid: FC1 stages and FC2 jobs are each
+// cut evenly over the CTAs. A unit's FC2 waits for its hidden vector, which is
+// complete only when the FC1 ranges holding its items are done, so the FC1
+// ranges are kept equal rather than evening out FC1 + FC2 stages per CTA.
+// Every CTA computes the same table.
+struct Split {
+  int T1, J, G;
+  __host__ __device__ Split(int units, const Geometry& g, int grid) {
+    T1 = units * g.P1 * g.KC1;
+    J = units * g.NQ;
+    G = grid;
+  }
+  // 32-bit products: T1 <= 2M stages and c <= 256 for every supported layer.
+  __host__ __device__ int fc2_begin(int c) const {
+    const uint32_t cu = static_cast<uint32_t>(c);
+    return static_cast<int>(cu * static_cast<uint32_t>(J) / static_cast<uint32_t>(G));
+  }
+  __host__ __device__ int fc1_begin(int c) const {
+    if (c >= G) return T1;
+    const uint32_t cu = static_cast<uint32_t>(c);
+    return static_cast<int>(cu * static_cast<uint32_t>(T1) / static_cast<uint32_t>(G));
+  }
+};
+
+struct Ctx {
+  const ExpertsArgs* a;
+  volatile uint32_t* abort_flag;
+};
+
+// Bounded mbarrier wait: false after the time limit (recording the error)
+// or once another role of this CTA has given up.
+__device__ bool wait_bar(const Ctx& cx, uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t start = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_wait_hint(bar, parity, kWaitHintNs)) return true;
+    if ((i & 7u) == 0) {
+      if (*cx.abort_flag) return false;
+      if (global_timer_ns() - start > cx.a->timeout_ns) {
+        *cx.abort_flag = 1;
+        report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// wait_bar for barriers that other CTAs of the cluster arrive on.
+__device__ bool wait_bar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const uint64_t start = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*cx.abort_flag) return false;
+      if (global_timer_ns() - start > cx.a->timeout_ns) {
+        *cx.abort_flag = 1;
+        report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Bounded wait on a completion that is bound to come (this thread's own
+// tensor-core work, or a barrier another thread has seen complete), taken
+// after a failure as well: the abort flag does not end it.
+__device__ void wait_own(const Ctx& cx, uint64_t* bar, uint32_t parity) {
+  const uint64_t start = global_timer_ns();
+  for (uint32_t i = 1; !mbar_test(bar, parity); ++i) {
+    if ((i & 63u) == 0 && global_timer_ns() - start > cx.a->timeout_ns) {
+      report(cx.a->status, MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// The epilogue threads' common decision on accumulator k (true: process it).
+// A thread that saw the barrier complete and then the abort flag still clear
+// goes on: the barrier completed before any abort. Any other thread calls
+// this: it tests the barrier once more and proposes to go on if it has
+// completed, to stop if not; the first proposal for k, kept by
+// compare-and-swap, decides for every such thread. The two kinds agree, as a
+// proposal to stop shows that the barrier had not completed when the abort
+// came. So no epilogue warp goes on into a named barrier that another has
+// left. A thread runs at most NACC accumulators ahead of another, so
+// 2 * NACC slots keep the decisions in flight apart.
+__device__ __noinline__ bool epilogue_agree(const Ctx& cx, uint64_t* bar, uint32_t parity, int k, int* agree) {
+  const int proposal = (k << 2) | (mbar_test(bar, parity) ? 1 : 2);
+  int* slot = agree + (k & (kAgreeSlots - 1));
+  int v = *reinterpret_cast<volatile int*>(slot);
+  while ((v >> 2) != k) {
+    const int w = atomicCAS(slot, v, proposal);
+    v = w == v ? proposal : w;
+  }
+  if ((v & 3) != 1) return false;
+  wait_own(cx, bar, parity);  // completed already: some thread saw it
+  return true;
+}
+
+// After a failed wait nobody waits for the copies still in flight into (or
+// out of) this CTA's shared memory: give them 50 us to land before it exits.
+__device__ void settle_copies() {
+  const uint64_t start = global_timer_ns();
+  while (global_timer_ns() - start < 50000) __nanosleep(1000);
+}
+
+// Release increment (no result): the caller's earlier stores, and those of
+// the threads it synchronized with, are visible to whoever acquires the count.
+__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Launch clock (moe_debug_kernel_span): CTA c stores its start and end times
+// (%globaltimer) into words 2c and 2c + 1; plain stores, so the clock costs
+// the launch nothing measurable. The host reduces them to the launch's span.
+__device__ __forceinline__ void span_enter(uint64_t* span) {
+  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x] = global_timer_ns();
+}
+
+__device__ __forceinline__ void span_leave(uint64_t* span) {
+  if (span != nullptr && blockIdx.x < kMaxSpanCtas) span[2 * blockIdx.x + 1] = global_timer_ns();
+}
+
+// Phase stamps for timing studies, compiled in only with -DMOE_TRACE: slot k
+// of this CTA's 32-word record gets the time the CTA passed point k.
+#ifdef MOE_TRACE
+#define MOE_STAMP(k)                                                                        \
+  do {                                                                                      \
+    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 32 + (k)] = global_timer_ns(); \
+  } while (0)
+#define MOE_STAMP_VALUE(k, v)                                                              \
+  do {                                                                                     \
+    if (a.trace != nullptr) a.trace[static_cast<size_t>(blockIdx.x) * 32 + (k)] = (v);     \
+  } while (0)
+#else
+#define MOE_STAMP(k) \
+  do {               \
+  } while (0)
+#define MOE_STAMP_VALUE(k, v) \
+  do {                        \
+  } while (0)
+#endif
+
+// The largest |v| over the 32 lanes of the warp, in one warp reduction: for
+// non-negative floats (finite or infinite) the order of the bit patterns as
+// unsigned integers is the order of the values.
+__device__ __forceinline__ float warp_amax(float v) {
+  return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
+}
+
+__device__ __forceinline__ float silu_times(float gate, float up) {
+  return gate / (1.0f + expf(-gate)) * up;
+}
+
+__device__ __forceinline__ uint64_t desc_sw128(const void* p) {
+  return smem_desc(smem_addr(p), 16, 1024, 2);
+}
+__device__ __forceinline__ uint64_t desc_scales(const void* p) {
+  return smem_desc(smem_addr(p), 128, 128, 0);
+}
+
+// FC1 stage cursor: stage s = (item * KC1 + c), item = u * P1 + p.
+struct Fc1Cursor {
+  int s, item, c, u, p;
+  __device__ Fc1Cursor(int s0, const Geometry& g) : s(s0) {
+    item = s0 / g.KC1;
+    c = s0 - item * g.KC1;
+    u = item / g.P1;
+    p = item - u * g.P1;
+  }
+  __device__ void next(const Geometry& g) {
+    ++s;
+    if (++c == g.KC1) {
+      c = 0;
+      ++item;
+      if (++p == g.P1) {
+        p = 0;
+        ++u;
+      }
+    }
+  }
+};
+
+// FC2 job cursor: job j = u * NQ + q.
+struct Fc2Cursor {
+  int j, u, q;
+  __device__ Fc2Cursor(int j0, const Geometry& g) : j(j0) {
+    u = j0 / g.NQ;
+    q = j0 - u * g.NQ;
+  }
+  __device__ void next(const Geometry& g) {
+    ++j;
+    if (++q == g.NQ) {
+      q = 0;
+      ++u;
+    }
+  }
+};
+
+}  // namespace
+}  // namespace moe

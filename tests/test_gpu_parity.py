@@ -312,23 +312,34 @@ def test_supported_limits(moe, E, H, I, B, dist):
     layer.close()
 
 
+SMALL_PATHS = [1, 2]  # the small-batch kernel, the cluster variant
+
+
+def set_path(moe, layer, path, batch):
+    """Select an experts kernel for calls of `batch` tokens and check that it serves them."""
+    moe.moe_debug_paths(layer.handle, path)
+    assert moe.moe_kernel_path(layer.handle, batch) == path
+    if path == 2:
+        assert moe.moe_cluster_size(layer.handle, batch) >= 2
+
+
+@pytest.mark.parametrize("path", SMALL_PATHS, ids=["small", "cluster"])
 @pytest.mark.parametrize("E,H,I,B", [
-    (16, 512, 96, 1),      # partial tiles (I = 96), clusters of 6
+    (16, 512, 96, 1),      # partial tiles (I = 96); clusters of 6
     (16, 512, 96, 2),      # two-row units; the piece layout allows only small clusters
-    (8, 3584, 384, 1),     # fewer experts than slots: 8 units, clusters of 8
-    (32, 3584, 384, 2),    # the TP8 shard's shape at two tokens: clusters of 4, FC2 stages past the ring
+    (8, 3584, 384, 1),     # fewer experts than slots: 8 units; clusters of 8
+    (32, 3584, 384, 2),    # the TP8 shard's shape at two tokens; clusters of 4
     (1024, 256, 512, 2),   # the widest I with the smallest H
     (16, 16384, 512, 1),   # the largest H and I
 ])
-def test_cluster_path_shapes(moe, E, H, I, B):
-    """The cluster variant over the shapes it accepts, against the oracle."""
+def test_small_batch_path_shapes(moe, E, H, I, B, path):
+    """The small-batch kernel and the cluster variant over odd shapes, against the oracle."""
     weights = workload.make_weights(E, H, I, seed13=31, seed2=32)
     import torch
 
     layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
-    C = moe.moe_cluster_size(layer.handle, B)
-    print(f"[E={E} H={H} I={I} B={B}] clusters of {C}")
-    assert C >= 2
+    set_path(moe, layer, path, B)
+    print(f"[E={E} H={H} I={I} B={B}] path {path}, clusters of {moe.moe_cluster_size(layer.handle, B)}")
     x = workload.make_x(B, H, seed=33)
     ids = workload.make_ids(B, E, seed=34) if E >= 16 else np.stack(
         [np.random.default_rng(35 + t).permutation(16) % E for t in range(B)]).astype(np.int32)
@@ -337,34 +348,39 @@ def test_cluster_path_shapes(moe, E, H, I, B):
     if E >= 16:
         assert status == moe.MOE_OK
         ref = oracle.pairs_forward(weights, xq, xs, ids)
-        check_rows(got, ref["out"], f"cluster E={E} H={H} I={I} B={B}")
+        check_rows(got, ref["out"], f"path {path} E={E} H={H} I={I} B={B}")
     else:
         # 16 slots over 8 experts: each expert twice per token, the higher slot dropped.
         assert status == moe.MOE_ERR_DEVICE_IDS
         keep = np.array([t * 16 + s for t in range(B) for s in range(16)
                          if s == min(np.nonzero(ids[t] == ids[t, s])[0])], np.int32)
         ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=keep)
-        check_rows(got[keep], ref["out"], f"cluster E={E} H={H} I={I} B={B}")
+        check_rows(got[keep], ref["out"], f"path {path} E={E} H={H} I={I} B={B}")
     layer.close()
 
 
-def test_cluster_path_with_bad_and_repeated_ids(moe):
-    """One token whose ids include a repeat and an out-of-range id: 14 units,
-    so the last two clusters find no unit and leave at once."""
+@pytest.mark.parametrize("path", SMALL_PATHS, ids=["small", "cluster"])
+def test_small_batch_paths_with_bad_and_repeated_ids(moe, path):
+    """One token whose ids include a repeat and an out-of-range id: 14 units.
+    The small-batch kernel derives the same table from the ids in the kernel;
+    on the cluster variant the last two clusters find no unit and leave."""
     weights, x, ids = cached_inputs("tp8_b1")
     layer = layer_for(moe, weights)
-    assert moe.moe_cluster_size(layer.handle, 1) >= 2
+    set_path(moe, layer, path, 1)
     bad = ids.copy()
     bad[0, 9] = bad[0, 4]   # a repeat: slot 9 is dropped
     bad[0, 12] = 384        # out of range: slot 12 is dropped
-    got, status = run_layer(moe, layer, x, bad)
+    try:
+        got, status = run_layer(moe, layer, x, bad)
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
     assert status == moe.MOE_ERR_DEVICE_IDS
     experts, _ = units_of(moe, layer, 1)
     assert len(experts) == 14
     keep = np.array([s for s in range(16) if s not in (9, 12)], np.int32)
     xq, xs = oracle.quantize_x(x)
     ref = oracle.pairs_forward(weights, xq, xs, bad, pairs=keep)
-    check_rows(got[keep], ref["out"], "tp8 B1 with bad ids (cluster path)")
+    check_rows(got[keep], ref["out"], f"tp8 B1 with bad ids (path {path})")
 
 
 def test_repeated_expert_is_reported_and_others_kept(moe):
@@ -496,13 +512,12 @@ def test_out_of_range_ids_are_reported_and_skipped(moe):
     check_rows(got[keep], ref["out"], "tiny with bad ids")
 
 
-@pytest.mark.parametrize("allow_cluster", [1, 0], ids=["cluster", "grid"])
-def test_bounded_wait_reports_timeout_and_context_survives(moe, allow_cluster):
+@pytest.mark.parametrize("path", [1, 2, 0], ids=["small", "cluster", "grid"])
+def test_bounded_wait_reports_timeout_and_context_survives(moe, path):
     weights, x, ids = cached_inputs("tiny")
     layer = layer_for(moe, weights)
-    moe.moe_debug_paths(layer.handle, allow_cluster)
     try:
-        assert (moe.moe_cluster_size(layer.handle, x.shape[0]) > 0) == bool(allow_cluster)
+        set_path(moe, layer, path, x.shape[0])
         moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
         moe.moe_debug_withhold(layer.handle, 0)        # unit 0 never publishes its hidden vector
         _, status = run_layer(moe, layer, x, ids)
@@ -519,17 +534,19 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe, allow_cluster):
     check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
 
 
-@pytest.mark.parametrize("name", ["tiny", "tp16_b8"])
-def test_mbarrier_timeout_aborts_and_context_survives(moe, name):
+@pytest.mark.parametrize("name,path", [("tiny", 0), ("tp16_b8", 0), ("tiny", 1), ("tp8_b1", 1)],
+                         ids=["tiny-grid", "tp16_b8-grid", "tiny-small", "tp8_b1-small"])
+def test_mbarrier_timeout_aborts_and_context_survives(moe, name, path):
     """The grid kernel's abort path, made to run deterministically: the
     hidden loader never hands unit 0's image to the MMA issuers, so their
     bounded mbarrier wait runs out and every CTA with a job of that unit gives
     up (the other roles stop, MMAs drain, copies settle). The call reports
-    the timeout and ends; the next call is exact."""
+    the timeout and ends; the next call is exact. On the small-batch kernel
+    the epilogue never releases unit 0's hidden image to the issuers."""
     weights, x, ids = cached_inputs(name)
     layer = layer_for(moe, weights)
-    moe.moe_debug_paths(layer.handle, 0)
     try:
+        set_path(moe, layer, path, x.shape[0])
         moe.moe_set_timeout(layer.handle, 20_000_000)  # 20 ms
         moe.moe_debug_withhold_image(layer.handle, 0)
         _, status = run_layer(moe, layer, x, ids)
@@ -547,37 +564,35 @@ def test_mbarrier_timeout_aborts_and_context_survives(moe, name):
 
 
 @pytest.mark.parametrize("name", ["tiny", "tp8_b1"])
-def test_cluster_and_grid_paths_for_one_and_two_tokens(moe, name):
-    """One- and two-token calls run on thread-block clusters (one per unit,
-    split-K partials and hidden chunks exchanged in distributed shared
-    memory); the grid kernel still serves them when that variant is off.
-    Both meet the oracle's tolerances, and they agree with each other up to
-    the rounding of their different split-K groupings."""
+def test_three_paths_for_one_and_two_tokens(moe, name):
+    """One- and two-token calls run on the small-batch kernel by default; the
+    cluster variant and the grid kernel serve them when selected. All three
+    meet the oracle's tolerances and agree with each other up to the
+    rounding of their different split-K groupings."""
     weights, x, ids = cached_inputs(name)
     layer = layer_for(moe, weights)
     B = x.shape[0]
     pairs, ref = oracle_run(name)
-    assert moe.moe_cluster_size(layer.handle, B) >= 2
-    clus, status = run_layer(moe, layer, x, ids)
-    assert status == moe.MOE_OK
-    check_rows(clus[pairs], ref["out"], f"{name} cluster path")
-    moe.moe_debug_paths(layer.handle, 0)
+    assert moe.moe_kernel_path(layer.handle, B) == 1
+    rows = {}
     try:
-        assert moe.moe_cluster_size(layer.handle, B) == 0
-        grid, status = run_layer(moe, layer, x, ids)
+        for path, label in [(1, "small"), (2, "cluster"), (0, "grid")]:
+            set_path(moe, layer, path, B)
+            rows[label], status = run_layer(moe, layer, x, ids)
+            assert status == moe.MOE_OK
+            check_rows(rows[label][pairs], ref["out"], f"{name} {label} path")
     finally:
         moe.moe_debug_paths(layer.handle, 1)
-    assert status == moe.MOE_OK
-    check_rows(grid[pairs], ref["out"], f"{name} grid path")
-    a = bf16_to_float(grid).astype(np.float64)
-    b = bf16_to_float(clus).astype(np.float64)
-    rel = np.linalg.norm(a - b) / max(np.linalg.norm(a), 1e-300)
-    print(f"[{name}] cluster vs grid: rel L2 {rel:.3e}")
-    assert rel <= 2e-3
+    base = bf16_to_float(rows["grid"]).astype(np.float64)
+    for label in ("small", "cluster"):
+        other = bf16_to_float(rows[label]).astype(np.float64)
+        rel = np.linalg.norm(other - base) / max(np.linalg.norm(base), 1e-300)
+        print(f"[{name}] {label} vs grid: rel L2 {rel:.3e}")
+        assert rel <= 2e-3
 
 
-@pytest.mark.parametrize("allow_cluster", [1, 0])
-def test_floor_rule_pair_golden_on_the_gpu(moe, allow_cluster):
+@pytest.mark.parametrize("path", [1, 2, 0], ids=["small", "cluster", "grid"])
+def test_floor_rule_pair_golden_on_the_gpu(moe, path):
     """The hand-worked pair of golden/floor_rule_pair.json (I = 384: the floor
     rule saturates its hidden block) through the kernels: its hidden codes,
     scales and output bits are the golden's, on both paths, and every other
@@ -589,7 +604,7 @@ def test_floor_rule_pair_golden_on_the_gpu(moe, allow_cluster):
     dev = torch.device("cuda:0")
     layer = moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights))
     try:
-        moe.moe_debug_paths(layer.handle, allow_cluster)
+        set_path(moe, layer, path, 1)
         got, status = run_layer(moe, layer, x, ids)
         assert status == moe.MOE_OK
         H, I = spec["hidden"], spec["inter"]
@@ -613,7 +628,8 @@ def test_floor_rule_pair_golden_on_the_gpu(moe, allow_cluster):
         layer.close()
 
 
-def test_cluster_path_at_two_tokens_with_shared_experts(moe):
+@pytest.mark.parametrize("path", SMALL_PATHS, ids=["small", "cluster"])
+def test_small_batch_paths_at_two_tokens_with_shared_experts(moe, path):
     """Two tokens routed to the same experts: every unit holds two rows, so
     each split-K piece carries two rows of partial sums."""
     weights, x, _ = cached_inputs("tp8_b1")
@@ -622,8 +638,11 @@ def test_cluster_path_at_two_tokens_with_shared_experts(moe):
     row = rng.permutation(weights[0].shape[0])[:16].astype(np.int32)
     ids = np.stack([row, row[::-1]]).astype(np.int32)
     layer = layer_for(moe, weights)
-    assert moe.moe_cluster_size(layer.handle, 2) >= 2
-    got, status = run_layer(moe, layer, x2, ids)
+    try:
+        set_path(moe, layer, path, 2)
+        got, status = run_layer(moe, layer, x2, ids)
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
     assert status == moe.MOE_OK
     experts, rows = units_of(moe, layer, 2)
     assert len(experts) == 16 and np.all(rows[:, 1] >= 0)
