@@ -52,14 +52,6 @@ struct SmallPieces {
   int entry[kSmallUnitPieces];
 };
 
-// The CTA whose FC1 range holds stage s: the largest c with
-// floor(c * T1 / G) <= s, i.e. c * T1 < (s + 1) * G.
-__device__ __forceinline__ int owner_of(const Split& sp, int s) {
-  const int c = static_cast<int>((static_cast<uint32_t>(s + 1) * static_cast<uint32_t>(sp.G) - 1u) /
-                                 static_cast<uint32_t>(sp.T1));
-  return c < sp.G - 1 ? c : sp.G - 1;
-}
-
 // Warp 0: the canonical unit table of <= 32 pairs. Pair p = lane; a pair is
 // kept when its id is in [0, E) and no lower slot of its token has the same
 // id. Unit u is the u-th kept expert in ascending order; its rows are its
@@ -115,6 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   uint8_t* HSF = sm + L.hsf;
   SmallUnits* su = reinterpret_cast<SmallUnits*>(sm + L.table);
   SmallPieces* pl = reinterpret_cast<SmallPieces*>(su + 1);  // [kSmallHidden]
+  // FC1 range start and first item of CTAs 0..G (the output-staging region,
+  // which this kernel does not use).
+  uint32_t* span_tbl = reinterpret_cast<uint32_t*>(sm + L.out);  // [kMaxGrid + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + S;
   uint64_t* accfull = empty + S;
@@ -407,32 +402,51 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     // The item counters are cleared by the prep grid: no poll before it ends.
     grid_dependency_wait();
 
-    // The FC1 pieces behind each FC2 unit of this CTA (at most two units).
-    if (et == 0) {
-      int ordinal = 0;
-      for (int j = j0; j < j1 && ordinal < kSmallHidden; ++ordinal) {
-        const int u = j / g.NQ;
-        j = (u + 1) * g.NQ;
+    // The FC1 range starts (16 bits) and first items (16 bits) of CTAs 0..G,
+    // filled by all epilogue threads at once, so that the piece lists below
+    // need no division (a single thread running them with divisions took
+    // microseconds).
+    for (int c = et; c <= G; c += 128) {
+      const int b = sp.fc1_begin(c);
+      span_tbl[c] = static_cast<uint32_t>(b) | (static_cast<uint32_t>(b / g.KC1) << 16);
+    }
+    epilogue_sync();
+    // The FC1 pieces behind each FC2 unit of this CTA (at most two units):
+    // for every item, the CTAs holding its stages (a binary search over the
+    // range starts), in CTA order, skipping CTAs with empty ranges. Epilogue
+    // warp w builds the list of unit w.
+    if (q == 0 || q == 1) {
+      const int ordinal = q, want_unit = j0 / g.NQ + q;
+      const bool has = ordinal == 0 ? j1 > j0 : (j1 > j0 && (j1 - 1) / g.NQ >= want_unit);
+      if (has && lane == 0) {
+        const int u = want_unit;
+        auto owner = [&](int st) {  // the largest c with begin(c) <= st
+          int lo = 0, hi = G - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int>(span_tbl[mid] & 0xFFFFu) <= st) lo = mid; else hi = mid - 1;
+          }
+          return lo;
+        };
         SmallPieces& P = pl[ordinal];
         int n = 0;
         for (int p = 0; p < g.P1; ++p) {
           const int item = u * g.P1 + p, s0 = item * g.KC1;
-          const int lo = owner_of(sp, s0), hi = owner_of(sp, s0 + g.KC1 - 1);
+          const int lo = owner(s0), hi = owner(s0 + g.KC1 - 1);
           uint32_t want = 0;
-          int b = sp.fc1_begin(lo);
           for (int c = lo; c <= hi; ++c) {
-            const int b1 = sp.fc1_begin(c + 1);
-            if (b1 > b && n < kSmallUnitPieces) {
-              P.entry[n++] = (p << 16) | (c * kSmallPieces + (item - b / g.KC1));
+            const uint32_t e0 = span_tbl[c], e1 = span_tbl[c + 1];
+            if ((e1 & 0xFFFFu) > (e0 & 0xFFFFu) && n < kSmallUnitPieces) {
+              P.entry[n++] = (p << 16) | (c * kSmallPieces + (item - static_cast<int>(e0 >> 16)));
               ++want;
             }
-            b = b1;
           }
           P.want[p] = want;
         }
         P.n = n;
       }
     }
+    if (et == 0) MOE_STAMP(18);
     epilogue_sync();
 
     // The hidden image of each FC2 unit, built once this CTA's FC1 pieces are
