@@ -36,11 +36,11 @@ struct ExpertsArgs {
   const uint8_t* stages;      // [E * SPE] blocks of kStageBytes
   const int32_t* ids;         // [B, 16] routing ids of the call, or null: lets the cluster
                               // variant's producer find its unit without the prep grid
-  const uint8_t* plan_codes;  // [B, H]
-  const uint8_t* plan_scales; // [B, H / 32]
-  const int32_t* unit_count;
-  const int32_t* unit_expert;
-  const int16_t* unit_rows;
+  uint8_t* plan_codes;        // [B, H] (the small-batch kernel writes it, the others read it)
+  uint8_t* plan_scales;       // [B, H / 32]
+  int32_t* unit_count;
+  int32_t* unit_expert;
+  int16_t* unit_rows;
   uint32_t* item_counters;
   uint32_t* hidden_flags;
   float* partials;            // [grid, 2 halves, 2 tiles, 8 tokens, 128 rows]
@@ -54,6 +54,10 @@ struct ExpertsArgs {
   int withhold_image;         // test hook (grid kernel): never deliver this unit's hidden
                               // image to shared memory (-1 = off)
   uint64_t* span;             // or null: launch clock, [CTA][start, end] (moe_debug_kernel_span)
+  // Small-batch kernel only (the call is that one launch):
+  const uint16_t* x;          // BF16 [B, H]: quantized to MXFP8 in the kernel
+  uint32_t* cflags;           // [kMaxGrid][2][4] per-consumer piece counts, zero between calls
+  uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
 };
 
@@ -84,6 +88,7 @@ int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serve
 bool small_fits(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
+constexpr size_t kSmallFlagBytes = static_cast<size_t>(kMaxGrid) * 2 * 4 * 4;  // ExpertsArgs::cflags
 
 // Routing-weighted combine of each token's 16 rows (after the experts kernel).
 struct CombineArgs {

@@ -42,6 +42,7 @@ struct moe_ctx {
   int path = moe::kPathSmall;  // which experts kernel one- and two-token calls run on
   int small_ok[3] = {0, 0, 0};  // [batch]: the small-batch kernel's split fits this layer
   uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
+  uint32_t* cflags = nullptr;  // small-batch kernel: per-consumer piece counts (zero at rest)
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
@@ -208,9 +209,10 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
       static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8,           // launch clock
+      moe::kSmallFlagBytes,                                     // small-batch piece counts
   };
-  size_t offsets[13], total = 0;
-  for (int i = 0; i < 13; ++i) {
+  size_t offsets[14], total = 0;
+  for (int i = 0; i < 14; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -231,6 +233,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->pair_kept = w + offsets[10];
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
   h->span = reinterpret_cast<uint64_t*>(w + offsets[12]);
+  h->cflags = reinterpret_cast<uint32_t*>(w + offsets[13]);
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
   return encode_weight_map(h);
@@ -282,9 +285,17 @@ int check_device(const moe_ctx* h) {
     if (moe_rc_ != MOE_OK) return moe_rc_;      \
   } while (0)
 
+// Whether a call of `batch` tokens with its routing ids runs on the
+// small-batch kernel alone (no prep grid).
+bool small_call(const moe_ctx* h, int batch) {
+  return batch <= 2 && h->path == moe::kPathSmall && h->small_ok[batch];
+}
+
 // ids: the call's routing ids when the same call's prep grid runs just
-// before on this stream, else null.
-int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream) {
+// before on this stream (or, x given, when the call is the small-batch kernel
+// alone), else null.
+int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream,
+                   const void* x = nullptr) {
   moe::ExpertsArgs a{};
   a.wmap = h->wmap;
   a.stages = h->stages;
@@ -307,7 +318,36 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.withhold_image = h->withhold_image;
   a.span = h->span_on ? h->span : nullptr;
   a.trace = h->trace;
+  a.x = static_cast<const uint16_t*>(x);
+  a.cflags = h->cflags;
+  a.pair_kept = h->pair_kept;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
+  return MOE_OK;
+}
+
+// moe_run; fused = false keeps the prep grid in front of the small-batch
+// kernel (for inputs in host memory, which the prep grid reads once).
+int run_call(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
+             void* stream, bool fused) {
+  if (h == nullptr || !x_bf16 || !topk_ids || !out_bf16) return MOE_ERR_ARG;
+  if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(out_bf16) || check_batch(batch))
+    return MOE_ERR_ARG;
+  MOE_CHECK_DEVICE(h);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc;
+  if (fused && small_call(h, batch)) {
+    // One launch: the small-batch kernel quantizes x and groups the ids itself.
+    rc = launch_experts(h, out_bf16, batch, topk_ids, s, x_bf16);
+  } else {
+    MOE_CUDA(moe::launch_prep(
+        prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
+    rc = launch_experts(h, out_bf16, batch, topk_ids, s);
+  }
+  if (rc != MOE_OK) return rc;
+  h->plan_batch = batch;
+  h->group_batch = batch;
+  h->grouped = 1;
+  h->ran = 1;
   return MOE_OK;
 }
 
@@ -323,7 +363,7 @@ int capture_host_run(moe_ctx* h, const void* x_host, const int32_t* ids_host, vo
     MOE_CUDA(cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking));
   MOE_CUDA(cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal));
   h->status_dev = h->status_host;
-  const int rc = moe_run(h, x_host, ids_host, out_host, batch, h->capture_stream);
+  const int rc = run_call(h, x_host, ids_host, out_host, batch, h->capture_stream, false);
   h->status_dev = h->status;
   cudaGraph_t graph = nullptr;
   const cudaError_t ce = cudaStreamEndCapture(h->capture_stream, &graph);
@@ -391,20 +431,7 @@ int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream) {
 
 int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
             void* stream) {
-  if (h == nullptr || !x_bf16 || !topk_ids || !out_bf16) return MOE_ERR_ARG;
-  if (!aligned16(x_bf16) || !aligned16(topk_ids) || !aligned16(out_bf16) || check_batch(batch))
-    return MOE_ERR_ARG;
-  MOE_CHECK_DEVICE(h);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(moe::launch_prep(
-      prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
-  const int rc = launch_experts(h, out_bf16, batch, topk_ids, s);
-  if (rc != MOE_OK) return rc;
-  h->plan_batch = batch;
-  h->group_batch = batch;
-  h->grouped = 1;
-  h->ran = 1;
-  return MOE_OK;
+  return run_call(h, x_bf16, topk_ids, out_bf16, batch, stream, true);
 }
 
 int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
@@ -414,7 +441,7 @@ int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
       !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
   MOE_CHECK_DEVICE(h);
-  const int rc = moe_run(h, x_bf16, topk_ids, h->staged, batch, stream);
+  const int rc = run_call(h, x_bf16, topk_ids, h->staged, batch, stream, true);
   if (rc != MOE_OK) return rc;
   moe::CombineArgs c{};
   c.rows = h->staged;
@@ -444,7 +471,14 @@ int moe_sync_status(moe_handle h, void* stream) {
   MOE_CUDA(cudaMemcpyAsync(h->status_host, h->status, 4, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemsetAsync(h->status, 0, 4, s));
   MOE_CUDA(cudaStreamSynchronize(s));
-  return *h->status_host;
+  const int status = *h->status_host;
+  if (status == MOE_ERR_DEVICE_TIMEOUT) {
+    // A bounded wait ran out, so some piece counts of the small-batch kernel
+    // may not have been consumed (and set back to zero): clear them.
+    MOE_CUDA(cudaMemsetAsync(h->cflags, 0, moe::kSmallFlagBytes, s));
+    MOE_CUDA(cudaStreamSynchronize(s));
+  }
+  return status;
 }
 
 bool is_pinned_host(const void* p) {
@@ -739,9 +773,10 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
       static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
       static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
       static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
+      moe::kSmallFlagBytes,                                        // small-batch piece counts
   };
-  size_t offsets[9], total = 0;
-  for (int i = 0; i < 9; ++i) {
+  size_t offsets[10], total = 0;
+  for (int i = 0; i < 10; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -758,8 +793,10 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   if (rc != MOE_OK) return rc;
 
   // The grouping block of the prep kernel clears the counters and flags the
-  // experts kernel needs at zero; every other scratch byte is written before
-  // it is read within the call, so nothing is left over from the last call.
+  // grid kernel needs at zero; the small-batch kernel's piece counts are
+  // cleared below. Every other scratch byte is written before it is read
+  // within the call, so nothing is left over from the last call.
+  const bool small = small_call(h, batch);
   moe::PrepArgs pa = prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup);
   pa.unit_cap = cap;
   pa.plan_codes = w + offsets[0];
@@ -771,7 +808,11 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
   pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(moe::launch_prep(pa, s));
+  uint32_t* cflags = reinterpret_cast<uint32_t*>(w + offsets[9]);
+  if (small)
+    MOE_CUDA(cudaMemsetAsync(cflags, 0, moe::kSmallFlagBytes, s));  // a memset, not an allocation
+  else
+    MOE_CUDA(moe::launch_prep(pa, s));
 
   moe::ExpertsArgs ea{};
   ea.wmap = h->wmap;
@@ -793,7 +834,12 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.timeout_ns = h->timeout_ns;
   ea.withhold_unit = -1;
   ea.withhold_image = -1;
-  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->path, batch <= 2 && h->small_ok[batch]));
+  if (small) {
+    ea.x = static_cast<const uint16_t*>(x_bf16);
+    ea.cflags = cflags;
+    ea.pair_kept = nullptr;
+  }
+  MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->path, small));
   return MOE_OK;
 }
 

@@ -8,21 +8,30 @@
 // The persistent grid kernel's roles, ring, MMAs and work split (FC1 stages
 // and FC2 jobs each cut evenly over one CTA per SM), with two changes that
 // suit a call of at most 32 (token, slot) pairs:
-//   - Every CTA derives the unit table from the routing ids itself (warp 0:
-//     one pair per lane; a unit per distinct kept expert, experts ascending,
-//     rows in token order: the canonical table). The producer therefore
-//     streams weights from the kernel's first microsecond, without waiting
-//     for the prep grid, which the gather warp alone waits for (the plan).
+//   - A call on device buffers is this one launch: no prep grid runs before
+//     it (calls on host buffers keep the prep grid, which reads x once, and
+//     gather its plan). Every CTA
+//     derives the unit table from the routing ids itself (warp 0: one pair
+//     per lane; a unit per distinct kept expert, experts ascending, rows in
+//     token order: the canonical table), so the producer streams weights
+//     from the kernel's first microsecond, and the activation warp quantizes
+//     the x chunks it needs to MXFP8 itself. For read-back, CTA 0 writes the
+//     unit table and the kept-pair flags and CTA c the plan of K chunk c.
+//   - Consecutive launches overlap (programmatic dependent launch): each
+//     launch lets the next one start as its CTAs leave, and every role waits
+//     for the previous launch to end before it writes global memory that the
+//     previous launch reads or writes.
 //   - The FC1 -> FC2 hand-off takes one trip through L2 instead of two. Every
 //     piece of an FC1 item (a run of its K stages on one CTA) stores its FP32
-//     partial sums and release-increments the item's counter; there is no
-//     owner. Every CTA that runs FC2 jobs of a unit polls the counters of the
-//     unit's items, sums the pieces itself in CTA order (so every consumer
-//     gets the same bits), applies SiLU(gate) * up and the MXFP8 requant, and
-//     writes the hidden image straight into its own shared memory.
+//     partial sums and release-increments one count per consumer of its
+//     unit; there is no owner. Every CTA that runs FC2 jobs of a unit polls
+//     its own counts of the unit's items (and sets them back to zero), sums
+//     the pieces itself in CTA order (so every consumer gets the same bits),
+//     applies SiLU(gate) * up and the MXFP8 requant, and writes the hidden
+//     image straight into its own shared memory.
 // The warp roles: warp 0 TMA producer, warps 1-4 MMA issuers, warp 5 the
-// activation gather (FC1), warps 6-9 the epilogue (FC1 partial sums; the
-// hidden images of this CTA's FC2 units; BF16 output rows).
+// activations (FC1), warps 6-9 the epilogue (FC1 partial sums; the hidden
+// images of this CTA's FC2 units; BF16 output rows).
 #include "pipeline.cuh"
 
 namespace moe {
@@ -41,6 +50,7 @@ struct SmallUnits {
   int row[kSmallMaxUnits][2];   // pair t * 16 + s, -1 padding
   int valid[kSmallMaxUnits];
   unsigned bits[MOE_MAX_EXPERTS / 32];  // kept experts
+  unsigned kept;                        // bit p: pair p got a unit row
 };
 
 // The FC1 pieces of one FC2 unit of this CTA, in item order and CTA order
@@ -64,6 +74,7 @@ __device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, int lane, int
   const bool valid = lane < pairs && e >= 0 && e < a.g.E;
   const unsigned in_token = __match_any_sync(0xFFFFFFFFu, valid ? 2 * e + (lane >> 4) : -1 - lane);
   const bool kept = valid && __ffs(in_token) - 1 == lane;
+  const unsigned kept_mask = __ballot_sync(0xFFFFFFFFu, kept);
   __syncwarp();
   if (kept) atomicOr(&su->bits[e >> 5], 1u << (e & 31));
   __syncwarp();
@@ -90,7 +101,40 @@ __device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, int lane, int
   }
   __syncwarp();
   if (lane < units) su->valid[lane] = (su->row[lane][0] >= 0) + (su->row[lane][1] >= 0);
-  if (lane == 0) su->count = units;
+  if (lane == 0) {
+    su->count = units;
+    su->kept = kept_mask;
+  }
+}
+
+// The activation image of one FC1 stage: lane l quantizes values 4l..4l+3 of
+// the 128-value K chunk of each valid row (MXFP8: the 8 lanes of a 32-block
+// combine their maxima, ceil-rule E8M0 scale, e4m3 codes) and stores them in
+// the 128B-swizzled image and the scale atom of the stage's slot.
+__device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], const int (&tok)[2], uint8_t* img,
+                                              uint8_t* atom, int lane) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (tok[r] < 0) continue;  // the same for every lane
+    const uint32_t w[2] = {xv[r].x, xv[r].y};
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    const int E = mx_exponent(amax, false);
+    const float inv = pow2f(-E);
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) codes |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
+    *reinterpret_cast<uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4) = codes;
+    if ((lane & 7) == 0) atom[scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ ExpertsArgs a) {
@@ -130,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   if (tid == 0) {
     span_enter(a.span);
     MOE_STAMP(0);
+    // The next launch may start as this one's CTAs leave their SMs.
+    grid_launch_dependents();
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
       mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
@@ -257,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         }
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
         if (lead && n == 0) MOE_STAMP(4);
-        fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
+        fence_proxy_async_shared();  // the activation image was written by generic stores
         tc_fence_after_sync();
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
         tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
@@ -342,10 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       tc_commit(&drained[issuer]);
       wait_own(cx, &drained[issuer], 0);
     }
-  } else if (warp == kGatherWarp) {
-    // ------------------------------------------------ activation gather (FC1)
-    grid_dependency_wait();  // the prep grid's activation plan
-    if (lane == 0) MOE_STAMP(3);
+  } else if (warp == kGatherWarp && a.x == nullptr) {
+    // ------------------------------- activations (FC1), from the prep grid's plan
+    // The call's prep grid ran just before (inputs in host memory: it reads
+    // x once); each stage's 8 activation rows are gathered from its plan.
+    grid_dependency_wait();
     int n = 0, slot = 0, cu = -1;
     uint32_t phase = 0;
     int tok_code = -1, tok_scale = -1;
@@ -386,6 +433,53 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kGatherWarp) {
+    // -------------------------------------------- activations (FC1): x -> MXFP8
+    // The call is this launch alone: the x chunks of kAhead stages are loaded
+    // ahead (one 8-byte load per lane and row), so each stage's image is
+    // written as soon as its slot is free. x is an input of the call: no wait
+    // for the previous launch.
+    constexpr int kAhead = 4;
+    const int count = f1 - f0;
+    uint2 xv[kAhead][2];
+    int tok[kAhead][2];
+    auto fetch = [&](int i, int n) {  // ring entry i <- stage f0 + n
+      tok[i][0] = tok[i][1] = -1;
+      if (n >= count) return;
+      const int s = f0 + n, item = s / g.KC1, c = s - item * g.KC1, u = item / g.P1;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int pr = su->row[u][r];
+        tok[i][r] = pr >= 0 ? (pr >> 4) : -1;
+        if (pr >= 0)
+          xv[i][r] = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(pr >> 4) * g.H +
+                                                           c * kChunkK) + lane);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) fetch(i, i);
+    int slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int n0 = 0; n0 < count && ok; n0 += kAhead) {
+#pragma unroll
+      for (int i = 0; i < kAhead; ++i) {
+        const int n = n0 + i;
+        if (n >= count) break;
+        if (n >= S) {
+          bool freed = true;
+          if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
+          if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
+        }
+        quantize_rows(xv[i], tok[i], ACT + slot * kActImageBytes, BSF + slot * kScaleAtomBytes, lane);
+        mbar_arrive(&full[slot]);  // each lane's own stores, released to the MMA issuers
+        fetch(i, n + kAhead);
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+    }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
@@ -399,8 +493,37 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     const int first_item = f0 / g.KC1;
     const int pieces = f1 > f0 ? (f1 - 1) / g.KC1 - first_item + 1 : 0;
     int done = 0;
-    // The item counters are cleared by the prep grid: no poll before it ends.
+    // The previous launch may still read or write the buffers below (its
+    // partial sums and counts, the plan and unit table, the output): wait for
+    // it to end before the first global write.
     grid_dependency_wait();
+    // Read-back of the call's inputs as the prep grid would have left them,
+    // when no prep grid ran: CTA 0 writes the unit table and the kept-pair
+    // flags (and reports dropped pairs), CTA c the MXFP8 plan of K chunk c of
+    // every token.
+    if (cta == 0 && a.x != nullptr) {
+      if (et == 0) *a.unit_count = units;
+      for (int i = et; i < units * kUnitRows; i += 128) {
+        const int uu = i / kUnitRows, r = i % kUnitRows;
+        a.unit_rows[i] = static_cast<int16_t>(r < 2 ? su->row[uu][r] : -1);
+      }
+      for (int uu = et; uu < units; uu += 128) a.unit_expert[uu] = su->expert[uu];
+      const int pairs = B * kTopK;
+      if (a.pair_kept != nullptr)
+        for (int pp = et; pp < pairs; pp += 128) a.pair_kept[pp] = (su->kept >> pp) & 1u;
+      const unsigned all = pairs == 32 ? 0xFFFFFFFFu : (1u << pairs) - 1u;
+      if (et == 0 && su->kept != all) report(a.status, MOE_ERR_DEVICE_IDS);
+    }
+    for (int cc = cta; a.x != nullptr && cc < g.KC1; cc += G) {
+      for (int t = 0; t < B; ++t) {
+        const float v = __uint_as_float(static_cast<uint32_t>(a.x[static_cast<size_t>(t) * g.H + cc * kChunkK + et]) << 16);
+        const int E = mx_exponent(warp_amax(v), false);
+        a.plan_codes[static_cast<size_t>(t) * g.H + cc * kChunkK + et] = e4m3_code(v * pow2f(-E));
+        if (lane == 0)
+          a.plan_scales[static_cast<size_t>(t) * (g.H / kBlock) + cc * (kChunkK / kBlock) + (et >> 5)] =
+              static_cast<uint8_t>(E + 127);
+      }
+    }
 
     // The FC1 range starts (16 bits) and first items (16 bits) of CTAs 0..G,
     // filled by all epilogue threads at once, so that the piece lists below
@@ -471,7 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
           uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
           if (et < g.P1) {
-            const uint32_t* counter = a.item_counters + u * g.P1 + et;
+            // This CTA's own count of the item's pieces; set back to zero
+            // for the next call (whose pieces count only after this launch
+            // has ended).
+            uint32_t* counter = a.cflags + (cta * kSmallHidden + ordinal) * 4 + et;
             const uint32_t want = P.want[et];
             const uint64_t t_wait = global_timer_ns();
             for (uint32_t i = 0; load_acquire_gpu(counter) < want; ++i) {
@@ -481,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                 break;
               }
             }
+            *reinterpret_cast<volatile uint32_t*>(counter) = 0u;
           }
           epilogue_sync();
           if (et == 0) MOE_STAMP(7);
@@ -615,7 +742,23 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           dst[(B + t) * kTileM + m] = v1[t];
         }
         epilogue_sync();
-        if (et == 0 && u != a.withhold_unit) red_release_add_gpu(&a.item_counters[item], 1u);
+        // One count per CTA that runs FC2 jobs of the unit (the CTAs holding
+        // jobs u * NQ .. u * NQ + NQ - 1), each released by its own thread.
+        if (u != a.withhold_unit) {
+          const uint32_t J = static_cast<uint32_t>(sp.J), GG = static_cast<uint32_t>(G);
+          auto job_owner = [&](int j) {  // the largest c with floor(c * J / G) <= j
+            const int c = static_cast<int>((static_cast<uint32_t>(j + 1) * GG - 1u) / J);
+            return c < G - 1 ? c : G - 1;
+          };
+          const int k = job_owner(u * g.NQ) + et;
+          if (k <= job_owner(u * g.NQ + g.NQ - 1)) {
+            const int kb = sp.fc2_begin(k), ke = sp.fc2_begin(k + 1);
+            if (ke > kb) {
+              const int ordinal = kb / g.NQ == u ? 0 : 1;
+              red_release_add_gpu(a.cflags + (k * kSmallHidden + ordinal) * 4 + (item - u * g.P1), 1u);
+            }
+          }
+        }
         ++done;
       } else {
         // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.

@@ -706,3 +706,45 @@ def test_kernel_span_records_the_last_launch(moe, name):
     run_layer(moe, layer, x, ids)
     with pytest.raises(moe.MoeError):
         moe.moe_read_kernel_span(layer.handle)
+
+
+@pytest.mark.parametrize("name", ["tiny", "tp8_b1"])
+def test_single_launch_call_leaves_plan_and_units_for_read_back(moe, name):
+    """A one- or two-token moe_run is the small-batch kernel alone (no prep
+    grid): the activation plan and the unit table it leaves for read-back
+    are the oracle's, bit for bit, and two runs give the same bits."""
+    weights, x, ids = cached_inputs(name)
+    layer = layer_for(moe, weights)
+    B, H = x.shape
+    assert moe.moe_kernel_path(layer.handle, B) == moe.PATH_SMALL
+    first, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    codes = np.zeros((B, H), np.uint8)
+    scales = np.zeros((B, H // 32), np.uint8)
+    moe.moe_copy_plan(layer.handle, codes, scales, B)
+    ref_codes, ref_scales = oracle.quantize_x(x)
+    np.testing.assert_array_equal(scales, ref_scales)
+    np.testing.assert_array_equal(codes, ref_codes)
+    experts, rows = units_of(moe, layer, B)
+    ref_e, ref_r = oracle.group(ids, weights[0].shape[0])
+    np.testing.assert_array_equal(experts, ref_e)
+    np.testing.assert_array_equal(rows, ref_r)
+    again, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    np.testing.assert_array_equal(again, first)
+
+
+def test_single_launch_call_after_bad_ids_is_exact(moe):
+    """A call with a repeated and an out-of-range id reports them; the next
+    call, on the same handle, is exact (its piece counts start from zero)."""
+    weights, x, ids = cached_inputs("tp8_b1")
+    layer = layer_for(moe, weights)
+    bad = ids.copy()
+    bad[0, 3] = bad[0, 1]
+    bad[0, 7] = -1
+    _, status = run_layer(moe, layer, x, bad)
+    assert status == moe.MOE_ERR_DEVICE_IDS
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tp8 B1 after bad ids")
