@@ -45,7 +45,7 @@ extern "C" {
 #define MOE_MAX_EXPERTS 1024
 #define MOE_MAX_HIDDEN 16384
 #define MOE_MAX_INTER 512
-#define MOE_NOALLOC_SCRATCH_BYTES (4 << 20) /* static scratch of moe_run_noalloc */
+#define MOE_NOALLOC_SCRATCH_BYTES (8 << 20) /* static scratch of moe_run_noalloc */
 
 enum moe_status {
   MOE_OK = 0,

@@ -28,7 +28,7 @@ __all__ = [
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_IDS, MOE_ERR_STATE = 4, 5, 6
-MOE_NOALLOC_SCRATCH_BYTES = 4 << 20  # static scratch of moe_run_noalloc
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20  # static scratch of moe_run_noalloc
 TOPK, UNIT_ROWS, MAX_BATCH = 16, 8, 256
 
 

@@ -48,8 +48,33 @@ constexpr int kMaxInterChunks = MOE_MAX_INTER / kChunkK;  // 4
 constexpr int kMaxGrid = 256;             // partition table capacity (CTAs)
 constexpr int kMaxSpanCtas = 512;         // launch-clock slots: CTAs of any experts launch
 
-// Byte offset of the 16-byte chunk `c16` (0..7) of row `r` (0..7) in a
-// 1024-byte, 128-byte-swizzled 8-row image.
+// The grid kernel's units: the table's 8-row units for calls of at most 8
+// tokens, else pairs of them. An N = 16 MMA costs its issuing thread as much
+// as an N = 8 one, so a 16-row unit streams an expert's weights once for up
+// to 16 of its tokens. A pair-table entry: bits 0-19 the first unit, 20-29
+// the expert, bit 31 set when the next unit is the same expert's (rows 8-15).
+constexpr uint32_t kWideFirstMask = 0xFFFFFu;
+__host__ __device__ constexpr uint32_t wide_entry(int first, int expert, bool paired) {
+  return static_cast<uint32_t>(first) | (static_cast<uint32_t>(expert) << 20) | (paired ? 1u << 31 : 0u);
+}
+static_assert(MOE_MAX_EXPERTS <= 1024, "the pair-table entry holds a 10-bit expert");
+
+// Per-unit-size constants of the grid kernel: 16-row units take a 5-slot ring
+// (the images and staging double; a 5-slot ring streams as fast at 152 CTAs)
+// and 3 accumulator sets of 4 x 16 TMEM columns.
+template <int R>
+struct Rows {
+  static constexpr int kSlots = R == 8 ? kRingStages : 5;
+  static constexpr int kSets = R == 8 ? kAccSets : 3;
+  static constexpr int kImage = R * kChunkK;            // activation / hidden image of a K chunk
+  static constexpr int kSetColumns = kMmaWarps * R;     // one N = R accumulator per issuer
+  static constexpr int kScaleBase = kSets * kSetColumns;
+  static constexpr int kHiddenScaleBase = kScaleBase + kSlots * kSlotScaleColumns;
+  static_assert(kHiddenScaleBase + kMmaWarps * kHiddenScaleColumns <= kTmemColumns, "TMEM columns");
+};
+
+// Byte offset of the 16-byte chunk `c16` (0..7) of row `r` in a 128-byte-
+// swizzled image of 8-row, 1024-byte atoms (rows 8-15 are the second atom).
 __host__ __device__ constexpr uint32_t swizzle128(uint32_t r, uint32_t c16) {
   return r * 128u + ((c16 ^ (r & 7u)) << 4);
 }

@@ -42,12 +42,56 @@ namespace {
 
 using namespace ptx;
 
+// Unit u of a launch with R-row units: the table's unit u (R = 8), or the
+// pair-table entry u (R = 16; see kWideFirstMask).
+template <int R>
+__device__ __forceinline__ int unit_first_of(const ExpertsArgs& a, int u) {
+  if constexpr (R == 8) return u;
+  else return static_cast<int>(a.wide_units[u] & kWideFirstMask);
+}
+
+template <int R>
+__device__ __forceinline__ int unit_expert_of(const ExpertsArgs& a, int u) {
+  if constexpr (R == 8) return a.unit_expert[u];
+  else return static_cast<int>((a.wide_units[u] >> 20) & 0x3FFu);
+}
+
+// Rows of table unit tu: its pairs, then -1 padding (one 16-byte load).
+__device__ __forceinline__ int table_unit_valid(const ExpertsArgs& a, int tu) {
+  const int4 r4 = __ldcg(reinterpret_cast<const int4*>(a.unit_rows) + tu);
+  const uint32_t w4[4] = {static_cast<uint32_t>(r4.x), static_cast<uint32_t>(r4.y),
+                          static_cast<uint32_t>(r4.z), static_cast<uint32_t>(r4.w)};
+  int v = 0;
+#pragma unroll
+  for (int r = 0; r < kUnitRows; ++r) v += static_cast<int16_t>(w4[r >> 1] >> (16 * (r & 1))) >= 0;
+  return v;
+}
+
+// Row r of unit u: a pair index (token * 16 + slot) or -1 (padding). A
+// pair's rows 8-15 are the second table unit's, which follows the first.
+template <int R>
+__device__ __forceinline__ int unit_row_of(const ExpertsArgs& a, int u, int r) {
+  if constexpr (R == 8) {
+    return a.unit_rows[u * kUnitRows + r];
+  } else {
+    const uint32_t w = a.wide_units[u];
+    const int first = static_cast<int>(w & kWideFirstMask);
+    return (r < kUnitRows || (w >> 31)) ? a.unit_rows[first * kUnitRows + r] : -1;
+  }
+}
+
+template <int R>
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ ExpertsArgs a) {
+  // R rows per unit: the table's units (R = 8) or pairs of them (R = 16).
+  using RT = Rows<R>;
+  constexpr int S = RT::kSlots;
+  constexpr int NACC = RT::kSets;
+  constexpr int kImage = RT::kImage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const Geometry& g = a.g;
-  const Layout L(g.KC2);
+  const Layout L(g.KC2, R);
   uint8_t* W = sm + L.w;
   uint8_t* ACT = sm + L.act;
   uint8_t* ASF = sm + L.asf;
@@ -104,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
   // The plan, unit table and cleared counters of the preceding prep grid.
   grid_dependency_wait();
-  const int units = *a.unit_count;
+  const int units = a.unit_count[R == 8 ? 0 : 1];
   if (tid == 0) MOE_STAMP(3);
   // Half A = units [0, units_a). Small calls keep one half: their chain of
   // reductions is latency-bound and more pieces per item only lengthen it.
@@ -158,13 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       int cu = -1, e = 0;
       for (int h = 0; h < 2; ++h)
         for (Fc1Cursor cur(f0[h], g); cur.s < f1[h] && ok; cur.next(g)) {
-          if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+          if (cur.u != cu) { e = unit_expert_of<R>(a, cur.u); cu = cur.u; }
           ok = issue(e * g.SPE + cur.p * g.KC1 + cur.c, false);
         }
       cu = -1;
       for (int h = 0; h < 2; ++h)
         for (Fc2Cursor cur(j0[h], g); cur.j < j1[h] && ok; cur.next(g)) {
-          if (cur.u != cu) { e = a.unit_expert[cur.u]; cu = cur.u; }
+          if (cur.u != cu) { e = unit_expert_of<R>(a, cur.u); cu = cur.u; }
           const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
           for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
         }
@@ -179,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (lane == 0) {
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
-      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase + issuer * kHiddenScaleColumns;
+      const uint32_t hsf_cols = tmem + RT::kHiddenScaleBase + issuer * kHiddenScaleColumns;
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_c = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -208,15 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lead && n == 0) MOE_STAMP(4);
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
         tc_fence_after_sync();
-        const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+        const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns + issuer * 8;
         tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
         tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
         const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
-        const uint64_t dx = desc_sw128(ACT + slot * kActImageBytes + k0 * 32);
-        const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+        const uint64_t dx = desc_sw128(ACT + slot * kImage + k0 * 32);
+        const uint32_t d = tmem + set * RT::kSetColumns + issuer * R;
         // Descriptor start addresses count 16-byte units: +2 is the next K-step.
-        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
-        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0, R), sf, sf + 4, first ? 0u : 1u);
+        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1, R), sf, sf + 4, 1u);
         if (lead) MOE_STAMP(5);
         tc_commit(&empty[slot]);
         advance();
@@ -254,17 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           // K-steps of this chunk: 4, or fewer in the last chunk when I % 128 != 0.
           const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
           if (k0 < ksteps) {
-            const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns + issuer * 8;
             const int hc = hb * g.KC2 + c;
             const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
-            const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
-            const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+            const uint64_t dh = desc_sw128(HC + hc * kImage + k0 * 32);
+            const uint32_t d = tmem + set * RT::kSetColumns + issuer * R;
             // Descriptor start addresses count 16-byte units: +2 is the next K-step.
-            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
+            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0, R), sf, sfh, started ? 1u : 0u);
             if (k0 + 1 < ksteps)
-              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sfh, 1u);
+              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1, R), sf, sfh, 1u);
             started = true;
           }
           if (lead) MOE_STAMP(11);
@@ -302,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     for (int hf = 0; hf < 2; ++hf)
     for (Fc1Cursor cur(f0[hf], g); cur.s < f1[hf] && ok; cur.next(g)) {
       if (cur.u != cu) {
-        const int pc = a.unit_rows[cur.u * kUnitRows + (lane >> 2)];
-        const int ps = a.unit_rows[cur.u * kUnitRows + (lane & 7)];
+        // Lane l gathers row l / (32 / R) of the image and the scales of row l.
+        const int pc = unit_row_of<R>(a, cur.u, lane / (32 / R));
+        const int ps = unit_row_of<R>(a, cur.u, lane % R);
         tok_code = pc >= 0 ? (pc >> 4) : -1;
         tok_scale = ps >= 0 ? (ps >> 4) : -1;
         cu = cur.u;
@@ -313,16 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
         if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
       }
-      const int r = lane >> 2, piece = lane & 3;
-      uint8_t* img = ACT + slot * kActImageBytes;
+      constexpr int kLanesPerRow = 32 / R, kChunksPerLane = 8 / kLanesPerRow;
+      const int r = lane / kLanesPerRow, piece = lane % kLanesPerRow;
+      uint8_t* img = ACT + slot * kImage;
       const uint8_t* row = a.plan_codes + static_cast<size_t>(tok_code < 0 ? 0 : tok_code) * g.H +
                            cur.c * kChunkK;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c16 = piece * 2 + h;
+      for (int h = 0; h < kChunksPerLane; ++h) {
+        const int c16 = piece * kChunksPerLane + h;
         cp_async_16(img + swizzle128(r, c16), row + c16 * 16, tok_code < 0 ? 0u : 16u);
       }
-      if (lane < 8) {
+      if (lane < R) {
         const uint8_t* src = a.plan_scales +
                              static_cast<size_t>(tok_scale < 0 ? 0 : tok_scale) * (g.H / kBlock) +
                              cur.c * (kChunkK / kBlock);
@@ -368,22 +414,60 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       if (lane == 0 && ordinal == 0) MOE_STAMP(9);
       // The image (codes of every K chunk, then their scale atoms) in one
       // batch of independent 16-byte loads per lane: a single L2 round trip.
-      const uint4* src = reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes);
-      uint4* codes = reinterpret_cast<uint4*>(HC + b * g.KC2 * kActImageBytes);
-      uint4* scales = reinterpret_cast<uint4*>(HSF + b * g.KC2 * kScaleAtomBytes);
-      const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
-      constexpr int kPerLane = kMaxInterChunks * kHiddenChunkBytes / 16 / 32;
-      uint4 v[kPerLane];
+      if constexpr (R == 8) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(cur.u) * g.hidden_bytes);
+        uint4* codes = reinterpret_cast<uint4*>(HC + b * g.KC2 * kImage);
+        uint4* scales = reinterpret_cast<uint4*>(HSF + b * g.KC2 * kScaleAtomBytes);
+        const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
+        constexpr int kPerLane = kMaxInterChunks * kHiddenChunkBytes / 16 / 32;
+        uint4 v[kPerLane];
 #pragma unroll
-      for (int k = 0; k < kPerLane; ++k) {
-        const int i = lane + 32 * k;
-        if (i < n_all) v[k] = __ldcg(src + i);
-      }
+        for (int k = 0; k < kPerLane; ++k) {
+          const int i = lane + 32 * k;
+          if (i < n_all) v[k] = __ldcg(src + i);
+        }
 #pragma unroll
-      for (int k = 0; k < kPerLane; ++k) {
-        const int i = lane + 32 * k;
-        if (i < n_codes) codes[i] = v[k];
-        else if (i < n_all) scales[i - n_codes] = v[k];
+        for (int k = 0; k < kPerLane; ++k) {
+          const int i = lane + 32 * k;
+          if (i < n_codes) codes[i] = v[k];
+          else if (i < n_all) scales[i - n_codes] = v[k];
+        }
+      } else {
+        // A pair: rows 0-7 from the first unit's image, rows 8-15 (the
+        // second atom of every chunk, bytes 128-255 of every scale atom)
+        // from the second's. Per unit: KC2 x 64 code vectors, then the
+        // KC2 scale atoms' first 128 bytes (8 vectors each).
+        const uint32_t w = a.wide_units[cur.u];
+        const int first = static_cast<int>(w & kWideFirstMask);
+        const int per_unit = g.KC2 * (kActImageBytes / 16 + 8);
+        const int n_all = (w >> 31) ? 2 * per_unit : per_unit;
+        constexpr int kPerLane = 2 * kMaxInterChunks * (kActImageBytes / 16 + 8) / 32;
+        uint4 v[kPerLane];
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int i = lane + 32 * k;
+          if (i < n_all) {
+            const int half = i >= per_unit, j = i - half * per_unit;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.hidden + static_cast<size_t>(first + half) * g.hidden_bytes);
+            const int n_codes = g.KC2 * kActImageBytes / 16;
+            v[k] = __ldcg(src + (j < n_codes ? j : n_codes + ((j - n_codes) >> 3) * (kScaleAtomBytes / 16) +
+                                                      ((j - n_codes) & 7)));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int i = lane + 32 * k;
+          if (i < n_all) {
+            const int half = i >= per_unit, j = i - half * per_unit;
+            const int n_codes = g.KC2 * kActImageBytes / 16;
+            uint4* dst = j < n_codes
+                ? reinterpret_cast<uint4*>(HC + (b * g.KC2 + (j >> 6)) * kImage + half * kActImageBytes) + (j & 63)
+                : reinterpret_cast<uint4*>(HSF + (b * g.KC2 + ((j - n_codes) >> 3)) * kScaleAtomBytes + half * 128) +
+                      ((j - n_codes) & 7);
+            *dst = v[k];
+          }
+        }
       }
       fence_proxy_async_shared();
       __syncwarp();
@@ -399,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // Unit rows of this CTA's first units, fetched while the first stages stream.
     int* cache_unit = reinterpret_cast<int*>(sm + L.rows);
     int* cache_valid = cache_unit + kRowCache;
-    int16_t* cache_rows = reinterpret_cast<int16_t*>(cache_valid + kRowCache);
+    int* cache_first = cache_valid + kRowCache;  // the unit's (first) table unit
+    int16_t* cache_rows = reinterpret_cast<int16_t*>(cache_first + kRowCache);
     {
       const int per_unit_fc1 = g.P1 * g.KC1;
       int lo = units, hi = -1;
@@ -410,15 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       if (et < kRowCache) {
         const int u = lo + et;
         cache_unit[et] = (u <= hi) ? u : -1;
+        cache_first[et] = (u <= hi) ? unit_first_of<R>(a, u) : -1;
       }
-      if (et < kRowCache * kUnitRows) {
-        const int u = lo + et / kUnitRows;
-        cache_rows[et] = (u <= hi) ? a.unit_rows[u * kUnitRows + et % kUnitRows] : -1;
+      for (int i = et; i < kRowCache * R; i += 128) {
+        const int u = lo + i / R;
+        cache_rows[i] = (u <= hi) ? unit_row_of<R>(a, u, i % R) : -1;
       }
       epilogue_sync();
       if (et < kRowCache) {
         int v = 0;
-        while (v < kUnitRows && cache_rows[et * kUnitRows + v] >= 0) ++v;
+        while (v < R && cache_rows[et * R + v] >= 0) ++v;
         cache_valid[et] = v;
       }
       epilogue_sync();
@@ -429,21 +515,25 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     };
     auto unit_row = [&](int u, int r) -> int {
       const int i = cached(u);
-      return i >= 0 ? cache_rows[i * kUnitRows + r] : a.unit_rows[u * kUnitRows + r];
+      return i >= 0 ? cache_rows[i * R + r] : unit_row_of<R>(a, u, r);
+    };
+    auto unit_first = [&](int u) -> int {
+      const int i = cached(u);
+      return i >= 0 ? cache_first[i] : unit_first_of<R>(a, u);
     };
     auto unit_valid = [&](int u) -> int {
       const int i = cached(u);
       if (i >= 0) return cache_valid[i];
-      // Rows of a unit are its pairs, then -1 padding: one 16-byte load.
-      const int4 r4 = __ldcg(reinterpret_cast<const int4*>(a.unit_rows) + u);
-      const uint32_t w4[4] = {static_cast<uint32_t>(r4.x), static_cast<uint32_t>(r4.y),
-                              static_cast<uint32_t>(r4.z), static_cast<uint32_t>(r4.w)};
-      int v = 0;
-#pragma unroll
-      for (int r = 0; r < kUnitRows; ++r) v += static_cast<int16_t>(w4[r >> 1] >> (16 * (r & 1))) >= 0;
-      return v;
+      if constexpr (R == 8) {
+        return table_unit_valid(a, u);
+      } else {
+        // A pair's first unit is full: 8 + the second's rows.
+        const uint32_t w = a.wide_units[u];
+        const int first = static_cast<int>(w & kWideFirstMask);
+        return table_unit_valid(a, (w >> 31) ? first + 1 : first) + ((w >> 31) ? kUnitRows : 0);
+      }
     };
-    int k = 0, out_unit = -1, out_pair = -1, out_valid = 0;
+    int k = 0, out_unit = -1, out_pair = -1, out_pair2 = -1, out_valid = 0;
     for (;;) {
       const int set = k % NACC;
       // The metadata and the abort flag are read together, after the wait.
@@ -456,21 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         md = meta[set];
       }
       if (md.x == 2) break;
-      float v0[8], v1[8], x0[8], x1[8];
+      // The four issuers' accumulators: columns [0, R) tile 0 K-steps 0-1,
+      // [R, 2R) tile 0 K-steps 2-3, [2R, 3R) and [3R, 4R) tile 1.
+      float v0[R], v1[R], x0[R], x1[R];
       {
-        uint32_t r0[8], r1[8], r2[8], r3[8];
-        const uint32_t base = tmem + lanes + set * kAccSetColumns;
-        tmem_load_8_async(base + 0, r0);
-        tmem_load_8_async(base + 8, r1);
-        tmem_load_8_async(base + 16, r2);
-        tmem_load_8_async(base + 24, r3);
+        uint32_t rr[R / 2][8];
+        const uint32_t base = tmem + lanes + set * RT::kSetColumns;
+#pragma unroll
+        for (int j = 0; j < R / 2; ++j) tmem_load_8_async(base + 8 * j, rr[j]);
         tmem_wait_loads();
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          v0[t] = __uint_as_float(r0[t]);
-          x0[t] = __uint_as_float(r1[t]);
-          v1[t] = __uint_as_float(r2[t]);
-          x1[t] = __uint_as_float(r3[t]);
+        for (int t = 0; t < R; ++t) {
+          v0[t] = __uint_as_float(rr[t >> 3][t & 7]);
+          x0[t] = __uint_as_float(rr[(R + t) >> 3][t & 7]);
+          v1[t] = __uint_as_float(rr[(2 * R + t) >> 3][t & 7]);
+          x1[t] = __uint_as_float(rr[(3 * R + t) >> 3][t & 7]);
         }
       }
       tc_fence_before_sync();
@@ -480,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       ++k;
       if (md.x == 0 || fc2_upper_half) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < R; ++t) {
           v0[t] += x0[t];
           v1[t] += x1[t];
         }
@@ -499,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             // Hand the partial sums to the owner and move on: a CTA owns
             // every item whose first stage it holds, so this is its only
             // hand-off in this half.
-            float* dst = a.partials + static_cast<size_t>(cta * 2 + hf) * 2 * kUnitRows * kTileM;
+            float* dst = a.partials + static_cast<size_t>(cta * 2 + hf) * 2 * R * kTileM;
 #pragma unroll
-            for (int t = 0; t < kUnitRows; ++t) {
+            for (int t = 0; t < R; ++t) {
               if (t >= valid) break;
               dst[t * kTileM + m] = v0[t];
-              dst[kUnitRows * kTileM + t * kTileM + m] = v1[t];
+              dst[R * kTileM + t * kTileM + m] = v1[t];
             }
             epilogue_sync();
             if (et == 0) red_release_add_gpu(&a.item_counters[item], 1u);
@@ -532,27 +622,28 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           epilogue_sync();
           if (et == 0) MOE_STAMP(7);
           // Sum the pieces in CTA order, the owner's own piece first; the
-          // loads of up to four pieces are issued together.
-          for (int c0 = cta + 1; c0 < c_end; c0 += 4) {
-            float p0[4][kUnitRows], p1[4][kUnitRows];
-            bool has[4];
+          // loads of up to 32 / R pieces are issued together.
+          constexpr int kBatch = 32 / R;
+          for (int c0 = cta + 1; c0 < c_end; c0 += kBatch) {
+            float p0[kBatch][R], p1[kBatch][R];
+            bool has[kBatch];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
               const int c = c0 + j;
               has[j] = c < c_end && st[c] < st[c + 1];
-              const float* src = a.partials + static_cast<size_t>(c * 2 + hf) * 2 * kUnitRows * kTileM;
+              const float* src = a.partials + static_cast<size_t>(c * 2 + hf) * 2 * R * kTileM;
 #pragma unroll
-              for (int t = 0; t < kUnitRows; ++t) {
+              for (int t = 0; t < R; ++t) {
                 const bool ld = has[j] && t < valid;
                 p0[j][t] = ld ? __ldcg(src + t * kTileM + m) : 0.f;
-                p1[j][t] = ld ? __ldcg(src + kUnitRows * kTileM + t * kTileM + m) : 0.f;
+                p1[j][t] = ld ? __ldcg(src + R * kTileM + t * kTileM + m) : 0.f;
               }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
               if (!has[j]) continue;
 #pragma unroll
-              for (int t = 0; t < kUnitRows; ++t) {
+              for (int t = 0; t < R; ++t) {
                 v0[t] += p0[j][t];
                 v1[t] += p1[j][t];
               }
@@ -561,18 +652,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         }
         // SiLU(gate) * up, MXFP8 per 32 hidden values (= this warp's 32 rows).
         if (p * kTileM + q * 32 < g.I) {
-          uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
+          // Row t goes to the hidden image of table unit first + t / 8 (its
+          // row t % 8), the layout the read-back decodes.
+          const int first = unit_first(u);
           // Rows past `valid` are padding: FC2 reads them but its output
           // columns for them are never stored, so they stay unwritten.
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
+          for (int t = 0; t < R; ++t) {
             if (t >= valid) break;
+            uint8_t* img = a.hidden + static_cast<size_t>(first + (t >> 3)) * g.hidden_bytes;
             const float h = silu_times(v0[t], v1[t]);
             const float amax = warp_amax(h);
             const int E = mx_exponent(amax, g.floor_rule != 0);
-            img[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
+            img[p * kActImageBytes + swizzle128(t & 7, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
             if (lane == 0)
-              img[g.KC2 * kActImageBytes + p * kScaleAtomBytes + scale_atom(t, q)] =
+              img[g.KC2 * kActImageBytes + p * kScaleAtomBytes + scale_atom(t & 7, q)] =
                   static_cast<uint8_t>(E + 127);
           }
         }
@@ -585,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         if (u != out_unit) {
           out_pair = unit_row(u, et >> 4);
+          if (R == 16) out_pair2 = unit_row(u, 8 + (et >> 4));
           out_valid = unit_valid(u);
           out_unit = u;
         }
@@ -602,14 +697,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           continue;
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < R; ++t) {
           OUT[t * 2 * kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
           OUT[t * 2 * kTileM + kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
         }
         epilogue_sync();
-        if (out_pair >= 0) {
-          const int r = et >> 4, ch = et & 15;
-          uint16_t* dst = a.out + static_cast<size_t>(out_pair) * g.H + qq * 2 * kTileM;
+        // 16 threads per row, two 16-byte stores each; rows 8-15 after 0-7.
+#pragma unroll
+        for (int half = 0; half < R / 8; ++half) {
+          const int pair = half == 0 ? out_pair : out_pair2;
+          if (pair < 0) continue;
+          const int r = (et >> 4) + 8 * half, ch = et & 15;
+          uint16_t* dst = a.out + static_cast<size_t>(pair) * g.H + qq * 2 * kTileM;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int chunk = ch + 16 * h;
@@ -1171,9 +1270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int experts_smem_bytes(const Geometry& g) { return Layout(g.KC2).bytes; }
+int experts_smem_bytes(const Geometry& g, int unit_rows) { return Layout(g.KC2, unit_rows).bytes; }
 
-bool experts_layout_aligned(const Geometry& g) { return Layout(g.KC2).aligned(); }
+bool experts_layout_aligned(const Geometry& g) {
+  return Layout(g.KC2, 8).aligned() && Layout(g.KC2, 16).aligned();
+}
 
 namespace {
 int g_resident_clusters[9] = {};  // clusters of this many CTAs resident at once (0: none)
@@ -1184,7 +1285,10 @@ cudaError_t experts_configure(const Geometry& g) {
   // layout any handle can need (I = 512), so every prepared layer launches.
   (void)g;
   const int bytes = Layout(kMaxInterChunks).bytes;
-  cudaError_t e = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(experts_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(experts_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Layout(kMaxInterChunks, 16).bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
@@ -1234,18 +1338,26 @@ int cluster_size_for(const Geometry& g, int batch) {
 }
 
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, experts_kernel, kThreads,
-                                                       experts_smem_bytes(g));
+  int wide = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, experts_kernel<8>, kThreads,
+                                                                experts_smem_bytes(g, 8));
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&wide, experts_kernel<16>, kThreads,
+                                                      experts_smem_bytes(g, 16));
+  if (e == cudaSuccess && wide < *blocks_per_sm) *blocks_per_sm = wide;
+  return e;
 }
 
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
                            int path, bool small_ok) {
   if (path == kPathSmall && small_ok && a.ids != nullptr && a.B <= 2)
     return launch_small(a, grid, stream, pdl);
+  // Calls of more than 8 tokens run 16-row units (pairs of the table's units).
+  const int rows = a.B > kUnitRows ? 16 : 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = experts_smem_bytes(a.g);
+  cfg.dynamicSmemBytes = experts_smem_bytes(a.g, rows);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -1285,7 +1397,8 @@ cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, 
     return cudaLaunchKernelEx(&cfg, cluster_kernel, a, plan);
   }
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, experts_kernel, a);
+  if (rows == 16) return cudaLaunchKernelEx(&cfg, experts_kernel<16>, a);
+  return cudaLaunchKernelEx(&cfg, experts_kernel<8>, a);
 }
 
 }  // namespace moe

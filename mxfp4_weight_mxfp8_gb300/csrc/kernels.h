@@ -18,6 +18,7 @@ struct PrepArgs {
   int32_t* unit_count;      // [1]
   int32_t* unit_expert;     // [unit_cap]
   int16_t* unit_rows;       // [unit_cap, 8]
+  uint32_t* wide_units;     // [unit_cap]: the pairs of units (see kWideFirstMask)
   uint32_t* item_counters;  // [unit_cap * P1], cleared per call
   uint32_t* hidden_flags;   // [unit_cap * KC2], cleared per call
   uint8_t* pair_kept;       // [B * 16] or null: 1 where the pair got a unit row
@@ -38,12 +39,13 @@ struct ExpertsArgs {
                               // variant's producer find its unit without the prep grid
   uint8_t* plan_codes;        // [B, H] (the small-batch kernel writes it, the others read it)
   uint8_t* plan_scales;       // [B, H / 32]
-  int32_t* unit_count;
+  int32_t* unit_count;         // [0] units, [1] pairs of units
   int32_t* unit_expert;
   int16_t* unit_rows;
+  const uint32_t* wide_units;  // [unit_cap]: the 16-row units of calls of more than 8 tokens
   uint32_t* item_counters;
   uint32_t* hidden_flags;
-  float* partials;            // [grid, 2 halves, 2 tiles, 8 tokens, 128 rows]
+  float* partials;            // [grid, 2 halves, 2 tiles, R rows, 128 weight rows]
   uint8_t* hidden;            // [unit_cap, hidden_bytes]
   uint16_t* out;              // BF16 [B * 16, H]
   int32_t* status;
@@ -61,7 +63,7 @@ struct ExpertsArgs {
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
 };
 
-int experts_smem_bytes(const Geometry& g);
+int experts_smem_bytes(const Geometry& g, int unit_rows = 8);
 bool experts_layout_aligned(const Geometry& g);
 cudaError_t experts_configure(const Geometry& g);
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);

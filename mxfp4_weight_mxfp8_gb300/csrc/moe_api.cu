@@ -24,6 +24,7 @@ struct moe_ctx {
   int32_t* unit_count = nullptr;
   int32_t* unit_expert = nullptr;
   int16_t* unit_rows = nullptr;
+  uint32_t* wide_units = nullptr;  // pairs of units: the grid kernel's units above 8 tokens
   uint32_t* item_counters = nullptr;
   uint32_t* hidden_flags = nullptr;
   float* partials = nullptr;
@@ -198,21 +199,22 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   const size_t sizes[] = {
       static_cast<size_t>(MOE_MAX_BATCH) * g.H,                 // plan codes
       static_cast<size_t>(MOE_MAX_BATCH) * (g.H / moe::kBlock), // plan scales
-      4,                                                        // unit count
+      8,                                                        // unit count, pair count
       static_cast<size_t>(h->unit_cap) * 4,                     // unit experts
       static_cast<size_t>(h->unit_cap) * moe::kUnitRows * 2,    // unit rows
       static_cast<size_t>(h->unit_cap) * g.P1 * 4,              // FC1 item counters
       static_cast<size_t>(h->unit_cap) * g.KC2 * 4,             // hidden flags
-      static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
+      static_cast<size_t>(h->grid) * 2 * 2 * 16 * moe::kTileM * 4,  // partials (16-row units)
       static_cast<size_t>(h->unit_cap) * g.hidden_bytes,        // hidden images
       4,                                                        // status
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
       static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8,           // launch clock
       moe::kSmallFlagBytes,                                     // small-batch piece counts
+      static_cast<size_t>(h->unit_cap) * 4,                     // pairs of units
   };
-  size_t offsets[14], total = 0;
-  for (int i = 0; i < 14; ++i) {
+  size_t offsets[15], total = 0;
+  for (int i = 0; i < 15; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -234,6 +236,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
   h->span = reinterpret_cast<uint64_t*>(w + offsets[12]);
   h->cflags = reinterpret_cast<uint32_t*>(w + offsets[13]);
+  h->wide_units = reinterpret_cast<uint32_t*>(w + offsets[14]);
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
   return encode_weight_map(h);
@@ -254,6 +257,7 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
   a.unit_count = h->unit_count;
   a.unit_expert = h->unit_expert;
   a.unit_rows = h->unit_rows;
+  a.wide_units = h->wide_units;
   a.item_counters = h->item_counters;
   a.hidden_flags = h->hidden_flags;
   a.pair_kept = h->pair_kept;
@@ -305,6 +309,7 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.unit_count = h->unit_count;
   a.unit_expert = h->unit_expert;
   a.unit_rows = h->unit_rows;
+  a.wide_units = h->wide_units;
   a.item_counters = h->item_counters;
   a.hidden_flags = h->hidden_flags;
   a.partials = h->partials;
@@ -766,17 +771,18 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   const size_t sizes[] = {
       static_cast<size_t>(batch) * g.H,                            // plan codes
       static_cast<size_t>(batch) * (g.H / moe::kBlock),            // plan scales
-      4,                                                           // unit count
+      8,                                                           // unit count, pair count
       static_cast<size_t>(cap) * 4,                                // unit experts
       static_cast<size_t>(cap) * moe::kUnitRows * 2,               // unit rows
       static_cast<size_t>(cap) * g.P1 * 4,                         // FC1 item counters
       static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
-      static_cast<size_t>(h->grid) * 2 * 2 * moe::kUnitRows * moe::kTileM * 4,  // partials
+      static_cast<size_t>(h->grid) * 2 * 2 * (batch > moe::kUnitRows ? 16 : 8) * moe::kTileM * 4,  // partials
       static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
       moe::kSmallFlagBytes,                                        // small-batch piece counts
+      static_cast<size_t>(cap) * 4,                                // pairs of units
   };
-  size_t offsets[10], total = 0;
-  for (int i = 0; i < 10; ++i) {
+  size_t offsets[11], total = 0;
+  for (int i = 0; i < 11; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -804,6 +810,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.unit_count = reinterpret_cast<int32_t*>(w + offsets[2]);
   pa.unit_expert = reinterpret_cast<int32_t*>(w + offsets[3]);
   pa.unit_rows = reinterpret_cast<int16_t*>(w + offsets[4]);
+  pa.wide_units = reinterpret_cast<uint32_t*>(w + offsets[10]);
   pa.item_counters = reinterpret_cast<uint32_t*>(w + offsets[5]);
   pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
   pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
@@ -823,6 +830,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.unit_count = pa.unit_count;
   ea.unit_expert = pa.unit_expert;
   ea.unit_rows = pa.unit_rows;
+  ea.wide_units = pa.wide_units;
   ea.item_counters = pa.item_counters;
   ea.hidden_flags = pa.hidden_flags;
   ea.partials = reinterpret_cast<float*>(w + offsets[7]);

@@ -19,28 +19,34 @@ constexpr int NACC = kAccSets;
 constexpr int kHalvesFrom = 256;  // more units than this: split them into halves A and B
 constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memory
 constexpr int kAgreeSlots = 2 * NACC;  // epilogue decisions in flight after an abort
+static_assert(kAgreeSlots >= 2 * Rows<16>::kSets, "agreement slots for every unit size");
 constexpr uint32_t kWaitHintNs = 20000;  // longest suspension of one mbarrier wait step
 
 // Shared-memory carve-up. The swizzled operand images (weights, activation
 // and hidden codes) start on 1024-byte boundaries, every other region on a
 // 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
+// Units of `rows` rows (8, or 16 in the grid kernel's larger calls) set the
+// ring depth, the accumulator sets and the image sizes (Rows<R>).
 struct Layout {
   int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, bytes;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
-  __host__ __device__ explicit Layout(int kc2) {
+  __host__ __device__ explicit Layout(int kc2, int unit_rows = 8) {
+    const int slots = unit_rows == 8 ? Rows<8>::kSlots : Rows<16>::kSlots;
+    const int sets = unit_rows == 8 ? Rows<8>::kSets : Rows<16>::kSets;
+    const int image = unit_rows * kChunkK;
     int o = 0;
-    w = o;                 o += S * kStageSmemWeights;
-    act = o = up(o, 1024); o += S * kActImageBytes;
-    hcodes = o = up(o, 1024); o += 2 * kc2 * kActImageBytes;
-    asf = o = up(o, 16);   o += S * 2 * kScaleAtomBytes;
-    out = o = up(o, 16);   o += kUnitRows * 2 * kTileM * 2;
-    bsf = o = up(o, 16);   o += S * kScaleAtomBytes;
+    w = o;                 o += slots * kStageSmemWeights;
+    act = o = up(o, 1024); o += slots * image;
+    hcodes = o = up(o, 1024); o += 2 * kc2 * image;
+    asf = o = up(o, 16);   o += slots * 2 * kScaleAtomBytes;
+    out = o = up(o, 16);   o += unit_rows * 2 * kTileM * 2;
+    bsf = o = up(o, 16);   o += slots * kScaleAtomBytes;
     hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
     table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
-    bars = o = up(o, 16);  o += (2 * S + 2 * NACC + 4 + kMmaWarps) * 8;
-    meta = o = up(o, 16);  o += NACC * 16;
+    bars = o = up(o, 16);  o += (2 * slots + 2 * sets + 4 + kMmaWarps) * 8;
+    meta = o = up(o, 16);  o += sets * 16;
     misc = o = up(o, 16);  o += 16;
-    rows = o = up(o, 16);  o += kRowCache * (8 + kUnitRows * 2);
+    rows = o = up(o, 16);  o += kRowCache * (12 + unit_rows * 2);
     agree = o = up(o, 16); o += kAgreeSlots * 4;
     bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }

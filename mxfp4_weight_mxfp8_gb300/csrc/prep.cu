@@ -11,7 +11,11 @@
 // Grouping: ExpertsKernel.group / ExpertsGroupKernel: per-expert token
 // bitmasks (atomic OR), unit counts ceil(n_e / 8), an exclusive scan in
 // expert order, and each pair's row = popcount of the lower tokens' bits.
-// Experts ascend, rows keep token order, padding is -1.
+// Experts ascend, rows keep token order, padding is -1. Alongside, the
+// table of 16-row units the grid kernel runs for calls of more than 8
+// tokens: expert e's units taken two at a time (ceil(units_e / 2) entries,
+// in table order), each entry the first unit's index, the expert and
+// whether the next unit belongs to it (see kWideFirstMask).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -106,15 +110,17 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   }
   __syncthreads();
 
-  // Units per expert over a contiguous expert range per thread, then an
-  // exclusive scan in expert order.
+  // Units and pairs of units per expert over a contiguous expert range per
+  // thread, then one exclusive scan in expert order of both counts packed
+  // into one word (units << 16 | pairs; both stay below 2^15).
   const int span = (E + kPrepThreads - 1) / kPrepThreads;
   const int e0 = tid * span, e1 = min(E, e0 + span);
   int local = 0;
   for (int e = e0; e < e1; ++e) {
     int n = 0;
     for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
-    local += (n + 7) >> 3;
+    const int un = (n + 7) >> 3;
+    local += (un << 16) | ((un + 1) >> 1);
   }
   int incl = local;
 #pragma unroll
@@ -131,16 +137,23 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   for (int e = e0; e < e1; ++e) {
     int n = 0;
     for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
-    ustart[e] = start;
-    start += (n + 7) >> 3;
+    const int un = (n + 7) >> 3, us = start >> 16, ws = start & 0xFFFF;
+    ustart[e] = us;
+    for (int k = 0; 2 * k < un && ws + k < a.unit_cap; ++k)
+      a.wide_units[ws + k] = wide_entry(us + 2 * k, e, 2 * k + 1 < un);
+    start += (un << 16) | ((un + 1) >> 1);
   }
   __syncthreads();
-  int units = *grand;
+  int units = *grand >> 16;
+  const int wides = *grand & 0xFFFF;
   if (units > a.unit_cap) {  // cannot happen: units <= 2B + min(E, 16B)
     report(a.status, MOE_ERR_DEVICE_IDS);
     units = 0;
   }
-  if (tid == 0) *a.unit_count = units;
+  if (tid == 0) {
+    a.unit_count[0] = units;
+    a.unit_count[1] = units > 0 ? wides : 0;
+  }
   if (units == 0) return;
   // One thread per unit: its expert is the last one whose first unit is at
   // or before it (experts without units share the next one's start). Rows
@@ -203,14 +216,21 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
     }
   nun[tid] = (kept && before == 0) ? (n + 7) >> 3 : 0;
   __syncthreads();
-  int units = 0, ubefore = 0;
+  // Each expert here has at most 16 pairs: one or two units, one pair of units.
+  int units = 0, ubefore = 0, wides = 0, wbefore = 0;
 #pragma unroll 4
   for (int q = 0; q < pairs; q += 4) {
     const int4 v = nun4[q >> 2], k = key4[q >> 2];
     units += v.x + v.y + v.z + v.w;
     ubefore += (k.x < e ? v.x : 0) + (k.y < e ? v.y : 0) + (k.z < e ? v.z : 0) + (k.w < e ? v.w : 0);
+    wides += (v.x > 0) + (v.y > 0) + (v.z > 0) + (v.w > 0);
+    wbefore += (k.x < e && v.x > 0) + (k.y < e && v.y > 0) + (k.z < e && v.z > 0) + (k.w < e && v.w > 0);
   }
-  if (tid == 0) *a.unit_count = units;
+  if (tid == 0) {
+    a.unit_count[0] = units;
+    a.unit_count[1] = wides;
+  }
+  if (kept && before == 0) a.wide_units[wbefore] = wide_entry(ubefore, e, n > 8);
   if (kept) {
     const int u = ubefore + (before >> 3), r = before & 7;
     a.unit_rows[u * kUnitRows + r] = static_cast<int16_t>(tid);

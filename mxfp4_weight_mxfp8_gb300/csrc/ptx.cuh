@@ -317,13 +317,13 @@ __device__ __forceinline__ void tmem_wait_loads() {
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A = E2M1 (5),
-// B = E4M3 (0), both K-major, N = 8, UE8M0 scales, M = 128; scale_id selects
-// byte scale_id of the 32-bit TMEM scale words for both A and B.
-__host__ __device__ constexpr uint32_t mma_idesc(uint32_t scale_id) {
+// B = E4M3 (0), both K-major, N (8 or 16), UE8M0 scales, M = 128; scale_id
+// selects byte scale_id of the 32-bit TMEM scale words for both A and B.
+__host__ __device__ constexpr uint32_t mma_idesc(uint32_t scale_id, uint32_t n = 8) {
   return (scale_id << 4)          // B scale-factor byte
          | (5u << 7)              // A: e2m1
          | (0u << 10)             // B: e4m3
-         | ((8u >> 3) << 17)      // N / 8
+         | ((n >> 3) << 17)       // N / 8
          | (1u << 23)             // UE8M0 scale factors
          | ((128u >> 4) << 24)    // M / 16
          | (scale_id << 29);      // A scale-factor byte

@@ -748,3 +748,59 @@ def test_single_launch_call_after_bad_ids_is_exact(moe):
     assert status == moe.MOE_OK
     xq, xs = oracle.quantize_x(x)
     check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tp8 B1 after bad ids")
+
+
+def ids_with_counts(B, E, counts, seed):
+    """Routing ids where expert k is picked by the first counts[k] tokens and
+    the other slots by distinct experts >= len(counts), in shuffled order."""
+    rng = np.random.default_rng(seed)
+    ids = np.zeros((B, 16), np.int32)
+    for t in range(B):
+        row = [k for k, c in enumerate(counts) if t < c]
+        row += list(rng.choice(np.arange(len(counts), E), 16 - len(row), replace=False))
+        row = np.array(row, np.int32)
+        rng.shuffle(row)
+        ids[t] = row
+    return ids
+
+
+@pytest.mark.parametrize("shape", [(32, 256, 64), (64, 512, 384)], ids=["tiny", "I384"])
+@pytest.mark.parametrize("B,counts", [
+    (12, [7, 8, 9, 12]),                          # one grouping block path (<= 256 pairs)
+    (16, [7, 8, 9, 15, 16]),
+    (40, [7, 8, 9, 15, 16, 17, 24, 32, 40]),      # the general grouping path
+])
+def test_pairs_of_units_at_unit_boundaries(moe, shape, B, counts):
+    """Calls of more than 8 tokens run pairs of the table's 8-row units as
+    16-row units. Experts with 7, 8, 9, 15, 16, 17, 24, 32 and 40 tokens give
+    single units, full and partial pairs and odd unit counts; the output, the
+    unit table and the hidden read-back (rows 8-15 of a pair land in the
+    second unit's image) must hold for every pair."""
+    import torch
+
+    E, H, I = shape
+    weights = workload.make_weights(E, H, I, seed13=41, seed2=42)
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
+    x = workload.make_x(B, H, seed=43 + B)
+    ids = ids_with_counts(B, E, counts, seed=44 + B)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids, want_hidden=True)
+    check_rows(got, ref["out"], f"E={E} H={H} I={I} B={B} counts {counts}")
+    experts, rows = units_of(moe, layer, B)
+    ref_e, ref_r = oracle.group(ids, E)
+    np.testing.assert_array_equal(experts, ref_e)
+    np.testing.assert_array_equal(rows, ref_r)
+    hq = np.zeros((len(experts), 8, I), np.uint8)
+    hs = np.zeros((len(experts), 8, I // 32), np.uint8)
+    moe.moe_copy_hidden(layer.handle, hq, hs, len(experts))
+    flips = 0
+    for u in range(len(experts)):
+        for r in range(8):
+            p = int(rows[u, r])
+            if p >= 0:
+                flips += int(np.sum(hq[u, r] != ref["hq"][p]))
+                assert np.sum(hs[u, r] != ref["hs"][p]) <= 1, f"unit {u} row {r}: hidden scales"
+    assert flips <= max(8, B * 16 * I // 100), f"{flips} hidden code flips"
+    layer.close()

@@ -121,13 +121,13 @@ def test_noalloc_matches_moe_run_on_consecutive_calls_tp8(moe):
 def test_noalloc_refuses_a_batch_beyond_the_static_buffer(moe):
     import torch
 
-    weights, x, ids = cached_inputs("tp8_b64")
+    weights, x, ids = cached_inputs("tp8_b256")  # about 9 MB of scratch
     layer = make_layer(moe, weights)
     xd, idsd = to_device(x, ids)
-    out = torch.zeros((64, 16, layer.hidden), dtype=torch.bfloat16, device=xd.device)
+    out = torch.zeros((256, 16, layer.hidden), dtype=torch.bfloat16, device=xd.device)
     torch.cuda.synchronize()
     rc = moe.library().moe_run_noalloc(layer.handle, xd.data_ptr(), idsd.data_ptr(),
-                                       out.data_ptr(), 64, torch.cuda.current_stream().cuda_stream)
+                                       out.data_ptr(), 256, torch.cuda.current_stream().cuda_stream)
     assert rc == moe.MOE_ERR_ARG
     detail = moe.moe_last_error_detail()
     assert "scratch" in detail and str(moe.MOE_NOALLOC_SCRATCH_BYTES) in detail, detail
