@@ -135,9 +135,17 @@ int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream);
  *   topk_ids   device int32 [batch, 16] (same rules as moe_group)
  *   out_bf16   device BF16 [batch, 16, H], 16-byte aligned; row t*16+s is
  *              expert ids[t, s]'s output for token t
- * Asynchronous on `stream` (two kernel launches, the second overlapping the
- * first's tail); device-side errors surface through moe_sync_status.
- * Errors: MOE_ERR_ARG (nulls, misalignment, batch range), MOE_ERR_CUDA.
+ * Asynchronous on `stream`; device-side errors surface through
+ * moe_sync_status. A call of one or two tokens is one launch of the
+ * small-batch kernel, any other call a prep grid and the experts kernel.
+ * Launches are chained with programmatic dependent launch: the small-batch
+ * kernel lets the next launch on the stream start while its own CTAs still
+ * run, and a call reads its x and ids as soon as it starts. So x and ids
+ * must not be the out_bf16 of the moe_run call just before on the stream
+ * (every other producer is safe: a kernel of the caller, or
+ * moe_run_combined, whose last launch lets the next start only when it has
+ * ended). Errors: MOE_ERR_ARG (nulls, misalignment, batch range),
+ * MOE_ERR_CUDA.
  */
 int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
             void* stream);

@@ -20,9 +20,9 @@ namespace {
 constexpr int kCombineThreads = 256;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
-  // The next call's experts kernel may start now: it writes nothing this
-  // grid reads before this grid has ended.
-  ptx::grid_launch_dependents();
+  // No early trigger: the next call may read this call's output as its
+  // input (stacked layers), before any wait of its own, so it starts only
+  // once this grid has completed.
   ptx::grid_dependency_wait();  // the experts grid's rows
   const int per_token = a.H / 8;
   const int i = blockIdx.x * kCombineThreads + threadIdx.x;
@@ -78,7 +78,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = stream;
   // Chained to the experts launch before it (programmatic dependent launch):
-  // its few blocks sit beside the experts kernel's CTAs until that grid ends.
+  // its blocks may be placed while that grid runs and wait for it to end.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

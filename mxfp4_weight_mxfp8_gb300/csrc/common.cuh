@@ -44,6 +44,12 @@ constexpr int kMmaWarp0 = 1;              // warps 1..4
 constexpr int kGatherWarp = 5;
 constexpr int kEpilogueWarp0 = 6;         // warps 6..9: the epilogue warpgroup
 constexpr int kThreads = 320;             // 10 warps
+// The grid kernel adds two scale-copy warps (10, 11): they copy each stage's
+// three scale atoms (weights of tile 0 and 1, activations) into TMEM once
+// for all four issuers, which then issue only MMAs and a commit per stage.
+constexpr int kCopierWarp0 = 10;
+constexpr int kCopiers = 2;
+constexpr int kGridThreads = 384;         // 12 warps
 constexpr int kMaxInterChunks = MOE_MAX_INTER / kChunkK;  // 4
 constexpr int kMaxGrid = 256;             // partition table capacity (CTAs)
 constexpr int kMaxSpanCtas = 512;         // launch-clock slots: CTAs of any experts launch

@@ -81,7 +81,7 @@ __device__ __forceinline__ int unit_row_of(const ExpertsArgs& a, int u, int r) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ ExpertsArgs a) {
+__global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_constant__ ExpertsArgs a) {
   // R rows per unit: the table's units (R = 8) or pairs of them (R = 16).
   using RT = Rows<R>;
   constexpr int S = RT::kSlots;
@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   uint64_t* accempty = accfull + NACC;
   uint64_t* hfull = accempty + NACC;
   uint64_t* hempty = hfull + 2;
-  uint64_t* drained = hempty + 2;  // [issuer]: its tensor-core work has finished
+  uint64_t* drained = hempty + 2;  // [issuer, then copier]: its tensor-core work has finished
+  uint64_t* scaled = drained + kMmaWarps + kCopiers;  // [slot]: the stage's scale atoms are in TMEM
   int* agree = reinterpret_cast<int*>(sm + L.agree);
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort, last flag
@@ -118,6 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   if (tid == 0) {
     span_enter(a.span);
     MOE_STAMP(0);
+    // The next call's prep grid may start as this grid's CTAs leave: it
+    // writes nothing before it has waited for this grid to end.
+    grid_launch_dependents();
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
       mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
@@ -135,11 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     fence_mbar_init();
     prefetch_tensormap(&a.wmap);
   } else if (warp == kMmaWarp0 + 1 && lane == 0) {
-    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&drained[i], 1);
+    for (int i = 0; i < kMmaWarps + kCopiers; ++i) mbar_init(&drained[i], 1);
+    for (int s = 0; s < S; ++s) mbar_init(&scaled[s], kCopiers);  // one commit per copier
     for (int i = 0; i < kAgreeSlots; ++i) agree[i] = -1;
     fence_mbar_init();
   }
-  for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
+  for (int i = tid; i < S * kScaleAtomBytes / 16; i += kGridThreads)
     reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
   if (warp == kMmaWarp0) {
     tmem_alloc(&misc[0], kTmemColumns);
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
   const int stage_base[2] = {0, units_a * g.P1 * g.KC1};
   const int job_base[2] = {0, units_a * g.NQ};
   const int items_a = units_a * g.P1;
-  for (int c = tid; c <= G; c += kThreads) {
+  for (int c = tid; c <= G; c += kGridThreads) {
     start[c] = half[0].fc1_begin(c);
     start[G + 1 + c] = stage_base[1] + half[1].fc1_begin(c);
   }
@@ -249,18 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           first_c = cur.c;
         }
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        if (!(ok = wait_bar(cx, &scaled[slot], phase))) break;
         if (lead && n == 0) MOE_STAMP(4);
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
         tc_fence_after_sync();
-        const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns + issuer * 8;
-        tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-        tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
+        // The slot's scale atoms: tile 0's weights, tile 1's, the activations.
+        const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns;
         const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
         const uint64_t dx = desc_sw128(ACT + slot * kImage + k0 * 32);
         const uint32_t d = tmem + set * RT::kSetColumns + issuer * R;
         // Descriptor start addresses count 16-byte units: +2 is the next K-step.
-        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0, R), sf, sf + 4, first ? 0u : 1u);
-        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1, R), sf, sf + 4, 1u);
+        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0, R), sf + 4 * t, sf + 8, first ? 0u : 1u);
+        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1, R), sf + 4 * t, sf + 8, 1u);
         if (lead) MOE_STAMP(5);
         tc_commit(&empty[slot]);
         advance();
@@ -290,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         bool started = false;
         for (int c = 0; c < g.KC2 && ok; ++c) {
           if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+          if (!(ok = wait_bar(cx, &scaled[slot], phase))) break;
           if (lead && !fc2_seen) {
             MOE_STAMP(10);
             fc2_seen = true;
@@ -298,10 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
           // K-steps of this chunk: 4, or fewer in the last chunk when I % 128 != 0.
           const int ksteps = c + 1 < g.KC2 ? 4 : (g.I - c * kChunkK) / kBlock;
           if (k0 < ksteps) {
-            const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns + issuer * 8;
+            const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns + 4 * t;
             const int hc = hb * g.KC2 + c;
             const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
-            tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + hc * kImage + k0 * 32);
             const uint32_t d = tmem + set * RT::kSetColumns + issuer * R;
@@ -336,6 +341,39 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       // this thread has finished (after a failure nobody else waits on them).
       tc_commit(&drained[issuer]);
       wait_own(cx, &drained[issuer], 0);
+    }
+  } else if (warp >= kCopierWarp0) {
+    // ----------------------------------------------------------- scale copies
+    // Copier 0 copies tile 0's weight scales and (FC1) the activation scales
+    // of every stage, copier 1 tile 1's, into the slot's TMEM columns, and
+    // each commits to the slot's `scaled` barrier, which the issuers wait on.
+    // The slot is refilled only after the issuers' MMAs (which waited on
+    // these copies) are done, so the columns are free again by then.
+    if (lane == 0) {
+      const int c = warp - kCopierWarp0;
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      auto copy = [&](bool activations) {
+        if (!(ok = wait_bar(cx, &full[slot], phase))) return;
+        fence_proxy_async_shared();  // the activation scales were cp.async (generic) writes
+        tc_fence_after_sync();
+        const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns;
+        tc_copy_scales(sf + 4 * c, desc_scales(ASF + slot * 2 * kScaleAtomBytes + c * kScaleAtomBytes));
+        if (activations && c == 0) tc_copy_scales(sf + 8, desc_scales(BSF + slot * kScaleAtomBytes));
+        tc_commit(&scaled[slot]);
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+      };
+      for (int hf = 0; hf < 2; ++hf)
+        for (Fc1Cursor cur(f0[hf], g); cur.s < f1[hf] && ok; cur.next(g)) copy(true);
+      for (int hf = 0; hf < 2; ++hf)
+        for (Fc2Cursor cur(j0[hf], g); cur.j < j1[hf] && ok; cur.next(g))
+          for (int cc = 0; cc < g.KC2 && ok; ++cc) copy(false);
+      tc_commit(&drained[kMmaWarps + c]);
+      wait_own(cx, &drained[kMmaWarps + c], 0);
     }
   } else if (warp == kGatherWarp) {
     // ------------------------------- activation gather (FC1), hidden loader (FC2)
@@ -473,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
       __syncwarp();
       if (lane == 0 && cur.u != a.withhold_image) mbar_arrive(&hfull[b]);
     }
-  } else if (warp >= kEpilogueWarp0) {
+  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int et = tid - kEpilogueWarp0 * 32;
@@ -1339,10 +1377,10 @@ int cluster_size_for(const Geometry& g, int batch) {
 
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
   int wide = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, experts_kernel<8>, kThreads,
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, experts_kernel<8>, kGridThreads,
                                                                 experts_smem_bytes(g, 8));
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&wide, experts_kernel<16>, kThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&wide, experts_kernel<16>, kGridThreads,
                                                       experts_smem_bytes(g, 16));
   if (e == cudaSuccess && wide < *blocks_per_sm) *blocks_per_sm = wide;
   return e;
@@ -1397,6 +1435,7 @@ cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, 
     return cudaLaunchKernelEx(&cfg, cluster_kernel, a, plan);
   }
   cfg.numAttrs = n;
+  cfg.blockDim = dim3(kGridThreads);
   if (rows == 16) return cudaLaunchKernelEx(&cfg, experts_kernel<16>, a);
   return cudaLaunchKernelEx(&cfg, experts_kernel<8>, a);
 }

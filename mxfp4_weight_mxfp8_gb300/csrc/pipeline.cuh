@@ -43,7 +43,7 @@ struct Layout {
     bsf = o = up(o, 16);   o += slots * kScaleAtomBytes;
     hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
     table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
-    bars = o = up(o, 16);  o += (2 * slots + 2 * sets + 4 + kMmaWarps) * 8;
+    bars = o = up(o, 16);  o += (3 * slots + 2 * sets + 4 + kMmaWarps + kCopiers) * 8;
     meta = o = up(o, 16);  o += sets * 16;
     misc = o = up(o, 16);  o += 16;
     rows = o = up(o, 16);  o += kRowCache * (12 + unit_rows * 2);

@@ -25,16 +25,26 @@ namespace {
 constexpr int kPrepThreads = 256;
 constexpr int kQuantChunks = 4;  // 256-chunk runs per quantizer block
 
-__device__ void quantize_chunk(const PrepArgs& a, int chunk) {
+// One 8-value chunk (a 16-byte load) of the plan, computed in registers: the
+// four threads of a 32-block combine their maxima with two butterfly
+// shuffles. Stored by store_chunk.
+struct PlanChunk {
+  uint2 codes;
+  int token, c, E;
+  bool active;
+};
+
+__device__ PlanChunk quantize_chunk(const PrepArgs& a, int chunk) {
+  PlanChunk q{};
   const int per_row = a.H / 8;  // 8-value chunks per token
   const int total = a.B * per_row;
-  const bool active = chunk < total;  // uniform across each 4-lane block (total % 4 == 0)
-  const int token = active ? chunk / per_row : 0;
-  const int c = active ? chunk % per_row : 0;
+  q.active = chunk < total;  // uniform across each 4-lane block (total % 4 == 0)
+  q.token = q.active ? chunk / per_row : 0;
+  q.c = q.active ? chunk % per_row : 0;
   float v[8];
   float amax = 0.f;
-  if (active) {
-    uint4 w = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(token) * a.H + c * 8);
+  if (q.active) {
+    uint4 w = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(q.token) * a.H + q.c * 8);
     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -46,25 +56,37 @@ __device__ void quantize_chunk(const PrepArgs& a, int chunk) {
   }
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  if (!active) return;
-  const int E = mx_exponent(amax, false);
-  const float inv = pow2f(-E);
+  if (!q.active) return q;
+  q.E = mx_exponent(amax, false);
+  const float inv = pow2f(-q.E);
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
 #pragma unroll
   for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(e4m3_code(v[4 + i] * inv)) << (8 * i);
-  *reinterpret_cast<uint2*>(a.plan_codes + static_cast<size_t>(token) * a.H + c * 8) =
-      make_uint2(lo, hi);
-  if ((c & 3) == 0)
-    a.plan_scales[static_cast<size_t>(token) * (a.H / kBlock) + c / 4] =
-        static_cast<uint8_t>(E + 127);
+  q.codes = make_uint2(lo, hi);
+  return q;
 }
 
-// Quantizer blocks own kQuantChunks consecutive runs of 256 chunks each.
+__device__ void store_chunk(const PrepArgs& a, const PlanChunk& q) {
+  if (!q.active) return;
+  *reinterpret_cast<uint2*>(a.plan_codes + static_cast<size_t>(q.token) * a.H + q.c * 8) = q.codes;
+  if ((q.c & 3) == 0)
+    a.plan_scales[static_cast<size_t>(q.token) * (a.H / kBlock) + q.c / 4] =
+        static_cast<uint8_t>(q.E + 127);
+}
+
+// Quantizer blocks own kQuantChunks consecutive runs of 256 chunks each: all
+// are loaded and quantized first, then (after the previous grid on the
+// stream has ended) stored.
 __device__ void quantize_role(const PrepArgs& a, int block) {
+  PlanChunk q[kQuantChunks];
+#pragma unroll
   for (int r = 0; r < kQuantChunks; ++r)
-    quantize_chunk(a, (block * kQuantChunks + r) * kPrepThreads + threadIdx.x);
+    q[r] = quantize_chunk(a, (block * kQuantChunks + r) * kPrepThreads + threadIdx.x);
+  ptx::grid_dependency_wait();
+#pragma unroll
+  for (int r = 0; r < kQuantChunks; ++r) store_chunk(a, q[r]);
 }
 
 __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
@@ -87,7 +109,10 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   __syncthreads();
   // A pair is kept unless its id is out of range or repeats an earlier slot
   // of its token (whichever atomic OR lands first keeps the bit).
+  // (Dropped pairs are reported, and the kept flags stored, after the wait
+  // below: nothing is written to global memory before it.)
   uint32_t kept_bits = 0;
+  bool dropped = false;
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
     const int base = it * kPrepThreads + warp * 32;
@@ -96,17 +121,14 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
     bool kept = false;
     if (p < pairs) {
       const int e = ev[it], t = p >> 4;
-      if (e < 0 || e >= E) {
-        report(a.status, MOE_ERR_DEVICE_IDS);
-      } else {
+      if (e >= 0 && e < E) {
         const uint32_t bit = 1u << (t & 31);
         const uint32_t old = atomicOr(&masks[e * words + (t >> 5)], bit);
-        kept = !(old & bit);
-        if (!kept) report(a.status, MOE_ERR_DEVICE_IDS);  // the expert repeats within token t
+        kept = !(old & bit);  // else the expert repeats within token t
       }
+      dropped |= !kept;
     }
     kept_bits |= static_cast<uint32_t>(kept) << it;
-    if (a.pair_kept != nullptr && p < pairs) a.pair_kept[p] = kept ? 1 : 0;
   }
   __syncthreads();
 
@@ -134,6 +156,15 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   for (int w = 0; w < warp; ++w) before += warp_total[w];
   if (tid == kPrepThreads - 1) *grand = before + incl;
   int start = before + incl - local;
+  // The previous grid on the stream may still read the tables written below.
+  ptx::grid_dependency_wait();
+  if (dropped) report(a.status, MOE_ERR_DEVICE_IDS);
+  if (a.pair_kept != nullptr)
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int p = it * kPrepThreads + tid;
+      if (p < pairs) a.pair_kept[p] = (kept_bits >> it) & 1u;
+    }
   for (int e = e0; e < e1; ++e) {
     int n = 0;
     for (int w = 0; w < words; ++w) n += __popc(masks[e * words + w]);
@@ -198,8 +229,6 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   const bool valid = tid < pairs && e >= 0 && e < a.E;
   const unsigned same = __match_any_sync(0xFFFFFFFFu, valid ? 2 * e + ((lane >> 4) & 1) : -1 - lane);
   const bool kept = valid && __ffs(same) - 1 == lane;
-  if (tid < pairs && !kept) report(a.status, MOE_ERR_DEVICE_IDS);  // out of range or repeated
-  if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   key[tid] = kept ? e : 0x7FFFFFFF;
   __syncthreads();
   // Both loops read four pairs per 16-byte load (pairs is a multiple of 16).
@@ -226,6 +255,10 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
     wides += (v.x > 0) + (v.y > 0) + (v.z > 0) + (v.w > 0);
     wbefore += (k.x < e && v.x > 0) + (k.y < e && v.y > 0) + (k.z < e && v.z > 0) + (k.w < e && v.w > 0);
   }
+  // The previous grid on the stream may still read the tables written below.
+  ptx::grid_dependency_wait();
+  if (tid < pairs && !kept) report(a.status, MOE_ERR_DEVICE_IDS);  // out of range or repeated
+  if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   if (tid == 0) {
     a.unit_count[0] = units;
     a.unit_count[1] = wides;
@@ -243,6 +276,11 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
   for (int i = tid; i < units * a.KC2; i += kPrepThreads) a.hidden_flags[i] = 0;
 }
 
+// Chained to the previous launch on the stream (programmatic dependent
+// launch): every role reads ids and x and does its work in registers and
+// shared memory first, and waits for the previous grid to end only before
+// its first global write, so that work overlaps the previous experts
+// kernel's tail. ids and x themselves are read at once (see moe_run).
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   // Let the experts kernel start its prologue; it waits for this grid's end
@@ -279,9 +317,17 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (a.roles & kPrepQuantize) blocks += a.quant_blocks;
   if (a.roles & kPrepGroup) blocks += 1;
   if (blocks == 0) return cudaSuccess;
-  const int smem = (a.roles & kPrepGroup) ? prep_group_smem_bytes(a.E) : 0;
-  prep_kernel<<<blocks, kPrepThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kPrepThreads);
+  cfg.dynamicSmemBytes = (a.roles & kPrepGroup) ? prep_group_smem_bytes(a.E) : 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prep_kernel, a);
 }
 
 }  // namespace moe

@@ -804,3 +804,37 @@ def test_pairs_of_units_at_unit_boundaries(moe, shape, B, counts):
                 assert np.sum(hs[u, r] != ref["hs"][p]) <= 1, f"unit {u} row {r}: hidden scales"
     assert flips <= max(8, B * 16 * I // 100), f"{flips} hidden code flips"
     layer.close()
+
+
+@pytest.mark.parametrize("batch", [1, 2, 8])
+def test_stacked_combined_calls_read_the_previous_output(moe, batch):
+    """Layer stacking: each moe_run_combined call takes the previous call's
+    combined output as its x, queued back to back on one stream. The chained
+    launches must not let a call read x before the call that writes it has
+    ended: the rows equal those of the same calls with a synchronize between."""
+    import torch
+
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    H = layer.hidden
+    x0 = workload.make_x(batch, H, seed=61 + batch)
+    ids = workload.make_ids(batch, weights[0].shape[0], seed=62 + batch)
+    xd, idsd = to_device(x0, ids)
+    wd = torch.from_numpy(routing_weights(batch, seed=63)).to("cuda:0")
+    depth = 6
+
+    def stack(sync):
+        bufs = [xd] + [torch.empty((batch, H), dtype=torch.bfloat16, device="cuda:0") for _ in range(depth)]
+        for i in range(depth):
+            moe.moe_run_combined(layer.handle, bufs[i], idsd, wd, bufs[i + 1], batch)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert moe.moe_sync_status(layer.handle) == moe.MOE_OK
+        return [b.view(torch.int16).cpu().numpy() for b in bufs[1:]]
+
+    ref = stack(True)
+    for rep in range(3):
+        got = stack(False)
+        for i in range(depth):
+            np.testing.assert_array_equal(got[i], ref[i], err_msg=f"rep {rep} layer {i}")
