@@ -43,17 +43,18 @@ namespace {
 using namespace ptx;
 
 // Unit u of a launch with R-row units: the table's unit u (R = 8), or the
-// pair-table entry u (R = 16; see kWideFirstMask).
+// pair-table entry u (R = 16; see kWideFirstMask). `xc` is the shared-memory
+// copy of unit_expert (R = 8) or of the pair table (R = 16).
 template <int R>
-__device__ __forceinline__ int unit_first_of(const ExpertsArgs& a, int u) {
+__device__ __forceinline__ int unit_first_of(const uint32_t* xc, int u) {
   if constexpr (R == 8) return u;
-  else return static_cast<int>(a.wide_units[u] & kWideFirstMask);
+  else return static_cast<int>(xc[u] & kWideFirstMask);
 }
 
 template <int R>
-__device__ __forceinline__ int unit_expert_of(const ExpertsArgs& a, int u) {
-  if constexpr (R == 8) return a.unit_expert[u];
-  else return static_cast<int>((a.wide_units[u] >> 20) & 0x3FFu);
+__device__ __forceinline__ int unit_expert_of(const uint32_t* xc, int u) {
+  if constexpr (R == 8) return static_cast<int>(xc[u]);
+  else return static_cast<int>((xc[u] >> 20) & 0x3FFu);
 }
 
 // Rows of table unit tu: its pairs, then -1 padding (one 16-byte load).
@@ -70,11 +71,11 @@ __device__ __forceinline__ int table_unit_valid(const ExpertsArgs& a, int tu) {
 // Row r of unit u: a pair index (token * 16 + slot) or -1 (padding). A
 // pair's rows 8-15 are the second table unit's, which follows the first.
 template <int R>
-__device__ __forceinline__ int unit_row_of(const ExpertsArgs& a, int u, int r) {
+__device__ __forceinline__ int unit_row_of(const ExpertsArgs& a, const uint32_t* xc, int u, int r) {
   if constexpr (R == 8) {
     return a.unit_rows[u * kUnitRows + r];
   } else {
-    const uint32_t w = a.wide_units[u];
+    const uint32_t w = xc[u];
     const int first = static_cast<int>(w & kWideFirstMask);
     return (r < kUnitRows || (w >> 31)) ? a.unit_rows[first * kUnitRows + r] : -1;
   }
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const Geometry& g = a.g;
-  const Layout L(g.KC2, R);
+  const Layout L(g.KC2, R, true);
   uint8_t* W = sm + L.w;
   uint8_t* ACT = sm + L.act;
   uint8_t* ASF = sm + L.asf;
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
     for (int i = 0; i < kAgreeSlots; ++i) agree[i] = -1;
     fence_mbar_init();
   }
-  for (int i = tid; i < S * kScaleAtomBytes / 16; i += kGridThreads)
+  for (int i = tid; i < ((S - 1) * L.bsf_stride + kScaleAtomBytes) / 16; i += kGridThreads)
     reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
   if (warp == kMmaWarp0) {
     tmem_alloc(&misc[0], kTmemColumns);
@@ -152,7 +153,15 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
   }
 
   // The plan, unit table and cleared counters of the preceding prep grid.
+  // Every unit's expert goes to shared memory in the same round trip as the
+  // unit count (entries past the count are never used).
   grid_dependency_wait();
+  uint32_t* xc = reinterpret_cast<uint32_t*>(sm + L.units);
+  {
+    const int cap = min(2 * a.B + min(g.E, kTopK * a.B), R == 8 ? kUnitCache8 : kUnitCache16);
+    const uint32_t* src = R == 8 ? reinterpret_cast<const uint32_t*>(a.unit_expert) : a.wide_units;
+    for (int i = tid; i < cap; i += kGridThreads) xc[i] = src[i];
+  }
   const int units = a.unit_count[R == 8 ? 0 : 1];
   if (tid == 0) MOE_STAMP(3);
   // Half A = units [0, units_a). Small calls keep one half: their chain of
@@ -207,13 +216,13 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
       int cu = -1, e = 0;
       for (int h = 0; h < 2; ++h)
         for (Fc1Cursor cur(f0[h], g); cur.s < f1[h] && ok; cur.next(g)) {
-          if (cur.u != cu) { e = unit_expert_of<R>(a, cur.u); cu = cur.u; }
+          if (cur.u != cu) { e = unit_expert_of<R>(xc, cur.u); cu = cur.u; }
           ok = issue(e * g.SPE + cur.p * g.KC1 + cur.c, false);
         }
       cu = -1;
       for (int h = 0; h < 2; ++h)
         for (Fc2Cursor cur(j0[h], g); cur.j < j1[h] && ok; cur.next(g)) {
-          if (cur.u != cu) { e = unit_expert_of<R>(a, cur.u); cu = cur.u; }
+          if (cur.u != cu) { e = unit_expert_of<R>(xc, cur.u); cu = cur.u; }
           const int base = e * g.SPE + fc1_stages + cur.q * g.KC2;
           for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
         }
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         tc_fence_after_sync();
         const uint32_t sf = tmem + RT::kScaleBase + slot * kSlotScaleColumns;
         tc_copy_scales(sf + 4 * c, desc_scales(ASF + slot * 2 * kScaleAtomBytes + c * kScaleAtomBytes));
-        if (activations && c == 0) tc_copy_scales(sf + 8, desc_scales(BSF + slot * kScaleAtomBytes));
+        if (activations && c == 0) tc_copy_scales(sf + 8, desc_scales(BSF + slot * L.bsf_stride));
         tc_commit(&scaled[slot]);
         if (++slot == S) {
           slot = 0;
@@ -385,8 +394,8 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
     for (Fc1Cursor cur(f0[hf], g); cur.s < f1[hf] && ok; cur.next(g)) {
       if (cur.u != cu) {
         // Lane l gathers row l / (32 / R) of the image and the scales of row l.
-        const int pc = unit_row_of<R>(a, cur.u, lane / (32 / R));
-        const int ps = unit_row_of<R>(a, cur.u, lane % R);
+        const int pc = unit_row_of<R>(a, xc, cur.u, lane / (32 / R));
+        const int ps = unit_row_of<R>(a, xc, cur.u, lane % R);
         tok_code = pc >= 0 ? (pc >> 4) : -1;
         tok_scale = ps >= 0 ? (ps >> 4) : -1;
         cu = cur.u;
@@ -410,7 +419,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         const uint8_t* src = a.plan_scales +
                              static_cast<size_t>(tok_scale < 0 ? 0 : tok_scale) * (g.H / kBlock) +
                              cur.c * (kChunkK / kBlock);
-        cp_async_4(BSF + slot * kScaleAtomBytes + lane * 16, src, tok_scale < 0 ? 0u : 4u);
+        cp_async_4(BSF + slot * L.bsf_stride + lane * 16, src, tok_scale < 0 ? 0u : 4u);
       }
       cp_async_arrive_noinc(&full[slot]);
       ++n;
@@ -475,7 +484,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         // second atom of every chunk, bytes 128-255 of every scale atom)
         // from the second's. Per unit: KC2 x 64 code vectors, then the
         // KC2 scale atoms' first 128 bytes (8 vectors each).
-        const uint32_t w = a.wide_units[cur.u];
+        const uint32_t w = xc[cur.u];
         const int first = static_cast<int>(w & kWideFirstMask);
         const int per_unit = g.KC2 * (kActImageBytes / 16 + 8);
         const int n_all = (w >> 31) ? 2 * per_unit : per_unit;
@@ -533,11 +542,11 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
       if (et < kRowCache) {
         const int u = lo + et;
         cache_unit[et] = (u <= hi) ? u : -1;
-        cache_first[et] = (u <= hi) ? unit_first_of<R>(a, u) : -1;
+        cache_first[et] = (u <= hi) ? unit_first_of<R>(xc, u) : -1;
       }
       for (int i = et; i < kRowCache * R; i += 128) {
         const int u = lo + i / R;
-        cache_rows[i] = (u <= hi) ? unit_row_of<R>(a, u, i % R) : -1;
+        cache_rows[i] = (u <= hi) ? unit_row_of<R>(a, xc, u, i % R) : -1;
       }
       epilogue_sync();
       if (et < kRowCache) {
@@ -553,11 +562,11 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
     };
     auto unit_row = [&](int u, int r) -> int {
       const int i = cached(u);
-      return i >= 0 ? cache_rows[i * R + r] : unit_row_of<R>(a, u, r);
+      return i >= 0 ? cache_rows[i * R + r] : unit_row_of<R>(a, xc, u, r);
     };
     auto unit_first = [&](int u) -> int {
       const int i = cached(u);
-      return i >= 0 ? cache_first[i] : unit_first_of<R>(a, u);
+      return i >= 0 ? cache_first[i] : unit_first_of<R>(xc, u);
     };
     auto unit_valid = [&](int u) -> int {
       const int i = cached(u);
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         return table_unit_valid(a, u);
       } else {
         // A pair's first unit is full: 8 + the second's rows.
-        const uint32_t w = a.wide_units[u];
+        const uint32_t w = xc[u];
         const int first = static_cast<int>(w & kWideFirstMask);
         return table_unit_valid(a, (w >> 31) ? first + 1 : first) + ((w >> 31) ? kUnitRows : 0);
       }
@@ -1308,10 +1317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int experts_smem_bytes(const Geometry& g, int unit_rows) { return Layout(g.KC2, unit_rows).bytes; }
+int experts_smem_bytes(const Geometry& g, int unit_rows) { return Layout(g.KC2, unit_rows, true).bytes; }
+
+int experts_max_smem_bytes(const Geometry& g) {
+  const int sizes[] = {Layout(g.KC2, 8, true).bytes, Layout(g.KC2, 16, true).bytes, Layout(g.KC2).bytes};
+  int m = 0;
+  for (int b : sizes) m = b > m ? b : m;
+  return m;
+}
 
 bool experts_layout_aligned(const Geometry& g) {
-  return Layout(g.KC2, 8).aligned() && Layout(g.KC2, 16).aligned();
+  return Layout(g.KC2, 8, true).aligned() && Layout(g.KC2, 16, true).aligned() && Layout(g.KC2).aligned();
 }
 
 namespace {
@@ -1322,11 +1338,12 @@ cudaError_t experts_configure(const Geometry& g) {
   // The attribute belongs to the kernel, not to a handle: allow the largest
   // layout any handle can need (I = 512), so every prepared layer launches.
   (void)g;
-  const int bytes = Layout(kMaxInterChunks).bytes;
-  cudaError_t e = cudaFuncSetAttribute(experts_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const int bytes = Layout(kMaxInterChunks).bytes;  // the cluster variant's
+  cudaError_t e = cudaFuncSetAttribute(experts_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout(kMaxInterChunks, 8, true).bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(experts_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Layout(kMaxInterChunks, 16).bytes);
+                           Layout(kMaxInterChunks, 16, true).bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
@@ -1414,6 +1431,7 @@ cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, 
     attr[n].val.clusterDim.z = 1;
     ++n;
     cfg.numAttrs = n;
+    cfg.dynamicSmemBytes = Layout(a.g.KC2).bytes;
     const int max_units = a.g.E < a.B * kTopK ? a.g.E : a.B * kTopK;
     cfg.gridDim = dim3(max_units * C);
     ClusterPlan plan = {};

@@ -64,6 +64,8 @@ struct ExpertsArgs {
 };
 
 int experts_smem_bytes(const Geometry& g, int unit_rows = 8);
+// The most dynamic shared memory any experts kernel takes for this layer.
+int experts_max_smem_bytes(const Geometry& g);
 bool experts_layout_aligned(const Geometry& g);
 cudaError_t experts_configure(const Geometry& g);
 cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm);

@@ -150,7 +150,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   cudaDeviceProp prop{};
   MOE_CUDA(cudaGetDevice(&h->device));
   MOE_CUDA(cudaGetDeviceProperties(&prop, h->device));
-  h->smem_bytes = moe::experts_smem_bytes(g);
+  h->smem_bytes = moe::experts_max_smem_bytes(g);
   if (!moe::experts_layout_aligned(g)) {
     std::snprintf(g_detail, sizeof g_detail, "internal: misaligned shared-memory layout");
     return MOE_ERR_UNSUPPORTED;
@@ -159,7 +159,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     std::snprintf(g_detail, sizeof g_detail,
                   "needs an sm_103 GPU (GB300) with %d B of shared memory per block; found sm_%d%d "
                   "with %zu B (the library carries sm_103a code only)",
-                  moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)), prop.major,
+                  moe::experts_max_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)), prop.major,
                   prop.minor, static_cast<size_t>(prop.sharedMemPerBlockOptin));
     return MOE_ERR_UNSUPPORTED;
   }
@@ -714,7 +714,7 @@ const char* moe_last_error_detail(void) { return g_detail; }
 
 int moe_device_supported(int cc_major, int cc_minor, size_t smem_per_block_optin) {
   if (cc_major != 10 || cc_minor != 3) return MOE_ERR_UNSUPPORTED;
-  const size_t need = static_cast<size_t>(moe::experts_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)));
+  const size_t need = static_cast<size_t>(moe::experts_max_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)));
   return smem_per_block_optin >= need ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 

@@ -21,16 +21,26 @@ constexpr int kRowCache = 16;    // unit rows the epilogue keeps in shared memor
 constexpr int kAgreeSlots = 2 * NACC;  // epilogue decisions in flight after an abort
 static_assert(kAgreeSlots >= 2 * Rows<16>::kSets, "agreement slots for every unit size");
 constexpr uint32_t kWaitHintNs = 20000;  // longest suspension of one mbarrier wait step
+// The grid kernel keeps every unit's expert (R = 8: unit_expert; R = 16: the
+// pair-table entry) in shared memory: at most 2B + min(E, 16B) units, B <= 8
+// and B <= 256 (E <= 1024).
+constexpr int kUnitCache8 = 2 * 8 + 16 * 8;
+constexpr int kUnitCache16 = 2 * MOE_MAX_BATCH + MOE_MAX_EXPERTS;
 
 // Shared-memory carve-up. The swizzled operand images (weights, activation
 // and hidden codes) start on 1024-byte boundaries, every other region on a
 // 16-byte boundary (mbarriers need 8, int4 metadata and uint4 copies 16).
 // Units of `rows` rows (8, or 16 in the grid kernel's larger calls) set the
-// ring depth, the accumulator sets and the image sizes (Rows<R>).
+// ring depth, the accumulator sets and the image sizes (Rows<R>). The grid
+// kernel (`grid`) packs the per-slot activation scale atoms R x 16 bytes
+// apart: only rows 0..R-1 of an atom are written and used (the 32-row copy
+// of slot s reads slot s + 1's rows into TMEM lanes that an N = R MMA never
+// reads), and only the last atom is a full 512 bytes.
 struct Layout {
-  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, bytes;
+  int w, act, asf, hcodes, out, bsf, hsf, table, bars, meta, misc, rows, agree, units, bytes;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
-  __host__ __device__ explicit Layout(int kc2, int unit_rows = 8) {
+  int bsf_stride;
+  __host__ __device__ explicit Layout(int kc2, int unit_rows = 8, bool grid = false) {
     const int slots = unit_rows == 8 ? Rows<8>::kSlots : Rows<16>::kSlots;
     const int sets = unit_rows == 8 ? Rows<8>::kSets : Rows<16>::kSets;
     const int image = unit_rows * kChunkK;
@@ -40,20 +50,24 @@ struct Layout {
     hcodes = o = up(o, 1024); o += 2 * kc2 * image;
     asf = o = up(o, 16);   o += slots * 2 * kScaleAtomBytes;
     out = o = up(o, 16);   o += unit_rows * 2 * kTileM * 2;
-    bsf = o = up(o, 16);   o += slots * kScaleAtomBytes;
+    bsf_stride = grid ? unit_rows * 16 : kScaleAtomBytes;
+    bsf = o = up(o, 16);   o += (slots - 1) * bsf_stride + kScaleAtomBytes;
     hsf = o = up(o, 16);   o += 2 * kc2 * kScaleAtomBytes;
     table = o = up(o, 16); o += 2 * (kMaxGrid + 1) * 4;
-    bars = o = up(o, 16);  o += (3 * slots + 2 * sets + 4 + kMmaWarps + kCopiers) * 8;
+    // full, empty (+ the grid kernel's scaled) per slot, accfull/accempty per
+    // set, hfull/hempty, drained per issuer (+ per copier).
+    bars = o = up(o, 16);  o += ((grid ? 3 : 2) * slots + 2 * sets + 4 + kMmaWarps + (grid ? kCopiers : 0)) * 8;
     meta = o = up(o, 16);  o += sets * 16;
     misc = o = up(o, 16);  o += 16;
-    rows = o = up(o, 16);  o += kRowCache * (12 + unit_rows * 2);
+    rows = o = up(o, 16);  o += kRowCache * ((grid ? 12 : 8) + unit_rows * 2);
     agree = o = up(o, 16); o += kAgreeSlots * 4;
+    units = o = up(o, 16); o += grid ? (unit_rows == 8 ? kUnitCache8 : kUnitCache16) * 4 : 0;
     bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }
   __host__ __device__ bool aligned() const {
     return w % 1024 == 0 && act % 1024 == 0 && hcodes % 1024 == 0 && asf % 16 == 0 &&
            out % 16 == 0 && bsf % 16 == 0 && hsf % 16 == 0 && table % 16 == 0 && bars % 16 == 0 &&
-           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0 && agree % 16 == 0;
+           meta % 16 == 0 && misc % 16 == 0 && rows % 16 == 0 && agree % 16 == 0 && units % 16 == 0;
   }
 };
 
