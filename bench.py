@@ -3,8 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config tp8_b1] [--no-extra]
 
-A step is one moe_run call (MXFP8 quantize + grouping + persistent experts
-kernel + BF16 epilogue) over one batch. Metric: microseconds per call and
+A step is one moe_run call over one batch. A call of one or two tokens is
+one launch of the small-batch experts kernel (MXFP8 quantize, grouping, FC1,
+FC2, BF16 rows); any other call is the prep grid (quantize + grouping) and
+the persistent grid experts kernel. Metric: microseconds per call and
 touched-weight HBM GB/s. The main workload is the TP8 shard at B = 1
 (E = 384, H = 3584, I = 384, uniform distinct top-16 ids); the TP16 B = 8,
 TP8 B = 64 (Zipf 1.1) and TP8 B = 256 (Zipf 1.1, 1% x50 rows) workloads are
@@ -13,19 +15,19 @@ reported under "configs". Inputs are synthetic and seeded (workload/).
 L2: every call reads a different replica of the weights (R replicas, each a
 separate moe_prepare of the same weights) with (R - 1) x touched bytes >= 3 x
 L2, so no call finds its weights in the 126 MiB L2. The K timed calls are
-replayed from a CUDA graph (no host launch gaps), bracketed by a barrier and
-a device synchronize, timed with CUDA events.
+replayed from one CUDA graph (K <= 256; beyond, graphs of whole rounds over
+the replicas), queued behind a spin kernel so that the host's launch of the
+graph stays out of the timed region, bracketed by a barrier and a device
+synchronize, and timed with CUDA events.
 
-Roofline: the experts kernel's own time inside the step. A second pass replays
-the same K calls from a graph captured with the handles' launch clock on
-(moe_debug_kernel_span): every launch records, on the device, the span from
-its first CTA's start to its last CTA's end, and kernel_us is the mean span.
-The launch overlaps the prep grid (programmatic dependent launch), so the span
-starts while the prep grid still runs. The experts kernel timed alone (CUDA
-events around moe_experts after separate moe_quantize + moe_group launches)
-is kept as kernel_us_isolated. At one or two tokens the experts kernel is the
-cluster variant (one thread-block cluster per unit), otherwise the persistent
-grid kernel.
+Roofline: the experts kernel's own time per call (kernel_us). When a call is
+one launch, consecutive launches overlap (programmatic dependent launch), so
+its time per call is the timed per-call time; its launch-clock span (first
+CTA start to last CTA end, moe_debug_kernel_span) includes waiting for the
+previous launch and is kept as kernel_span_us. Otherwise kernel_us is that
+span for the experts kernel inside the step. kernel_us_isolated: CUDA events
+around moe_experts alone (the grid kernel, after separate moe_quantize and
+moe_group launches).
 
 Parity: the CPU-baseline leg runs the float64 oracle on the main workload;
 the same run compares one GPU call against it (activation plan and unit
@@ -67,7 +69,7 @@ import workload  # noqa: E402
 MAIN_CONFIG = "tp8_b1"
 EXTRA_CONFIGS = ["tp16_b8", "tp8_b64", "tp8_b256"]
 L2_FALLBACK_BYTES = 126 * 2 ** 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "cluster_kernel_tp8_b1.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "small_kernel_tp8_b1.md")
 KERNEL_SOURCES = ["experts.cu", "small.cu", "pipeline.cuh", "ptx.cuh", "common.cuh", "kernels.h"]
 
 
@@ -395,10 +397,14 @@ class OurArm:
         return g
 
     def time_graphs(self, plan, calls):
-        """Replay [(graph, times), ...] between two CUDA events; ms per call."""
+        """Replay [(graph, times), ...] between two CUDA events; ms per call.
+        A 100 us spin kernel goes first, so the start event and the graph
+        launches are queued on a busy GPU: the timed region holds the calls'
+        device work, not the host's launch of the first graph."""
         torch = self.torch
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        torch.cuda._sleep(200_000)
         start.record()
         for g, times in plan:
             for _ in range(times):
@@ -417,13 +423,16 @@ class OurArm:
         handle, B = self.layers[0].handle, self.cfg.batch
         path = self.moe.moe_kernel_path(handle, B)
         if path == self.moe.PATH_SMALL:
-            return ("small_kernel (one CTA per SM; unit table derived from the routing ids in the "
-                    "kernel; FC1 partial sums summed by every FC2 CTA; tcgen05 block-scaled MMA)")
+            return ("small_kernel (the whole call in one launch, one CTA per SM: MXFP8 quantize and "
+                    "unit table in the kernel; FC1 partial sums summed by every FC2 CTA; tcgen05 "
+                    "block-scaled MMA)")
         if path == self.moe.PATH_CLUSTER:
             C = self.moe.moe_cluster_size(handle, B)
             return (f"cluster_kernel (experts kernel on thread-block clusters of {C} CTAs, "
                     "one per unit; tcgen05 block-scaled MMA)")
-        return "experts_kernel (persistent, tcgen05 block-scaled MMA)"
+        rows = 16 if B > 8 else 8
+        return (f"experts_kernel<{rows}> (persistent, {rows}-row units, tcgen05 block-scaled MMA "
+                f"N = {rows}, two scale-copy warps)")
 
     def experts_kernel_ms(self, calls):
         """Mean device time of the experts kernel alone: moe_quantize and
@@ -497,10 +506,14 @@ def run_ours(args, rank, world, local):
         arm.call(i)
     arm.check_status()
 
-    # Exactly K timed calls: a graph of c calls (a multiple of R) replayed
-    # K // c times, then a graph of the K % c remaining calls.
+    # Exactly K timed calls. Up to 256: one graph of the K calls (rotating
+    # over the R replicas), replayed once. Beyond: a graph of c calls (a
+    # multiple of R) replayed K // c times, then a graph of the K % c rest.
     steps = max(1, args.steps)
-    calls_per_graph = max(arm.R, min(steps, 256) // arm.R * arm.R)
+    if steps <= 256:
+        calls_per_graph = steps
+    else:
+        calls_per_graph = max(arm.R, 256 // arm.R * arm.R)
     replays = steps // calls_per_graph
     g = arm.graph(calls_per_graph)
     tail = arm.graph(steps - replays * calls_per_graph) if steps % calls_per_graph else None
@@ -524,8 +537,10 @@ def run_ours(args, rank, world, local):
     clocks = sampler.summary(t_warm, t1)
     ms_per_call = max_over_ranks(ms_per_call, world, device)
 
+    # The launch clock pass: a graph of whole rounds over the R replicas.
+    span_calls = max(arm.R, min(steps, 256) // arm.R * arm.R)
     span_us, span_pass_ms, span_samples = arm.kernel_span_us(max(4, min(40, replays * 4)),
-                                                              calls_per_graph)
+                                                              span_calls)
     arm.check_status()
     kernel_ms = arm.experts_kernel_ms(min(200, max(20, args.steps // 10)))
     arm.check_status()
@@ -586,7 +601,7 @@ def run_ours(args, rank, world, local):
                 if single_launch else "") +
                 "in-step span of the experts kernel (first CTA start to last CTA end, device "
                 f"clock): mean {span_us:.3f} us over {span_samples} launches inside replays of a "
-                f"graph of {calls_per_graph} back-to-back calls with the launch clock on "
+                f"graph of {span_calls} back-to-back calls with the launch clock on "
                 f"({span_pass_ms * 1e3:.3f} us/call in those replays)",
             "kernel_span_us": round(span_us, 3),
             "kernel_us_isolated": round(kernel_ms * 1e3, 3),
