@@ -731,14 +731,14 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
           out_unit = u;
         }
         if (out_valid <= 2) {
-          // Few rows: each thread stores its two values of each row directly
-          // (a warp writes 64 contiguous bytes per row and tile).
+          // Few rows: no staging; each warp writes its 32 outputs of each row
+          // and tile as four 16-byte stores.
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= out_valid) break;
-            uint16_t* dst = a.out + static_cast<size_t>(unit_row(u, t)) * g.H + qq * 2 * kTileM;
-            dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
-            dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
+            uint16_t* dst = a.out + static_cast<size_t>(unit_row(u, t)) * g.H + qq * 2 * kTileM + q * 32;
+            store_row32_bf16(dst, v0[t], lane);
+            store_row32_bf16(dst + kTileM, v1[t], lane);
           }
           if (et == 0) MOE_STAMP(12);
           continue;
@@ -1284,9 +1284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kClusterMaxRows; ++t) {
           if (t >= valid) break;
-          uint16_t* dst = a.out + static_cast<size_t>(rows[t]) * g.H + qq * 2 * kTileM;
-          dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
-          dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
+          // Each warp writes its 32 outputs of each tile as four 16-byte stores.
+          uint16_t* dst = a.out + static_cast<size_t>(rows[t]) * g.H + qq * 2 * kTileM + q * 32;
+          store_row32_bf16(dst, v0[t], lane);
+          store_row32_bf16(dst + kTileM, v1[t], lane);
         }
         if (et == 0) MOE_STAMP(12);
       }

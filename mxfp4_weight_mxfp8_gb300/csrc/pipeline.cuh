@@ -224,6 +224,20 @@ __device__ __forceinline__ float warp_amax(float v) {
   return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
 }
 
+// One output row segment of a warp: lane l holds the value of column l of
+// 32 consecutive BF16 outputs at `dst` (16-byte aligned). Adjacent lanes pair
+// their values into 32-bit words, and lane 8j gathers the words of lanes 8j,
+// 8j + 2, 8j + 4, 8j + 6 and stores columns 8j .. 8j + 7 as one 16-byte store.
+// Every lane of the warp must call it.
+__device__ __forceinline__ void store_row32_bf16(uint16_t* dst, float v, int lane) {
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  const uint32_t pair = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 16);
+  const uint32_t w1 = __shfl_down_sync(0xFFFFFFFFu, pair, 2);
+  const uint32_t w2 = __shfl_down_sync(0xFFFFFFFFu, pair, 4);
+  const uint32_t w3 = __shfl_down_sync(0xFFFFFFFFu, pair, 6);
+  if ((lane & 7) == 0) *reinterpret_cast<uint4*>(dst + lane) = make_uint4(pair, w1, w2, w3);
+}
+
 __device__ __forceinline__ float silu_times(float gate, float up) {
   return gate / (1.0f + expf(-gate)) * up;
 }

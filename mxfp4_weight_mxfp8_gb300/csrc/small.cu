@@ -767,9 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= valid) break;
-          uint16_t* dst = a.out + static_cast<size_t>(su->row[u][t]) * g.H + qq * 2 * kTileM;
-          dst[m] = __bfloat16_as_ushort(__float2bfloat16_rn(v0[t]));
-          dst[kTileM + m] = __bfloat16_as_ushort(__float2bfloat16_rn(v1[t]));
+          // Each warp writes its 32 outputs of each tile as four 16-byte stores.
+          uint16_t* dst = a.out + static_cast<size_t>(su->row[u][t]) * g.H + qq * 2 * kTileM + q * 32;
+          store_row32_bf16(dst, v0[t], lane);
+          store_row32_bf16(dst + kTileM, v1[t], lane);
         }
         if (et == 0) MOE_STAMP(12);
       }
