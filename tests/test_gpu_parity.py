@@ -179,11 +179,7 @@ def test_grouping_paths_at_the_small_batch_threshold(moe, batch):
 
 
 def oracle_pairs_for(name, weights, x, ids):
-    if name == "tp8_b256":  # every pair of 64 tokens, including the x50 outlier rows
-        outliers = np.flatnonzero(np.abs(bf16_to_float(x)).max(axis=1) > 20)
-        rng = np.random.default_rng(0)
-        tokens = np.unique(np.concatenate([outliers, rng.choice(x.shape[0], 64, replace=False)]))
-        return (tokens[:, None] * 16 + np.arange(16)).reshape(-1).astype(np.int32)
+    """Every pair of the call (TP8 B256: 4,096 pairs, about 15 s of oracle time)."""
     return np.arange(ids.size, dtype=np.int32)
 
 
