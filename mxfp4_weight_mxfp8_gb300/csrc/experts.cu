@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
           if (!(ok = acquire(set))) break;
           first_c = cur.c;
         }
-        if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        // The scale barrier completes only after the copiers have seen the
+        // slot's full barrier (weights and activations landed): one wait.
         if (!(ok = wait_bar(cx, &scaled[slot], phase))) break;
         if (lead && n == 0) MOE_STAMP(4);
         fence_proxy_async_shared();  // the gathered activations were cp.async (generic) writes
@@ -303,8 +304,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         if (!(ok = acquire(set))) break;
         bool started = false;
         for (int c = 0; c < g.KC2 && ok; ++c) {
-          if (!(ok = wait_bar(cx, &full[slot], phase))) break;
-          if (!(ok = wait_bar(cx, &scaled[slot], phase))) break;
+          if (!(ok = wait_bar(cx, &scaled[slot], phase))) break;  // implies full (see FC1)
           if (lead && !fc2_seen) {
             MOE_STAMP(10);
             fc2_seen = true;
@@ -355,7 +355,9 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
     // ----------------------------------------------------------- scale copies
     // Copier 0 copies tile 0's weight scales and (FC1) the activation scales
     // of every stage, copier 1 tile 1's, into the slot's TMEM columns, and
-    // each commits to the slot's `scaled` barrier, which the issuers wait on.
+    // each commits to the slot's `scaled` barrier, which the issuers wait on
+    // in place of the full barrier: the copiers wait on that one first, so a
+    // completed `scaled` phase is ordered after the stage's data landed.
     // The slot is refilled only after the issuers' MMAs (which waited on
     // these copies) are done, so the columns are free again by then.
     if (lane == 0) {
