@@ -58,7 +58,8 @@ struct ExpertsArgs {
   uint64_t* span;             // or null: launch clock, [CTA][start, end] (moe_debug_kernel_span)
   // Small-batch kernel only (the call is that one launch):
   const uint16_t* x;          // BF16 [B, H]: quantized to MXFP8 in the kernel
-  uint32_t* cflags;           // [kMaxGrid][2][4] per-consumer piece counts, zero between calls
+  uint32_t* piece_sums;       // [kMaxGrid][4 pieces][kSmallPieceWords]: FC1 partial sums, sentinel at rest
+  uint32_t* piece_readers;    // [kMaxGrid][4 pieces]: consumers that read the piece, zero at rest
   uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
 };
@@ -92,7 +93,14 @@ int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serve
 bool small_fits(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
-constexpr size_t kSmallFlagBytes = static_cast<size_t>(kMaxGrid) * 2 * 4 * 4;  // ExpertsArgs::cflags
+// The small-batch kernel's FC1 piece slots: gate and up FP32 sums of up to
+// two token rows per 128-row tile, and a read count per slot. A slot holds
+// kPieceSentinel in every word between calls (no finite or canonical-NaN
+// FP32 sum has this pattern), so a consumer polls the sums themselves.
+constexpr int kSmallPieceWords = 2 * 2 * 128;
+constexpr uint32_t kPieceSentinel = 0xFFFFFFFFu;
+constexpr size_t kSmallPieceBytes = static_cast<size_t>(kMaxGrid) * 4 * kSmallPieceWords * 4;
+constexpr size_t kSmallReaderBytes = static_cast<size_t>(kMaxGrid) * 4 * 4;
 
 // Routing-weighted combine of each token's 16 rows (after the experts kernel).
 struct CombineArgs {

@@ -43,7 +43,8 @@ struct moe_ctx {
   int path = moe::kPathSmall;  // which experts kernel one- and two-token calls run on
   int small_ok[3] = {0, 0, 0};  // [batch]: the small-batch kernel's split fits this layer
   uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
-  uint32_t* cflags = nullptr;  // small-batch kernel: per-consumer piece counts (zero at rest)
+  uint32_t* piece_sums = nullptr;     // small-batch kernel: FC1 piece slots (sentinel at rest)
+  uint32_t* piece_readers = nullptr;  // small-batch kernel: read counts per slot (zero at rest)
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
@@ -210,11 +211,12 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
       static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8,           // launch clock
-      moe::kSmallFlagBytes,                                     // small-batch piece counts
+      moe::kSmallReaderBytes,                                   // small-batch read counts
       static_cast<size_t>(h->unit_cap) * 4,                     // pairs of units
+      moe::kSmallPieceBytes,                                    // small-batch piece slots
   };
-  size_t offsets[15], total = 0;
-  for (int i = 0; i < 15; ++i) {
+  size_t offsets[16], total = 0;
+  for (int i = 0; i < 16; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -235,8 +237,10 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->pair_kept = w + offsets[10];
   h->staged = reinterpret_cast<uint16_t*>(w + offsets[11]);
   h->span = reinterpret_cast<uint64_t*>(w + offsets[12]);
-  h->cflags = reinterpret_cast<uint32_t*>(w + offsets[13]);
+  h->piece_readers = reinterpret_cast<uint32_t*>(w + offsets[13]);
   h->wide_units = reinterpret_cast<uint32_t*>(w + offsets[14]);
+  h->piece_sums = reinterpret_cast<uint32_t*>(w + offsets[15]);
+  MOE_CUDA(cudaMemset(h->piece_sums, 0xFF, moe::kSmallPieceBytes));  // every word the sentinel
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
   return encode_weight_map(h);
@@ -324,7 +328,8 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.span = h->span_on ? h->span : nullptr;
   a.trace = h->trace;
   a.x = static_cast<const uint16_t*>(x);
-  a.cflags = h->cflags;
+  a.piece_sums = h->piece_sums;
+  a.piece_readers = h->piece_readers;
   a.pair_kept = h->pair_kept;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
   return MOE_OK;
@@ -478,9 +483,11 @@ int moe_sync_status(moe_handle h, void* stream) {
   MOE_CUDA(cudaStreamSynchronize(s));
   const int status = *h->status_host;
   if (status == MOE_ERR_DEVICE_TIMEOUT) {
-    // A bounded wait ran out, so some piece counts of the small-batch kernel
-    // may not have been consumed (and set back to zero): clear them.
-    MOE_CUDA(cudaMemsetAsync(h->cflags, 0, moe::kSmallFlagBytes, s));
+    // A bounded wait ran out, so some piece slots of the small-batch kernel
+    // may not have been read by all their consumers (and put back to rest):
+    // reset them.
+    MOE_CUDA(cudaMemsetAsync(h->piece_readers, 0, moe::kSmallReaderBytes, s));
+    MOE_CUDA(cudaMemsetAsync(h->piece_sums, 0xFF, moe::kSmallPieceBytes, s));
     MOE_CUDA(cudaStreamSynchronize(s));
   }
   return status;
@@ -768,6 +775,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
     return MOE_ERR_ARG;
   const Geometry& g = h->g;
   const int cap = moe::unit_capacity(batch, g.E);
+  const bool small = small_call(h, batch);
   const size_t sizes[] = {
       static_cast<size_t>(batch) * g.H,                            // plan codes
       static_cast<size_t>(batch) * (g.H / moe::kBlock),            // plan scales
@@ -778,11 +786,12 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
       static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
       static_cast<size_t>(h->grid) * 2 * 2 * (batch > moe::kUnitRows ? 16 : 8) * moe::kTileM * 4,  // partials
       static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
-      moe::kSmallFlagBytes,                                        // small-batch piece counts
+      small ? moe::kSmallReaderBytes : 0,                          // small-batch read counts
       static_cast<size_t>(cap) * 4,                                // pairs of units
+      small ? moe::kSmallPieceBytes : 0,                           // small-batch piece slots
   };
-  size_t offsets[11], total = 0;
-  for (int i = 0; i < 11; ++i) {
+  size_t offsets[12], total = 0;
+  for (int i = 0; i < 12; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -799,10 +808,9 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   if (rc != MOE_OK) return rc;
 
   // The grouping block of the prep kernel clears the counters and flags the
-  // grid kernel needs at zero; the small-batch kernel's piece counts are
-  // cleared below. Every other scratch byte is written before it is read
-  // within the call, so nothing is left over from the last call.
-  const bool small = small_call(h, batch);
+  // grid kernel needs at zero; the small-batch kernel's piece slots and read
+  // counts are put to rest below. Every other scratch byte is written before
+  // it is read within the call, so nothing is left over from the last call.
   moe::PrepArgs pa = prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup);
   pa.unit_cap = cap;
   pa.plan_codes = w + offsets[0];
@@ -815,11 +823,14 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
   pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t* cflags = reinterpret_cast<uint32_t*>(w + offsets[9]);
-  if (small)
-    MOE_CUDA(cudaMemsetAsync(cflags, 0, moe::kSmallFlagBytes, s));  // a memset, not an allocation
-  else
+  uint32_t* piece_readers = reinterpret_cast<uint32_t*>(w + offsets[9]);
+  uint32_t* piece_sums = reinterpret_cast<uint32_t*>(w + offsets[11]);
+  if (small) {  // memsets, not allocations
+    MOE_CUDA(cudaMemsetAsync(piece_readers, 0, moe::kSmallReaderBytes, s));
+    MOE_CUDA(cudaMemsetAsync(piece_sums, 0xFF, moe::kSmallPieceBytes, s));
+  } else {
     MOE_CUDA(moe::launch_prep(pa, s));
+  }
 
   moe::ExpertsArgs ea{};
   ea.wmap = h->wmap;
@@ -844,7 +855,8 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   ea.withhold_image = -1;
   if (small) {
     ea.x = static_cast<const uint16_t*>(x_bf16);
-    ea.cflags = cflags;
+    ea.piece_sums = piece_sums;
+    ea.piece_readers = piece_readers;
     ea.pair_kept = nullptr;
   }
   MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->path, small));

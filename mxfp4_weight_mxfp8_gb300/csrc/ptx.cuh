@@ -226,6 +226,23 @@ __device__ __forceinline__ uint32_t load_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
+// A load that every poll re-issues (relaxed, GPU scope: sees other SMs'
+// stores once they reach L2). No memory clobber: the polled word is its own
+// flag, so other accesses may move around it and several stay in flight.
+__device__ __forceinline__ uint32_t load_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Fetch-and-add with acquire-release semantics at GPU scope: the caller's
+// earlier accesses are ordered before it, later ones after it.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void store_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -58,7 +58,6 @@ struct SmallUnits {
 // start, off the critical path.
 struct SmallPieces {
   int n;
-  uint32_t want[4];  // pieces per item: the count its counter reaches
   int entry[kSmallUnitPieces];
 };
 
@@ -135,6 +134,21 @@ __device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], const int (&
     *reinterpret_cast<uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4) = codes;
     if ((lane & 7) == 0) atom[scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
   }
+}
+
+// The CTAs that run FC2 jobs of unit u (those holding jobs u * NQ ..
+// u * NQ + NQ - 1 with a non-empty range): every one of them reads every
+// FC1 piece of the unit.
+__device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g, int u, int G) {
+  const uint32_t J = static_cast<uint32_t>(sp.J), GG = static_cast<uint32_t>(G);
+  auto job_owner = [&](int j) {  // the largest c with floor(c * J / G) <= j
+    const int c = static_cast<int>((static_cast<uint32_t>(j + 1) * GG - 1u) / J);
+    return c < G - 1 ? c : G - 1;
+  };
+  int n = 0;
+  for (int k = job_owner(u * g.NQ); k <= job_owner(u * g.NQ + g.NQ - 1); ++k)
+    n += sp.fc2_begin(k + 1) > sp.fc2_begin(k);
+  return n;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ ExpertsArgs a) {
@@ -488,7 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     const int B = a.B;
-    const int piece_floats = 2 * B * kTileM;      // [tile][token row][128]
     // FC1 pieces this CTA holds: one per item its range touches.
     const int first_item = f0 / g.KC1;
     const int pieces = f1 > f0 ? (f1 - 1) / g.KC1 - first_item + 1 : 0;
@@ -556,15 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         for (int p = 0; p < g.P1; ++p) {
           const int item = u * g.P1 + p, s0 = item * g.KC1;
           const int lo = owner(s0), hi = owner(s0 + g.KC1 - 1);
-          uint32_t want = 0;
           for (int c = lo; c <= hi; ++c) {
             const uint32_t e0 = span_tbl[c], e1 = span_tbl[c + 1];
-            if ((e1 & 0xFFFFu) > (e0 & 0xFFFFu) && n < kSmallUnitPieces) {
+            if ((e1 & 0xFFFFu) > (e0 & 0xFFFFu) && n < kSmallUnitPieces)
               P.entry[n++] = (p << 16) | (c * kSmallPieces + (item - static_cast<int>(e0 >> 16)));
-              ++want;
-            }
           }
-          P.want[p] = want;
         }
         P.n = n;
       }
@@ -573,9 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     epilogue_sync();
 
     // The hidden image of each FC2 unit, built once this CTA's FC1 pieces are
-    // out: one thread per item polls its counter (acquire, with a short
-    // back-off) and the epilogue barrier passes that order on to every thread.
-    // Every piece's loads go out together (16 at a time), and each item's
+    // out. The partial-sum slots hold a sentinel (a NaN pattern no sum is
+    // stored as) until their piece lands, so the sums are their own flags:
+    // every piece's loads go out together (16 at a time), and each item's
     // pieces are summed in CTA order: the masked-out terms add -0.0, which
     // leaves every sum (a zero's sign included) unchanged.
     bool built = j1 <= j0;
@@ -593,23 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           const int valid = su->valid[u];
           uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
           uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
-          if (et < g.P1) {
-            // This CTA's own count of the item's pieces; set back to zero
-            // for the next call (whose pieces count only after this launch
-            // has ended).
-            uint32_t* counter = a.cflags + (cta * kSmallHidden + ordinal) * 4 + et;
-            const uint32_t want = P.want[et];
-            const uint64_t t_wait = global_timer_ns();
-            for (uint32_t i = 0; load_acquire_gpu(counter) < want; ++i) {
-              __nanosleep(64);
-              if ((i & 15u) == 15u && global_timer_ns() - t_wait > a.timeout_ns) {
-                report(a.status, MOE_ERR_DEVICE_TIMEOUT);
-                break;
-              }
-            }
-            *reinterpret_cast<volatile uint32_t*>(counter) = 0u;
-          }
-          epilogue_sync();
           if (et == 0) MOE_STAMP(7);
 #ifdef MOE_TRACE
           const long long c_start = clock64();
@@ -620,20 +612,48 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           for (int p = 0; p < 4; ++p)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[p][r] = -0.0f;
+          // Each thread polls exactly the sums it adds up (rows m of every
+          // piece): 16 pieces' loads in flight, then the sentinels among
+          // them re-loaded until every sum has landed (bounded).
+          const uint64_t t_wait = global_timer_ns();
           for (int e0 = 0; e0 < P.n; e0 += 16) {
-            float v[16][4];
+            uint32_t v[16][4];
             int pit[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int e = e0 + i;
               const int entry = e < P.n ? P.entry[e] : -1;
               pit[i] = entry >> 16;  // -1 past the end
-              const float* src = a.partials + static_cast<size_t>(entry < 0 ? 0 : (entry & 0xFFFF)) * piece_floats;
+              const uint32_t* src = a.piece_sums + static_cast<size_t>(entry < 0 ? 0 : (entry & 0xFFFF)) * kSmallPieceWords;
 #pragma unroll
               for (int t = 0; t < 2; ++t) {
                 const bool ld = entry >= 0 && t < valid;
-                v[i][t] = ld ? __ldcg(src + t * kTileM + m) : -0.0f;
-                v[i][2 + t] = ld ? __ldcg(src + (B + t) * kTileM + m) : -0.0f;
+                v[i][t] = ld ? load_relaxed_gpu(src + t * kTileM + m) : 0x80000000u;
+                v[i][2 + t] = ld ? load_relaxed_gpu(src + (B + t) * kTileM + m) : 0x80000000u;
+              }
+            }
+            for (uint32_t poll = 0;; ++poll) {
+              bool missing = false;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int entry = e0 + i < P.n ? P.entry[e0 + i] : -1;
+                const uint32_t* src = a.piece_sums + static_cast<size_t>(entry < 0 ? 0 : (entry & 0xFFFF)) * kSmallPieceWords;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  if (v[i][t] == kPieceSentinel) {
+                    missing = true;
+                    v[i][t] = load_relaxed_gpu(src + t * kTileM + m);
+                  }
+                  if (v[i][2 + t] == kPieceSentinel) {
+                    missing = true;
+                    v[i][2 + t] = load_relaxed_gpu(src + (B + t) * kTileM + m);
+                  }
+                }
+              }
+              if (!missing) break;
+              if ((poll & 7u) == 7u && global_timer_ns() - t_wait > a.timeout_ns) {
+                report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                break;  // go on with whatever landed
               }
             }
 #pragma unroll
@@ -641,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
               for (int p = 0; p < 4; ++p)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) acc[p][r] += pit[i] == p ? v[i][r] : -0.0f;
+                for (int r = 0; r < 4; ++r) acc[p][r] += pit[i] == p ? __uint_as_float(v[i][r]) : -0.0f;
           }
 #ifdef MOE_TRACE
           {
@@ -686,6 +706,20 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
               reinterpret_cast<uint4*>(img)[i] =
                   i < n_codes ? reinterpret_cast<const uint4*>(hc)[i]
                               : reinterpret_cast<const uint4*>(hs)[i - n_codes];
+          }
+          // This CTA has read every piece of the unit: count it per piece. The
+          // unit's last consumer puts the sentinels back and clears the count,
+          // so each slot is empty again for the next call (whose pieces are
+          // stored only after this launch has ended).
+          const int readers = unit_consumers(sp, g, u, G);
+          for (int e = et; e < P.n; e += 128) {
+            const int slot_index = P.entry[e] & 0xFFFF;
+            if (atom_add_acq_rel_gpu(a.piece_readers + slot_index, 1u) + 1u == static_cast<uint32_t>(readers)) {
+              uint4* sums = reinterpret_cast<uint4*>(a.piece_sums + static_cast<size_t>(slot_index) * kSmallPieceWords);
+              for (int i = 0; i < kSmallPieceWords / 4; ++i)
+                sums[i] = make_uint4(kPieceSentinel, kPieceSentinel, kPieceSentinel, kPieceSentinel);
+              a.piece_readers[slot_index] = 0u;
+            }
           }
         }
       }
@@ -734,29 +768,17 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         // ---- FC1 piece: gate = v0, up = v1 for rows 128p + m -> partial sums.
         const int item = md.y, u = item / g.P1;
         const int valid = su->valid[u];
-        float* dst = a.partials + static_cast<size_t>(cta * kSmallPieces + (item - first_item)) * piece_floats;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= valid) break;
-          dst[t * kTileM + m] = v0[t];
-          dst[(B + t) * kTileM + m] = v1[t];
-        }
-        epilogue_sync();
-        // One count per CTA that runs FC2 jobs of the unit (the CTAs holding
-        // jobs u * NQ .. u * NQ + NQ - 1), each released by its own thread.
+        // The piece's sums go straight into its slot, which the unit's
+        // consumers poll; a sum with the sentinel's bit pattern (a NaN) is
+        // stored as the canonical NaN.
         if (u != a.withhold_unit) {
-          const uint32_t J = static_cast<uint32_t>(sp.J), GG = static_cast<uint32_t>(G);
-          auto job_owner = [&](int j) {  // the largest c with floor(c * J / G) <= j
-            const int c = static_cast<int>((static_cast<uint32_t>(j + 1) * GG - 1u) / J);
-            return c < G - 1 ? c : G - 1;
-          };
-          const int k = job_owner(u * g.NQ) + et;
-          if (k <= job_owner(u * g.NQ + g.NQ - 1)) {
-            const int kb = sp.fc2_begin(k), ke = sp.fc2_begin(k + 1);
-            if (ke > kb) {
-              const int ordinal = kb / g.NQ == u ? 0 : 1;
-              red_release_add_gpu(a.cflags + (k * kSmallHidden + ordinal) * 4 + (item - u * g.P1), 1u);
-            }
+          uint32_t* dst = a.piece_sums + static_cast<size_t>(cta * kSmallPieces + (item - first_item)) * kSmallPieceWords;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= valid) break;
+            const uint32_t gb = __float_as_uint(v0[t]), ub = __float_as_uint(v1[t]);
+            dst[t * kTileM + m] = gb == kPieceSentinel ? 0x7FFFFFFFu : gb;
+            dst[(B + t) * kTileM + m] = ub == kPieceSentinel ? 0x7FFFFFFFu : ub;
           }
         }
         ++done;
