@@ -58,10 +58,13 @@ struct ExpertsArgs {
   uint64_t* span;             // or null: launch clock, [CTA][start, end] (moe_debug_kernel_span)
   // Small-batch kernel only (the call is that one launch):
   const uint16_t* x;          // BF16 [B, H]: quantized to MXFP8 in the kernel
-  uint32_t* piece_sums;       // [kMaxGrid][4 pieces][kSmallPieceWords]: FC1 partial sums, sentinel at rest
-  uint32_t* piece_readers;    // [kMaxGrid][4 pieces]: consumers that read the piece, zero at rest
+  uint32_t* piece_sums;       // [2 parities][seg_cap][kSmallPieceWords]: FC1 segment sums, sentinel at rest
+  uint32_t* piece_readers;    // [2][seg_cap]: consumers that read the segment, zero at rest
+  uint32_t* small_counters;   // [2][4]: segments claimed, CTAs finished (zero at rest)
   uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
+  int seg_cap;                // segment slots per parity
+  int parity;                 // which half of the slots and counters this call uses
 };
 
 int experts_smem_bytes(const Geometry& g, int unit_rows = 8);
@@ -93,14 +96,20 @@ int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serve
 bool small_fits(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
-// The small-batch kernel's FC1 piece slots: gate and up FP32 sums of up to
-// two token rows per 128-row tile, and a read count per slot. A slot holds
-// kPieceSentinel in every word between calls (no finite or canonical-NaN
-// FP32 sum has this pattern), so a consumer polls the sums themselves.
+// The small-batch kernel's FC1 segment slots: gate and up FP32 sums of up to
+// two token rows per 128-row tile (one segment: a run of kSegChunks K chunks
+// of one item), and a read count per slot, in two halves that consecutive
+// calls alternate. A slot holds kPieceSentinel in every word between uses (no
+// finite or canonical-NaN FP32 sum has this pattern), so a consumer polls the
+// sums themselves.
 constexpr int kSmallPieceWords = 2 * 2 * 128;
 constexpr uint32_t kPieceSentinel = 0xFFFFFFFFu;
-constexpr size_t kSmallPieceBytes = static_cast<size_t>(kMaxGrid) * 4 * kSmallPieceWords * 4;
-constexpr size_t kSmallReaderBytes = static_cast<size_t>(kMaxGrid) * 4 * 4;
+constexpr int kSegChunks = 4;
+// Segment slots per parity of a layer: 32 units of ceil(I / 128) items.
+inline int small_seg_cap(const Geometry& g) { return 2 * kTopK * g.P1 * ((g.KC1 + kSegChunks - 1) / kSegChunks); }
+inline size_t small_piece_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * kSmallPieceWords * 4; }
+inline size_t small_reader_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * 4; }
+constexpr size_t kSmallCounterBytes = 2 * 4 * 4;
 
 // Routing-weighted combine of each token's 16 rows (after the experts kernel).
 struct CombineArgs {

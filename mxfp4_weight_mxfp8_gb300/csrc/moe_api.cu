@@ -43,8 +43,10 @@ struct moe_ctx {
   int path = moe::kPathSmall;  // which experts kernel one- and two-token calls run on
   int small_ok[3] = {0, 0, 0};  // [batch]: the small-batch kernel's split fits this layer
   uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
-  uint32_t* piece_sums = nullptr;     // small-batch kernel: FC1 piece slots (sentinel at rest)
-  uint32_t* piece_readers = nullptr;  // small-batch kernel: read counts per slot (zero at rest)
+  uint32_t* piece_sums = nullptr;      // small-batch kernel: FC1 segment slots (sentinel at rest)
+  uint32_t* piece_readers = nullptr;   // small-batch kernel: read counts per slot (zero at rest)
+  uint32_t* small_counters = nullptr;  // small-batch kernel: segment claims, CTAs done (zero at rest)
+  int small_parity = 0;                // the half of the slots and counters the next call takes
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
@@ -211,12 +213,13 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK,            // kept pairs
       static_cast<size_t>(MOE_MAX_BATCH) * MOE_TOPK * g.H * 2,  // staged per-pair rows
       static_cast<size_t>(moe::kMaxSpanCtas) * 2 * 8,           // launch clock
-      moe::kSmallReaderBytes,                                   // small-batch read counts
+      moe::small_reader_bytes(g),                               // small-batch read counts
       static_cast<size_t>(h->unit_cap) * 4,                     // pairs of units
-      moe::kSmallPieceBytes,                                    // small-batch piece slots
+      moe::small_piece_bytes(g),                                // small-batch segment slots
+      moe::kSmallCounterBytes,                                  // small-batch claim counters
   };
-  size_t offsets[16], total = 0;
-  for (int i = 0; i < 16; ++i) {
+  size_t offsets[17], total = 0;
+  for (int i = 0; i < 17; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -240,7 +243,8 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->piece_readers = reinterpret_cast<uint32_t*>(w + offsets[13]);
   h->wide_units = reinterpret_cast<uint32_t*>(w + offsets[14]);
   h->piece_sums = reinterpret_cast<uint32_t*>(w + offsets[15]);
-  MOE_CUDA(cudaMemset(h->piece_sums, 0xFF, moe::kSmallPieceBytes));  // every word the sentinel
+  h->small_counters = reinterpret_cast<uint32_t*>(w + offsets[16]);
+  MOE_CUDA(cudaMemset(h->piece_sums, 0xFF, moe::small_piece_bytes(g)));  // every word the sentinel
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
   return encode_weight_map(h);
@@ -330,6 +334,12 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.x = static_cast<const uint16_t*>(x);
   a.piece_sums = h->piece_sums;
   a.piece_readers = h->piece_readers;
+  a.small_counters = h->small_counters;
+  a.seg_cap = moe::small_seg_cap(h->g);
+  // Consecutive calls take alternate halves of the small kernel's slots and
+  // counters (any other kernel ignores them).
+  a.parity = h->small_parity;
+  h->small_parity ^= 1;
   a.pair_kept = h->pair_kept;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
   return MOE_OK;
@@ -483,11 +493,12 @@ int moe_sync_status(moe_handle h, void* stream) {
   MOE_CUDA(cudaStreamSynchronize(s));
   const int status = *h->status_host;
   if (status == MOE_ERR_DEVICE_TIMEOUT) {
-    // A bounded wait ran out, so some piece slots of the small-batch kernel
-    // may not have been read by all their consumers (and put back to rest):
-    // reset them.
-    MOE_CUDA(cudaMemsetAsync(h->piece_readers, 0, moe::kSmallReaderBytes, s));
-    MOE_CUDA(cudaMemsetAsync(h->piece_sums, 0xFF, moe::kSmallPieceBytes, s));
+    // A bounded wait ran out, so some segment slots of the small-batch
+    // kernel may not have been read by all their consumers (and put back to
+    // rest), and its claim counters may not be back at zero: reset them.
+    MOE_CUDA(cudaMemsetAsync(h->piece_readers, 0, moe::small_reader_bytes(h->g), s));
+    MOE_CUDA(cudaMemsetAsync(h->piece_sums, 0xFF, moe::small_piece_bytes(h->g), s));
+    MOE_CUDA(cudaMemsetAsync(h->small_counters, 0, moe::kSmallCounterBytes, s));
     MOE_CUDA(cudaStreamSynchronize(s));
   }
   return status;
@@ -786,12 +797,13 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
       static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
       static_cast<size_t>(h->grid) * 2 * 2 * (batch > moe::kUnitRows ? 16 : 8) * moe::kTileM * 4,  // partials
       static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
-      small ? moe::kSmallReaderBytes : 0,                          // small-batch read counts
+      small ? moe::small_reader_bytes(g) / 2 : 0,                 // small-batch read counts (one half)
       static_cast<size_t>(cap) * 4,                                // pairs of units
-      small ? moe::kSmallPieceBytes : 0,                           // small-batch piece slots
+      small ? moe::small_piece_bytes(g) / 2 : 0,                  // small-batch segment slots (one half)
+      small ? moe::kSmallCounterBytes : 0,                         // small-batch claim counters
   };
-  size_t offsets[12], total = 0;
-  for (int i = 0; i < 12; ++i) {
+  size_t offsets[13], total = 0;
+  for (int i = 0; i < 13; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -825,9 +837,11 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* piece_readers = reinterpret_cast<uint32_t*>(w + offsets[9]);
   uint32_t* piece_sums = reinterpret_cast<uint32_t*>(w + offsets[11]);
-  if (small) {  // memsets, not allocations
-    MOE_CUDA(cudaMemsetAsync(piece_readers, 0, moe::kSmallReaderBytes, s));
-    MOE_CUDA(cudaMemsetAsync(piece_sums, 0xFF, moe::kSmallPieceBytes, s));
+  uint32_t* small_counters = reinterpret_cast<uint32_t*>(w + offsets[12]);
+  if (small) {  // memsets, not allocations; the call takes half 0 of the slots
+    MOE_CUDA(cudaMemsetAsync(piece_readers, 0, moe::small_reader_bytes(g) / 2, s));
+    MOE_CUDA(cudaMemsetAsync(piece_sums, 0xFF, moe::small_piece_bytes(g) / 2, s));
+    MOE_CUDA(cudaMemsetAsync(small_counters, 0, moe::kSmallCounterBytes, s));
   } else {
     MOE_CUDA(moe::launch_prep(pa, s));
   }
@@ -857,6 +871,9 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
     ea.x = static_cast<const uint16_t*>(x_bf16);
     ea.piece_sums = piece_sums;
     ea.piece_readers = piece_readers;
+    ea.small_counters = small_counters;
+    ea.seg_cap = moe::small_seg_cap(g);
+    ea.parity = 0;
     ea.pair_kept = nullptr;
   }
   MOE_CUDA(moe::launch_experts(ea, h->grid, s, true, h->path, small));

@@ -88,6 +88,12 @@ struct Split {
     const uint32_t cu = static_cast<uint32_t>(c);
     return static_cast<int>(cu * static_cast<uint32_t>(J) / static_cast<uint32_t>(G));
   }
+  // The CTA holding FC2 job j: the largest c < G with fc2_begin(c) <= j.
+  __host__ __device__ int job_owner(int j) const {
+    const int c = static_cast<int>((static_cast<uint32_t>(j + 1) * static_cast<uint32_t>(G) - 1u) /
+                                   static_cast<uint32_t>(J));
+    return c < G - 1 ? c : G - 1;
+  }
   __host__ __device__ int fc1_begin(int c) const {
     if (c >= G) return T1;
     const uint32_t cu = static_cast<uint32_t>(c);

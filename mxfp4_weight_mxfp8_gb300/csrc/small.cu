@@ -3,34 +3,46 @@
 // Pages: ...cutedsl.moe.experts (ExpertsKernel: the TMA producer warp, the
 // block-scaled FC1/FC2 tcgen05 stages, store_hidden, the hidden exchange
 // (ExpertsKernel.partials / load_hidden), fc2 output rows) and
-// ...cutedsl.moe.experts_runtime (PersistentExperts: one persistent grid).
+// ...cutedsl.moe.experts_runtime (PersistentExperts: one persistent grid;
+// `dynamic`: work claimed from a grid-wide counter because the CTAs' stream
+// rates differ by microseconds within a call; counters re-armed by call
+// parity).
 //
-// The persistent grid kernel's roles, ring, MMAs and work split (FC1 stages
-// and FC2 jobs each cut evenly over one CTA per SM), with two changes that
-// suit a call of at most 32 (token, slot) pairs:
+// The persistent grid kernel's roles, ring and MMAs, with these changes for a
+// call of at most 32 (token, slot) pairs:
 //   - A call on device buffers is this one launch: no prep grid runs before
 //     it (calls on host buffers keep the prep grid, which reads x once, and
-//     gather its plan). Every CTA
-//     derives the unit table from the routing ids itself (warp 0: one pair
-//     per lane; a unit per distinct kept expert, experts ascending, rows in
-//     token order: the canonical table), so the producer streams weights
-//     from the kernel's first microsecond, and the activation warp quantizes
-//     the x chunks it needs to MXFP8 itself. For read-back, CTA 0 writes the
-//     unit table and the kept-pair flags and CTA c the plan of K chunk c.
-//   - Consecutive launches overlap (programmatic dependent launch): each
-//     launch lets the next one start as its CTAs leave, and every role waits
-//     for the previous launch to end before it writes global memory that the
-//     previous launch reads or writes.
-//   - The FC1 -> FC2 hand-off takes one trip through L2 instead of two. Every
-//     piece of an FC1 item (a run of its K stages on one CTA) stores its FP32
-//     partial sums and release-increments one count per consumer of its
-//     unit; there is no owner. Every CTA that runs FC2 jobs of a unit polls
-//     its own counts of the unit's items (and sets them back to zero), sums
-//     the pieces itself in CTA order (so every consumer gets the same bits),
-//     applies SiLU(gate) * up and the MXFP8 requant, and writes the hidden
-//     image straight into its own shared memory.
+//     copy its plan). Every CTA derives the unit table from the routing ids
+//     itself (warp 0: one pair per lane; a unit per distinct kept expert,
+//     experts ascending, rows in token order: the canonical table), and five
+//     warps quantize x to MXFP8 once, into a shared-memory image per K chunk
+//     that holds every token of the call (the FC1 MMA computes all tokens for
+//     each expert; the epilogue keeps the unit's own columns). For
+//     read-back, CTA 0 writes the unit table and the kept-pair flags and CTA c
+//     the plan of K chunk c.
+//   - FC1 is cut into segments (kSegChunks K chunks of one item) that the
+//     CTAs claim from a counter as their producers get to them, so the CTAs
+//     that start first (consecutive launches overlap) take more of the work.
+//     FC2 jobs stay split evenly over the CTAs.
+//   - The FC1 -> FC2 hand-off takes one trip through L2. Each segment stores
+//     its FP32 partial sums into its own slot, whose words hold a sentinel
+//     until then; there is no owner and no count to wait for. Every CTA that
+//     runs FC2 jobs of a unit polls the sums of all the unit's segments, adds
+//     them in segment order (so every consumer gets the same bits), applies
+//     SiLU(gate) * up and the MXFP8 requant, and writes the hidden image
+//     straight into its own shared memory. The unit's last consumer puts the
+//     sentinels back.
+//   - Consecutive launches overlap (programmatic dependent launch). The claim
+//     counters and segment slots come in two halves that consecutive calls
+//     alternate (the host flips the parity per call), so a call's FC1 and
+//     hand-off need nothing from the previous call; every write of memory
+//     that the previous call reads or writes (the output rows, the read-back
+//     copies) waits for the previous call to end, and a CTA lets the next
+//     launch start only after that wait, so the call after next finds this
+//     call's half at rest.
 // The warp roles: warp 0 TMA producer, warps 1-4 MMA issuers, warp 5 the
-// activations (FC1), warps 6-9 the epilogue (FC1 partial sums; the hidden
+// activations (x quantization; the wait for the previous call; read-back),
+// warps 6-9 the epilogue (x quantization first; FC1 segment sums; the hidden
 // images of this CTA's FC2 units; BF16 output rows).
 #include "pipeline.cuh"
 
@@ -38,12 +50,25 @@ namespace moe {
 namespace {
 
 constexpr int kSmallMaxUnits = 2 * kTopK;  // distinct experts of two tokens
-constexpr int kSmallPieces = 4;            // FC1 pieces one CTA may hold (partials slots)
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
-constexpr int kSmallUnitPieces = 160;      // FC1 pieces of one unit (<= grid + 4)
+constexpr int kSmallSlots = 5;             // weight ring depth
+constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
+constexpr int kXPerWarp = 6;               // K chunks per x warp, at most (KC1 <= 30)
+constexpr int kXAtomStride = kUnitRows * 16;  // scale rows 0..7 of chunk c's atom (an N = 8 MMA reads no more)
+constexpr int kSmemLimit = 232448;         // dynamic shared memory one CTA may take
 
-// The unit table of the call, in shared memory (after the FC1 range-start
-// region of Layout::table, which this kernel does not use).
+// Stage descriptors, one per ring slot in shared memory: the producer writes
+// it before arriving on the slot's full barrier.
+constexpr uint32_t kDescSegMask = (1u << 19) - 1u;
+constexpr uint32_t kDescFirst = 1u << 27;  // the segment's first chunk: a fresh accumulator
+constexpr uint32_t kDescLast = 1u << 28;   // its last chunk: hand the accumulator to the epilogue
+constexpr uint32_t kDescEnd = 1u << 29;    // no data: this CTA's FC1 stages are over
+__device__ __forceinline__ uint32_t stage_desc(int seg, int c, bool first, bool last) {
+  return static_cast<uint32_t>(seg) | (static_cast<uint32_t>(c) << 19) | (first ? kDescFirst : 0u) |
+         (last ? kDescLast : 0u);
+}
+
+// The unit table of the call, in shared memory.
 struct SmallUnits {
   int count;
   int expert[kSmallMaxUnits];
@@ -53,12 +78,28 @@ struct SmallUnits {
   unsigned kept;                        // bit p: pair p got a unit row
 };
 
-// The FC1 pieces of one FC2 unit of this CTA, in item order and CTA order
-// within an item: (item of the unit) << 16 | partial-sum slot. Built at the
-// start, off the critical path.
-struct SmallPieces {
-  int n;
-  int entry[kSmallUnitPieces];
+// Shared-memory carve-up of the small kernel (images on 1024-byte boundaries).
+struct SmallLayout {
+  int w, xc, hcodes, xs, asf, hsf, table, bars, meta, desc, misc, agree, bytes;
+  __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
+  __host__ __device__ SmallLayout(int kc1, int kc2) {
+    int o = 0;
+    w = o;                    o += kSmallSlots * kStageSmemWeights;
+    xc = o = up(o, 1024);     o += kc1 * kActImageBytes;
+    hcodes = o = up(o, 1024); o += kSmallHidden * kc2 * kActImageBytes;
+    xs = o = up(o, 16);       o += kc1 * kXAtomStride + (kScaleAtomBytes - kXAtomStride);
+    asf = o = up(o, 16);      o += kSmallSlots * 2 * kScaleAtomBytes;
+    hsf = o = up(o, 16);      o += kSmallHidden * kc2 * kScaleAtomBytes;
+    table = o = up(o, 16);    o += static_cast<int>(sizeof(SmallUnits));
+    // full, empty per slot; accfull, accempty per set; hfull per unit;
+    // drained per issuer; x ready; previous call done.
+    bars = o = up(o, 16);     o += (2 * kSmallSlots + 2 * NACC + kSmallHidden + kMmaWarps + 2) * 8;
+    meta = o = up(o, 16);     o += NACC * 16;
+    desc = o = up(o, 16);     o += kSmallSlots * 4;
+    misc = o = up(o, 16);     o += 16;
+    agree = o = up(o, 16);    o += kAgreeSlots * 4;
+    bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
+  }
 };
 
 // Warp 0: the canonical unit table of <= 32 pairs. Pair p = lane; a pair is
@@ -106,15 +147,15 @@ __device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, int lane, int
   }
 }
 
-// The activation image of one FC1 stage: lane l quantizes values 4l..4l+3 of
-// the 128-value K chunk of each valid row (MXFP8: the 8 lanes of a 32-block
-// combine their maxima, ceil-rule E8M0 scale, e4m3 codes) and stores them in
-// the 128B-swizzled image and the scale atom of the stage's slot.
-__device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], const int (&tok)[2], uint8_t* img,
-                                              uint8_t* atom, int lane) {
+// MXFP8 of one 128-value K chunk of the call's tokens: lane l quantizes
+// values 4l..4l+3 of each token row (the 8 lanes of a 32-block combine their
+// maxima, ceil-rule E8M0 scale, e4m3 codes) into row `token` of the chunk's
+// 128B-swizzled image and scale rows.
+__device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], int B, uint8_t* img, uint8_t* atom,
+                                              int lane) {
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    if (tok[r] < 0) continue;  // the same for every lane
+    if (r >= B) continue;  // the same for every lane
     const uint32_t w[2] = {xv[r].x, xv[r].y};
     float v[4];
 #pragma unroll
@@ -137,18 +178,86 @@ __device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], const int (&
 }
 
 // The CTAs that run FC2 jobs of unit u (those holding jobs u * NQ ..
-// u * NQ + NQ - 1 with a non-empty range): every one of them reads every
-// FC1 piece of the unit.
-__device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g, int u, int G) {
-  const uint32_t J = static_cast<uint32_t>(sp.J), GG = static_cast<uint32_t>(G);
-  auto job_owner = [&](int j) {  // the largest c with floor(c * J / G) <= j
-    const int c = static_cast<int>((static_cast<uint32_t>(j + 1) * GG - 1u) / J);
-    return c < G - 1 ? c : G - 1;
-  };
+// u * NQ + NQ - 1 with a non-empty range): every one of them reads every FC1
+// segment of the unit.
+__device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g, int u) {
   int n = 0;
-  for (int k = job_owner(u * g.NQ); k <= job_owner(u * g.NQ + g.NQ - 1); ++k)
+  for (int k = sp.job_owner(u * g.NQ); k <= sp.job_owner(u * g.NQ + g.NQ - 1); ++k)
     n += sp.fc2_begin(k + 1) > sp.fc2_begin(k);
   return n;
+}
+
+// The build's sums: acc[item][t] and acc[item][2 + t] (gate and up of unit
+// row t < R, tile row m) over all nseg segments of the unit (slots seg0 ..),
+// item-major, added in segment order. Each thread polls exactly the sums it
+// adds up: 32 / R segments' loads in flight, then the sentinels among them
+// re-loaded until every sum has landed (bounded); the masked-out terms add
+// -0.0, which leaves every sum (a zero's sign included) unchanged.
+template <int R>
+__device__ __forceinline__ void sum_segments(const uint32_t* sums, int seg0, int nseg, int spi, int valid, int B,
+                                             int m, const ExpertsArgs& a, float (&acc)[4][4]) {
+  constexpr int NB = 32 / R;
+  const uint64_t t_wait = global_timer_ns();
+#ifdef MOE_TRACE
+  const long long c0 = clock64();
+  uint32_t rounds = 0;
+#endif
+  for (int e0 = 0; e0 < nseg; e0 += NB) {
+    // Slots are consecutive: entry e0 + i is at base + i * kSmallPieceWords.
+    const uint32_t* base = sums + static_cast<size_t>(seg0 + e0) * kSmallPieceWords + m;
+    uint32_t v[NB][2 * R];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+#pragma unroll
+      for (int t = 0; t < R; ++t) {
+        const bool ld = e0 + i < nseg && t < valid;
+        v[i][t] = ld ? load_relaxed_gpu(base + i * kSmallPieceWords + t * kTileM) : 0x80000000u;
+        v[i][R + t] = ld ? load_relaxed_gpu(base + i * kSmallPieceWords + (B + t) * kTileM) : 0x80000000u;
+      }
+    }
+    for (uint32_t poll = 0;; ++poll) {
+      bool missing = false;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+#pragma unroll
+        for (int t = 0; t < R; ++t) {
+          if (v[i][t] == kPieceSentinel) {
+            missing = true;
+            v[i][t] = load_relaxed_gpu(base + i * kSmallPieceWords + t * kTileM);
+          }
+          if (v[i][R + t] == kPieceSentinel) {
+            missing = true;
+            v[i][R + t] = load_relaxed_gpu(base + i * kSmallPieceWords + (B + t) * kTileM);
+          }
+        }
+      }
+#ifdef MOE_TRACE
+      if (poll == 0 && e0 == 0 && m == 64) MOE_STAMP_VALUE(27, static_cast<uint64_t>(clock64() - c0));
+      ++rounds;
+#endif
+      if (!missing) break;
+      if ((poll & 7u) == 7u && global_timer_ns() - t_wait > a.timeout_ns) {
+        report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+        break;  // go on with whatever landed
+      }
+    }
+#ifdef MOE_TRACE
+    if (m == 64) MOE_STAMP_VALUE(26, static_cast<uint64_t>(rounds));
+#endif
+    // Entry e is segment e % spi of item e / spi (at most 4 items).
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int e = e0 + i;
+      const int item = e < nseg ? (e >= spi) + (e >= 2 * spi) + (e >= 3 * spi) : -1;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int t = 0; t < R; ++t) {
+          acc[p][t] += item == p ? __uint_as_float(v[i][t]) : -0.0f;
+          acc[p][2 + t] += item == p ? __uint_as_float(v[i][R + t]) : -0.0f;
+        }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ ExpertsArgs a) {
@@ -156,49 +265,68 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const Geometry& g = a.g;
-  const Layout L(g.KC2);
+  const SmallLayout L(g.KC1, g.KC2);
   uint8_t* W = sm + L.w;
-  uint8_t* ACT = sm + L.act;
+  uint8_t* XC = sm + L.xc;
+  uint8_t* XS = sm + L.xs;
   uint8_t* ASF = sm + L.asf;
   uint8_t* HC = sm + L.hcodes;
-  uint8_t* BSF = sm + L.bsf;
   uint8_t* HSF = sm + L.hsf;
   SmallUnits* su = reinterpret_cast<SmallUnits*>(sm + L.table);
-  SmallPieces* pl = reinterpret_cast<SmallPieces*>(su + 1);  // [kSmallHidden]
-  // FC1 range start and first item of CTAs 0..G (the output-staging region,
-  // which this kernel does not use).
-  uint32_t* span_tbl = reinterpret_cast<uint32_t*>(sm + L.out);  // [kMaxGrid + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
-  uint64_t* empty = full + S;
-  uint64_t* accfull = empty + S;
+  uint64_t* empty = full + kSmallSlots;
+  uint64_t* accfull = empty + kSmallSlots;
   uint64_t* accempty = accfull + NACC;
   uint64_t* hfull = accempty + NACC;
-  uint64_t* drained = hfull + 4;  // [issuer] (hfull + 2 hempty words: Layout's barrier count)
+  uint64_t* drained = hfull + kSmallHidden;  // [issuer]
+  uint64_t* xready = drained + kMmaWarps;
+  uint64_t* prevdone = xready + 1;
   int* agree = reinterpret_cast<int*>(sm + L.agree);
   int4* meta = reinterpret_cast<int4*>(sm + L.meta);
+  volatile uint32_t* sdesc = reinterpret_cast<volatile uint32_t*>(sm + L.desc);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L.misc);  // tmem base, abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, G = gridDim.x;
+  const int B = a.B;
   Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
+  uint32_t* counters = a.small_counters + 4 * a.parity;  // [0] segments claimed, [1] CTAs finished
+  uint32_t* sums = a.piece_sums + static_cast<size_t>(a.parity) * a.seg_cap * kSmallPieceWords;
+  uint32_t* readers = a.piece_readers + static_cast<size_t>(a.parity) * a.seg_cap;
+  const int spi = (g.KC1 + kSegChunks - 1) / kSegChunks;  // segments per item
 
-  // The routing ids first: everything the producer streams depends on them.
+  // The routing ids and this CTA's first FC1 segment first: everything the
+  // producer streams depends on them. The x warps load their chunks of x.
   int my_id = -1;
-  if (warp == kProducerWarp && lane < a.B * kTopK) my_id = a.ids[lane];
+  uint32_t first_claim = 0;
+  if (warp == kProducerWarp && lane < B * kTopK) my_id = a.ids[lane];
+  if (tid == 0) first_claim = atomicAdd(counters, 1u);
+  uint2 xv[kXPerWarp][2];
+  const int xw = warp - kGatherWarp;  // x warp 0..4 (warps 5..9)
+  if (xw >= 0 && a.x != nullptr) {
+#pragma unroll
+    for (int i = 0; i < kXPerWarp; ++i) {
+      const int c = xw + i * kXWarps;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (c < g.KC1 && r < B)
+          xv[i][r] = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(r) * g.H + c * kChunkK) + lane);
+    }
+  }
   if (tid == 0) {
     span_enter(a.span);
     MOE_STAMP(0);
-    // The next launch may start as this one's CTAs leave their SMs.
-    grid_launch_dependents();
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
-      mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
+    for (int s = 0; s < kSmallSlots; ++s) {
+      mbar_init(&full[s], 1);            // the producer (with the bytes, or a descriptor alone)
+      mbar_init(&empty[s], kMmaWarps);   // one commit (or arrival) per issuer
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accfull[i], kMmaWarps + 1);  // issuer commits + the metadata arrival
       mbar_init(&accempty[i], 4);             // one per epilogue warp
     }
     for (int b = 0; b < kSmallHidden; ++b) mbar_init(&hfull[b], 1);
+    mbar_init(xready, kXWarps * 32);
+    mbar_init(prevdone, 1);
     misc[1] = 0;
     fence_mbar_init();
     prefetch_tensormap(&a.wmap);
@@ -214,8 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     derive_units(a, su, lane, my_id);
     if (lane == 0) MOE_STAMP(17);
   }
-  for (int i = tid; i < S * kScaleAtomBytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(BSF)[i] = make_uint4(0, 0, 0, 0);
   if (warp == kMmaWarp0) {
     tmem_alloc(&misc[0], kTmemColumns);
     tmem_relinquish();
@@ -226,61 +352,66 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   if (tid == 0) MOE_STAMP(16);
   const uint32_t tmem = misc[0];
   const int units = su->count;
+  const int NS = units * g.P1 * spi;  // FC1 segments of the call
   const Split sp(units, g, G);
-  const int f0 = sp.fc1_begin(cta), f1 = sp.fc1_begin(cta + 1);
   const int j0 = sp.fc2_begin(cta), j1 = sp.fc2_begin(cta + 1);
   const int fc1_stages = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      MOE_STAMP(18);
-#ifdef MOE_TRACE
-      const long long c0 = clock64();
-#endif
       const uint64_t policy = policy_evict_first();
-#ifdef MOE_TRACE
-      MOE_STAMP_VALUE(26, static_cast<uint64_t>(clock64() - c0));
-      {
-        const long long t0 = clock64();
-        const uint64_t gt = global_timer_ns();
-        asm volatile("" ::"l"(gt));
-        const long long t1 = clock64();
-        MOE_STAMP_VALUE(27, static_cast<uint64_t>(t1 - t0));
-      }
-#endif
-      int n = 0, slot = 0;
+      int n = 0, slot = 0, segs = 0;
       uint32_t phase = 0;
       bool ok = true;
-      auto issue = [&](int stage, bool stand_in) {
-        if (n >= S && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
-        if (n == 0) MOE_STAMP(19);
-        mbar_arrive_expect_tx(&full[slot], kStageWeightBytes + 2 * kScaleAtomBytes);
-        if (stand_in) mbar_arrive_count(&full[slot], 32);
-        tma_load_3d(W + slot * kStageSmemWeights, &a.wmap, 0, 0, stage, &full[slot], policy);
-        if (n == 0) MOE_STAMP(20);
-        bulk_load(ASF + slot * 2 * kScaleAtomBytes,
-                  a.stages + static_cast<size_t>(stage) * kStageBytes + kStageWeightBytes,
-                  2 * kScaleAtomBytes, &full[slot], policy);
-        if (n == 0) MOE_STAMP(1);
-        MOE_STAMP(2);
+      auto issue = [&](int stage, uint32_t desc) {
+        if (n >= kSmallSlots && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
+        sdesc[slot] = desc;
+        if (desc == kDescEnd) {
+          mbar_arrive(&full[slot]);
+        } else {
+          if (n == 0) MOE_STAMP(19);
+          mbar_arrive_expect_tx(&full[slot], kStageWeightBytes + 2 * kScaleAtomBytes);
+          tma_load_3d(W + slot * kStageSmemWeights, &a.wmap, 0, 0, stage, &full[slot], policy);
+          bulk_load(ASF + slot * 2 * kScaleAtomBytes,
+                    a.stages + static_cast<size_t>(stage) * kStageBytes + kStageWeightBytes,
+                    2 * kScaleAtomBytes, &full[slot], policy);
+          if (n == 0) MOE_STAMP(1);
+          MOE_STAMP(2);
+        }
         ++n;
-        if (++slot == S) {
+        if (++slot == kSmallSlots) {
           slot = 0;
           phase ^= 1;
         }
         return true;
       };
-      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g))
-        ok = issue(su->expert[cur.u] * g.SPE + cur.p * g.KC1 + cur.c, false);
+      // FC1: claimed segments, the next claim in flight while one streams.
+      // Claim t is segment NS - 1 - t: the last units' segments go first, so
+      // the CTAs that start last (which run the last units' FC2 jobs) find
+      // their hidden vectors nearly done, and the CTAs that start first take
+      // the first units' segments, which they consume themselves.
+      for (int ticket = static_cast<int>(first_claim); ok && ticket < NS;) {
+        const int next = static_cast<int>(atomicAdd(counters, 1u));
+        const int seg = NS - 1 - ticket;
+        const int item = seg / spi, part = seg - item * spi, u = item / g.P1, pp = item - u * g.P1;
+        const int c0 = part * kSegChunks, c1 = c0 + kSegChunks < g.KC1 ? c0 + kSegChunks : g.KC1;
+        const int base = su->expert[u] * g.SPE + pp * g.KC1;
+        for (int c = c0; c < c1 && ok; ++c) ok = issue(base + c, stage_desc(seg, c, c == c0, c == c1 - 1));
+        ++segs;
+        ticket = next;
+      }
+      if (ok) ok = issue(0, kDescEnd);
+      MOE_STAMP_VALUE(3, static_cast<uint64_t>(segs));
       for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
         const int base = su->expert[cur.u] * g.SPE + fc1_stages + cur.q * g.KC2;
-        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, true);
+        for (int c = 0; c < g.KC2 && ok; ++c) ok = issue(base + c, 0u);
       }
       MOE_STAMP_VALUE(15, static_cast<uint64_t>(n));
       // Drain: every issued stage consumed and released before exit.
       if (ok)
-        for (int k = (n > S ? n - S : 0); k < n && ok; ++k) ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
+        for (int k = (n > kSmallSlots ? n - kSmallSlots : 0); k < n && ok; ++k)
+          ok = wait_bar(cx, &empty[k % kSmallSlots], (k / kSmallSlots) & 1);
       if (!ok) settle_copies();
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
@@ -289,55 +420,71 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
       const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase + issuer * kHiddenScaleColumns;
-      int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0, first_c = 0;
+      int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0;
       uint32_t phase = 0;
-      bool ok = true;
-      bool fc2_seen = false;
+      bool ok = true, have_x = false, fc2_seen = false;
       (void)fc2_seen;
-#ifdef MOE_TRACE
-      int fc2_n = 0;
-#endif
       auto acquire = [&](int set) {
         return k < NACC || wait_bar(cx, &accempty[set], ((k / NACC) - 1) & 1);
       };
       auto advance = [&]() {
         ++n;
-        if (++slot == S) {
+        if (++slot == kSmallSlots) {
           slot = 0;
           phase ^= 1;
         }
       };
-      for (Fc1Cursor cur(f0, g); cur.s < f1 && ok; cur.next(g)) {
-        const bool first = (cur.s == f0) || (cur.c == 0);
-        const bool last = (cur.s == f1 - 1) || (cur.c == g.KC1 - 1);
-        const int set = k % NACC;
-        if (first) {
-          if (!(ok = acquire(set))) break;
-          first_c = cur.c;
-        }
+      // FC1: the stages of the segments this CTA's producer claimed, in the
+      // order of the descriptors, until the end marker.
+      for (;;) {
         if (!(ok = wait_bar(cx, &full[slot], phase))) break;
+        const uint32_t d = sdesc[slot];
+        if (d & kDescEnd) {
+          mbar_arrive(&empty[slot]);
+          advance();
+          break;
+        }
+        if (!have_x) {
+          // The x images are written by generic stores of the x warps.
+          if (!(ok = wait_bar(cx, xready, 0))) break;
+          fence_proxy_async_shared();
+          have_x = true;
+        }
         if (lead && n == 0) MOE_STAMP(4);
-        fence_proxy_async_shared();  // the activation image was written by generic stores
+        const int c = static_cast<int>((d >> 19) & 0xFFu);
+        const int set = k % NACC;
+        if ((d & kDescFirst) && !(ok = acquire(set))) break;
         tc_fence_after_sync();
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
         tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-        tc_copy_scales(sf + 4, desc_scales(BSF + slot * kScaleAtomBytes));
+        tc_copy_scales(sf + 4, desc_scales(XS + c * kXAtomStride));
         const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
-        const uint64_t dx = desc_sw128(ACT + slot * kActImageBytes + k0 * 32);
-        const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
+        const uint64_t dx = desc_sw128(XC + c * kActImageBytes + k0 * 32);
+        const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
         // Descriptor start addresses count 16-byte units: +2 is the next K-step.
-        tc_mma_mxf8f6f4(d, dw, dx, mma_idesc(k0), sf, sf + 4, first ? 0u : 1u);
-        tc_mma_mxf8f6f4(d, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
+        tc_mma_mxf8f6f4(dt, dw, dx, mma_idesc(k0), sf, sf + 4, (d & kDescFirst) ? 0u : 1u);
+        tc_mma_mxf8f6f4(dt, dw + 2, dx + 2, mma_idesc(k0 + 1), sf, sf + 4, 1u);
         if (lead) MOE_STAMP(5);
         tc_commit(&empty[slot]);
         advance();
-        if (last) {
-          // (FC1, item, piece starts the item's K range, piece ends it)
-          if (lead) meta[set] = make_int4(0, cur.item, first_c == 0, cur.c == g.KC1 - 1);
+        if (d & kDescLast) {
+          if (lead) meta[set] = make_int4(0, static_cast<int>(d & kDescSegMask), 0, 0);
           tc_commit(&accfull[set]);
           if (lead) mbar_arrive(&accfull[set]);
           ++k;
         }
+      }
+      // The end of this CTA's FC1 pieces, for the epilogue: an entry with
+      // metadata only.
+      if (ok) {
+        const int set = k % NACC;
+        if (lead) {
+          if ((ok = acquire(set))) {
+            meta[set] = make_int4(3, 0, 0, 0);
+            mbar_arrive_count(&accfull[set], kMmaWarps + 1);
+          }
+        }
+        ++k;
       }
       for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
         if (cur.u != cu) {
@@ -370,17 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
-            const uint32_t d = tmem + set * kAccSetColumns + issuer * 8;
-            tc_mma_mxf8f6f4(d, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
+            const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
+            tc_mma_mxf8f6f4(dt, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
             if (k0 + 1 < ksteps)
-              tc_mma_mxf8f6f4(d, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sfh, 1u);
+              tc_mma_mxf8f6f4(dt, dw + 2, dh + 2, mma_idesc(k0 + 1), sf, sfh, 1u);
             started = true;
           }
           if (lead) MOE_STAMP(11);
-#ifdef MOE_TRACE
-          if (lead && fc2_n < 4) MOE_STAMP(28 + fc2_n);
-          ++fc2_n;
-#endif
           tc_commit(&empty[slot]);
           advance();
         }
@@ -402,95 +545,73 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       tc_commit(&drained[issuer]);
       wait_own(cx, &drained[issuer], 0);
     }
-  } else if (warp == kGatherWarp && a.x == nullptr) {
-    // ------------------------------- activations (FC1), from the prep grid's plan
-    // The call's prep grid ran just before (inputs in host memory: it reads
-    // x once); each stage's 8 activation rows are gathered from its plan.
-    grid_dependency_wait();
-    int n = 0, slot = 0, cu = -1;
-    uint32_t phase = 0;
-    int tok_code = -1, tok_scale = -1;
-    for (Fc1Cursor cur(f0, g); cur.s < f1; cur.next(g)) {
-      if (cur.u != cu) {
-        const int rc = lane >> 2, rs = lane & 7;
-        const int pc = rc < 2 ? su->row[cur.u][rc] : -1;
-        const int ps = rs < 2 ? su->row[cur.u][rs] : -1;
-        tok_code = pc >= 0 ? (pc >> 4) : -1;
-        tok_scale = ps >= 0 ? (ps >> 4) : -1;
-        cu = cur.u;
-      }
-      if (n >= S) {
-        bool freed = true;
-        if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
-        if (!__shfl_sync(0xFFFFFFFFu, freed, 0)) break;
-      }
-      const int r = lane >> 2, piece = lane & 3;
-      uint8_t* img = ACT + slot * kActImageBytes;
-      const uint8_t* row = a.plan_codes + static_cast<size_t>(tok_code < 0 ? 0 : tok_code) * g.H +
-                           cur.c * kChunkK;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c16 = piece * 2 + h;
-        cp_async_16(img + swizzle128(r, c16), row + c16 * 16, tok_code < 0 ? 0u : 16u);
-      }
-      if (lane < 8) {
-        const uint8_t* src = a.plan_scales +
-                             static_cast<size_t>(tok_scale < 0 ? 0 : tok_scale) * (g.H / kBlock) +
-                             cur.c * (kChunkK / kBlock);
-        cp_async_4(BSF + slot * kScaleAtomBytes + lane * 16, src, tok_scale < 0 ? 0u : 4u);
-      }
-      cp_async_arrive_noinc(&full[slot]);
-      ++n;
-      if (++slot == S) {
-        slot = 0;
-        phase ^= 1;
-      }
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kGatherWarp) {
-    // -------------------------------------------- activations (FC1): x -> MXFP8
-    // The call is this launch alone: the x chunks of kAhead stages are loaded
-    // ahead (one 8-byte load per lane and row), so each stage's image is
-    // written as soon as its slot is free. x is an input of the call: no wait
-    // for the previous launch.
-    constexpr int kAhead = 4;
-    const int count = f1 - f0;
-    uint2 xv[kAhead][2];
-    int tok[kAhead][2];
-    auto fetch = [&](int i, int n) {  // ring entry i <- stage f0 + n
-      tok[i][0] = tok[i][1] = -1;
-      if (n >= count) return;
-      const int s = f0 + n, item = s / g.KC1, c = s - item * g.KC1, u = item / g.P1;
+    // ------------------------------------------------- activations (FC1)
+    if (a.x != nullptr) {
+      // x is an input of the call: quantized without waiting for the
+      // previous launch.
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int pr = su->row[u][r];
-        tok[i][r] = pr >= 0 ? (pr >> 4) : -1;
-        if (pr >= 0)
-          xv[i][r] = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(pr >> 4) * g.H +
-                                                           c * kChunkK) + lane);
+      for (int i = 0; i < kXPerWarp; ++i) {
+        const int c = xw + i * kXWarps;
+        if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
       }
-    };
-#pragma unroll
-    for (int i = 0; i < kAhead; ++i) fetch(i, i);
-    int slot = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int n0 = 0; n0 < count && ok; n0 += kAhead) {
-#pragma unroll
-      for (int i = 0; i < kAhead; ++i) {
-        const int n = n0 + i;
-        if (n >= count) break;
-        if (n >= S) {
-          bool freed = true;
-          if (lane == 0) freed = wait_bar(cx, &empty[slot], phase ^ 1);
-          if (!(ok = __shfl_sync(0xFFFFFFFFu, freed, 0))) break;
+      fence_proxy_async_shared();
+      mbar_arrive(xready);
+      grid_dependency_wait();
+    } else {
+      // The call's prep grid ran just before (inputs in host memory: it reads
+      // x once): copy its plan of every chunk into the images.
+      grid_dependency_wait();
+      for (int c = 0; c < g.KC1; ++c) {
+        const int r = lane >> 3, c16 = lane & 7;  // rows 0..3 of the image, 16 bytes each
+        const bool tok = r < B;
+        cp_async_16(XC + c * kActImageBytes + swizzle128(r, c16),
+                    a.plan_codes + static_cast<size_t>(tok ? r : 0) * g.H + c * kChunkK + c16 * 16,
+                    tok ? 16u : 0u);
+        if (lane < 2) {
+          const bool st = lane < B;
+          cp_async_4(XS + c * kXAtomStride + lane * 16,
+                     a.plan_scales + static_cast<size_t>(st ? lane : 0) * (g.H / kBlock) + c * (kChunkK / kBlock),
+                     st ? 4u : 0u);
         }
-        quantize_rows(xv[i], tok[i], ACT + slot * kActImageBytes, BSF + slot * kScaleAtomBytes, lane);
-        mbar_arrive(&full[slot]);  // each lane's own stores, released to the MMA issuers
-        fetch(i, n + kAhead);
-        if (++slot == S) {
-          slot = 0;
-          phase ^= 1;
+      }
+      cp_async_arrive_noinc(xready);
+    }
+    // The previous launch has ended: the next one may start as this CTA's
+    // work proceeds, and the epilogue may write what the previous launch
+    // reads or writes.
+    if (lane == 0) {
+      MOE_STAMP(18);
+      grid_launch_dependents();
+      mbar_arrive(prevdone);
+    }
+    // Read-back of the call's inputs as the prep grid would have left them,
+    // when no prep grid ran: CTA 0 writes the unit table and the kept-pair
+    // flags (and reports dropped pairs), CTA c the MXFP8 plan of K chunk c of
+    // every token (from its image).
+    if (a.x != nullptr) {
+      const bool have_x = wait_bar(cx, xready, 0);  // the images of every x warp
+      if (cta == 0) {
+        if (lane == 0) *a.unit_count = units;
+        for (int i = lane; i < units * kUnitRows; i += 32) {
+          const int uu = i / kUnitRows, r = i % kUnitRows;
+          a.unit_rows[i] = static_cast<int16_t>(r < 2 ? su->row[uu][r] : -1);
+        }
+        for (int uu = lane; uu < units; uu += 32) a.unit_expert[uu] = su->expert[uu];
+        const int pairs = B * kTopK;
+        if (a.pair_kept != nullptr)
+          for (int pp = lane; pp < pairs; pp += 32) a.pair_kept[pp] = (su->kept >> pp) & 1u;
+        const unsigned all = pairs == 32 ? 0xFFFFFFFFu : (1u << pairs) - 1u;
+        if (lane == 0 && su->kept != all) report(a.status, MOE_ERR_DEVICE_IDS);
+      }
+      for (int cc = cta; have_x && cc < g.KC1; cc += G) {
+        const uint8_t* img = XC + cc * kActImageBytes;
+        for (int r = 0; r < B; ++r) {
+          *reinterpret_cast<uint32_t*>(a.plan_codes + static_cast<size_t>(r) * g.H + cc * kChunkK + lane * 4) =
+              *reinterpret_cast<const uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4);
+          if (lane < 4)
+            a.plan_scales[static_cast<size_t>(r) * (g.H / kBlock) + cc * (kChunkK / kBlock) + lane] =
+                XS[cc * kXAtomStride + scale_atom(r, lane)];
         }
       }
     }
@@ -501,96 +622,35 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     const int m = q * 32 + lane;             // tile row of this thread
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
-    const int B = a.B;
-    // FC1 pieces this CTA holds: one per item its range touches.
-    const int first_item = f0 / g.KC1;
-    const int pieces = f1 > f0 ? (f1 - 1) / g.KC1 - first_item + 1 : 0;
-    int done = 0;
-    // The previous launch may still read or write the buffers below (its
-    // partial sums and counts, the plan and unit table, the output): wait for
-    // it to end before the first global write.
-    grid_dependency_wait();
-    // Read-back of the call's inputs as the prep grid would have left them,
-    // when no prep grid ran: CTA 0 writes the unit table and the kept-pair
-    // flags (and reports dropped pairs), CTA c the MXFP8 plan of K chunk c of
-    // every token.
-    if (cta == 0 && a.x != nullptr) {
-      if (et == 0) *a.unit_count = units;
-      for (int i = et; i < units * kUnitRows; i += 128) {
-        const int uu = i / kUnitRows, r = i % kUnitRows;
-        a.unit_rows[i] = static_cast<int16_t>(r < 2 ? su->row[uu][r] : -1);
+    // Its share of the x chunks first.
+    if (a.x != nullptr) {
+#pragma unroll
+      for (int i = 0; i < kXPerWarp; ++i) {
+        const int c = xw + i * kXWarps;
+        if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
       }
-      for (int uu = et; uu < units; uu += 128) a.unit_expert[uu] = su->expert[uu];
-      const int pairs = B * kTopK;
-      if (a.pair_kept != nullptr)
-        for (int pp = et; pp < pairs; pp += 128) a.pair_kept[pp] = (su->kept >> pp) & 1u;
-      const unsigned all = pairs == 32 ? 0xFFFFFFFFu : (1u << pairs) - 1u;
-      if (et == 0 && su->kept != all) report(a.status, MOE_ERR_DEVICE_IDS);
+      fence_proxy_async_shared();
     }
-    for (int cc = cta; a.x != nullptr && cc < g.KC1; cc += G) {
-      for (int t = 0; t < B; ++t) {
-        const float v = __uint_as_float(static_cast<uint32_t>(a.x[static_cast<size_t>(t) * g.H + cc * kChunkK + et]) << 16);
-        const int E = mx_exponent(warp_amax(v), false);
-        a.plan_codes[static_cast<size_t>(t) * g.H + cc * kChunkK + et] = e4m3_code(v * pow2f(-E));
-        if (lane == 0)
-          a.plan_scales[static_cast<size_t>(t) * (g.H / kBlock) + cc * (kChunkK / kBlock) + (et >> 5)] =
-              static_cast<uint8_t>(E + 127);
-      }
-    }
+    mbar_arrive(xready);
+    if (et == 0) MOE_STAMP(28);
+    // The previous launch has ended (the activation warp waited for it):
+    // false only when this CTA gave up waiting.
+    int prev = 0;  // 0: not asked yet, 1: ended, 2: gave up
+    auto await_prev = [&]() {
+      if (prev == 0) prev = wait_bar(cx, prevdone, 0) ? 1 : 2;
+      return prev == 1;
+    };
 
-    // The FC1 range starts (16 bits) and first items (16 bits) of CTAs 0..G,
-    // filled by all epilogue threads at once, so that the piece lists below
-    // need no division (a single thread running them with divisions took
-    // microseconds).
-    for (int c = et; c <= G; c += 128) {
-      const int b = sp.fc1_begin(c);
-      span_tbl[c] = static_cast<uint32_t>(b) | (static_cast<uint32_t>(b / g.KC1) << 16);
-    }
-    epilogue_sync();
-    // The FC1 pieces behind each FC2 unit of this CTA (at most two units):
-    // for every item, the CTAs holding its stages (a binary search over the
-    // range starts), in CTA order, skipping CTAs with empty ranges. Epilogue
-    // warp w builds the list of unit w.
-    if (q == 0 || q == 1) {
-      const int ordinal = q, want_unit = j0 / g.NQ + q;
-      const bool has = ordinal == 0 ? j1 > j0 : (j1 > j0 && (j1 - 1) / g.NQ >= want_unit);
-      if (has && lane == 0) {
-        const int u = want_unit;
-        auto owner = [&](int st) {  // the largest c with begin(c) <= st
-          int lo = 0, hi = G - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (static_cast<int>(span_tbl[mid] & 0xFFFFu) <= st) lo = mid; else hi = mid - 1;
-          }
-          return lo;
-        };
-        SmallPieces& P = pl[ordinal];
-        int n = 0;
-        for (int p = 0; p < g.P1; ++p) {
-          const int item = u * g.P1 + p, s0 = item * g.KC1;
-          const int lo = owner(s0), hi = owner(s0 + g.KC1 - 1);
-          for (int c = lo; c <= hi; ++c) {
-            const uint32_t e0 = span_tbl[c], e1 = span_tbl[c + 1];
-            if ((e1 & 0xFFFFu) > (e0 & 0xFFFFu) && n < kSmallUnitPieces)
-              P.entry[n++] = (p << 16) | (c * kSmallPieces + (item - static_cast<int>(e0 >> 16)));
-          }
-        }
-        P.n = n;
-      }
-    }
-    if (et == 0) MOE_STAMP(18);
-    epilogue_sync();
-
-    // The hidden image of each FC2 unit, built once this CTA's FC1 pieces are
-    // out. The partial-sum slots hold a sentinel (a NaN pattern no sum is
-    // stored as) until their piece lands, so the sums are their own flags:
-    // every piece's loads go out together (16 at a time), and each item's
-    // pieces are summed in CTA order: the masked-out terms add -0.0, which
+    // The hidden image of each FC2 unit, built once this CTA's FC1 segments
+    // are out. The slots hold a sentinel (a NaN pattern no sum is stored as)
+    // until their segment lands, so the sums are their own flags: every
+    // segment's loads go out together (16 at a time), and each item's
+    // segments are summed in order: the masked-out terms add -0.0, which
     // leaves every sum (a zero's sign included) unchanged.
-    bool built = j1 <= j0;
+    bool fc1_over = false, built = j1 <= j0;
     int k = 0;
     for (;;) {
-      if (!built && done == pieces) {
+      if (!built && fc1_over) {
         built = true;
         int ordinal = 0;
         for (int j = j0; j < j1 && ordinal < kSmallHidden; ++ordinal) {
@@ -598,81 +658,21 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           j = (u + 1) * g.NQ;  // the next unit's first job
           // No abort check here: every epilogue thread must pass the same
           // named barriers, and the build's only waits are bounded polls.
-          const SmallPieces& P = pl[ordinal];
           const int valid = su->valid[u];
+          const int seg0 = u * g.P1 * spi, nseg = g.P1 * spi;
           uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
           uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
           if (et == 0) MOE_STAMP(7);
-#ifdef MOE_TRACE
-          const long long c_start = clock64();
-#endif
           // acc[item][gate row 0, gate row 1, up row 0, up row 1]
           float acc[4][4];
 #pragma unroll
           for (int p = 0; p < 4; ++p)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[p][r] = -0.0f;
-          // Each thread polls exactly the sums it adds up (rows m of every
-          // piece): 16 pieces' loads in flight, then the sentinels among
-          // them re-loaded until every sum has landed (bounded).
-          const uint64_t t_wait = global_timer_ns();
-          for (int e0 = 0; e0 < P.n; e0 += 16) {
-            uint32_t v[16][4];
-            int pit[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int e = e0 + i;
-              const int entry = e < P.n ? P.entry[e] : -1;
-              pit[i] = entry >> 16;  // -1 past the end
-              const uint32_t* src = a.piece_sums + static_cast<size_t>(entry < 0 ? 0 : (entry & 0xFFFF)) * kSmallPieceWords;
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const bool ld = entry >= 0 && t < valid;
-                v[i][t] = ld ? load_relaxed_gpu(src + t * kTileM + m) : 0x80000000u;
-                v[i][2 + t] = ld ? load_relaxed_gpu(src + (B + t) * kTileM + m) : 0x80000000u;
-              }
-            }
-            for (uint32_t poll = 0;; ++poll) {
-              bool missing = false;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int entry = e0 + i < P.n ? P.entry[e0 + i] : -1;
-                const uint32_t* src = a.piece_sums + static_cast<size_t>(entry < 0 ? 0 : (entry & 0xFFFF)) * kSmallPieceWords;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                  if (v[i][t] == kPieceSentinel) {
-                    missing = true;
-                    v[i][t] = load_relaxed_gpu(src + t * kTileM + m);
-                  }
-                  if (v[i][2 + t] == kPieceSentinel) {
-                    missing = true;
-                    v[i][2 + t] = load_relaxed_gpu(src + (B + t) * kTileM + m);
-                  }
-                }
-              }
-              if (!missing) break;
-              if ((poll & 7u) == 7u && global_timer_ns() - t_wait > a.timeout_ns) {
-                report(a.status, MOE_ERR_DEVICE_TIMEOUT);
-                break;  // go on with whatever landed
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-#pragma unroll
-              for (int p = 0; p < 4; ++p)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[p][r] += pit[i] == p ? __uint_as_float(v[i][r]) : -0.0f;
-          }
-#ifdef MOE_TRACE
-          {
-            float sum = 0.f;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) sum += acc[p][0] + acc[p][2];
-            asm volatile("" ::"f"(sum));
-            const long long c_loaded = clock64();
-            if (et == 0) MOE_STAMP_VALUE(24, static_cast<uint64_t>(c_loaded - c_start));
-          }
-#endif
+          if (B == 1)
+            sum_segments<1>(sums, seg0, nseg, spi, valid, B, m, a, acc);
+          else
+            sum_segments<2>(sums, seg0, nseg, spi, valid, B, m, a, acc);
           if (et == 0) MOE_STAMP(21);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
@@ -687,38 +687,21 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
               if (lane == 0) hs[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
             }
           }
-#ifdef MOE_TRACE
-          __syncwarp();
-          if (et == 0) MOE_STAMP_VALUE(25, static_cast<uint64_t>(clock64() - c_start));
-#endif
-          if (et == 0) MOE_STAMP(22);
           fence_proxy_async_shared();  // generic writes, read by the tensor core
-          if (et == 0) MOE_STAMP(23);
           epilogue_sync();
           if (et == 0) MOE_STAMP(8);
           if (et == 0 && u != a.withhold_image) mbar_arrive(&hfull[ordinal]);
-          // The CTA holding the unit's first FC2 job also writes the image to
-          // global memory, for read-back.
-          if (j0 <= u * g.NQ) {
-            uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
-            const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
-            for (int i = et; i < n_all; i += 128)
-              reinterpret_cast<uint4*>(img)[i] =
-                  i < n_codes ? reinterpret_cast<const uint4*>(hc)[i]
-                              : reinterpret_cast<const uint4*>(hs)[i - n_codes];
-          }
-          // This CTA has read every piece of the unit: count it per piece. The
-          // unit's last consumer puts the sentinels back and clears the count,
-          // so each slot is empty again for the next call (whose pieces are
-          // stored only after this launch has ended).
-          const int readers = unit_consumers(sp, g, u, G);
-          for (int e = et; e < P.n; e += 128) {
-            const int slot_index = P.entry[e] & 0xFFFF;
-            if (atom_add_acq_rel_gpu(a.piece_readers + slot_index, 1u) + 1u == static_cast<uint32_t>(readers)) {
-              uint4* sums = reinterpret_cast<uint4*>(a.piece_sums + static_cast<size_t>(slot_index) * kSmallPieceWords);
+          // This CTA has read every segment of the unit: count it per slot.
+          // The unit's last consumer puts the sentinels back and clears the
+          // count, so the slot is at rest for the call after next.
+          const int nreaders = unit_consumers(sp, g, u);
+          for (int e = et; e < nseg; e += 128) {
+            const int s = seg0 + e;
+            if (atom_add_acq_rel_gpu(readers + s, 1u) + 1u == static_cast<uint32_t>(nreaders)) {
+              uint4* w = reinterpret_cast<uint4*>(sums + static_cast<size_t>(s) * kSmallPieceWords);
               for (int i = 0; i < kSmallPieceWords / 4; ++i)
-                sums[i] = make_uint4(kPieceSentinel, kPieceSentinel, kPieceSentinel, kPieceSentinel);
-              a.piece_readers[slot_index] = 0u;
+                w[i] = make_uint4(kPieceSentinel, kPieceSentinel, kPieceSentinel, kPieceSentinel);
+              readers[s] = 0u;
             }
           }
         }
@@ -735,6 +718,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         md = meta[set];
       }
       if (md.x == 2) break;
+      if (md.x == 3) {  // this CTA's FC1 segments are all out
+        if (et == 0) MOE_STAMP(29);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[set]);
+        ++k;
+        fc1_over = true;
+        continue;
+      }
       float v0[8], v1[8], x0[8], x1[8];
       {
         uint32_t r0[8], r1[8], r2[8], r3[8];
@@ -765,27 +756,29 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         }
       }
       if (md.x == 0) {
-        // ---- FC1 piece: gate = v0, up = v1 for rows 128p + m -> partial sums.
-        const int item = md.y, u = item / g.P1;
+        // ---- FC1 segment: gate = v0, up = v1 for rows 128p + m -> its slot.
+        // Column j of the accumulator is token j; the slot holds the unit's
+        // rows. A sum with the sentinel's bit pattern (a NaN) is stored as
+        // the canonical NaN.
+        const int seg = md.y, u = seg / (g.P1 * spi);
         const int valid = su->valid[u];
-        // The piece's sums go straight into its slot, which the unit's
-        // consumers poll; a sum with the sentinel's bit pattern (a NaN) is
-        // stored as the canonical NaN.
         if (u != a.withhold_unit) {
-          uint32_t* dst = a.piece_sums + static_cast<size_t>(cta * kSmallPieces + (item - first_item)) * kSmallPieceWords;
+          uint32_t* dst = sums + static_cast<size_t>(seg) * kSmallPieceWords;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= valid) break;
-            const uint32_t gb = __float_as_uint(v0[t]), ub = __float_as_uint(v1[t]);
+            const bool second = (su->row[u][t] >> 4) != 0;  // the row's token
+            const uint32_t gb = __float_as_uint(second ? v0[1] : v0[0]);
+            const uint32_t ub = __float_as_uint(second ? v1[1] : v1[0]);
             dst[t * kTileM + m] = gb == kPieceSentinel ? 0x7FFFFFFFu : gb;
             dst[(B + t) * kTileM + m] = ub == kPieceSentinel ? 0x7FFFFFFFu : ub;
           }
         }
-        ++done;
       } else {
-        // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
+        // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16,
+        // once the previous launch (which may read or write the output) has ended.
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
-        const int valid = su->valid[u];
+        const int valid = await_prev() ? su->valid[u] : 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= valid) break;
@@ -797,6 +790,23 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         if (et == 0) MOE_STAMP(12);
       }
     }
+    // Read-back of the hidden images: the CTA holding a unit's first FC2 job
+    // copies it to global memory.
+    if (built && j1 > j0 && await_prev()) {
+      int ordinal = 0;
+      for (int j = j0; j < j1 && ordinal < kSmallHidden; ++ordinal) {
+        const int u = j / g.NQ;
+        j = (u + 1) * g.NQ;
+        if (j0 > u * g.NQ) continue;
+        const uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
+        const uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
+        uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
+        const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
+        for (int i = et; i < n_all; i += 128)
+          reinterpret_cast<uint4*>(img)[i] = i < n_codes ? reinterpret_cast<const uint4*>(hc)[i]
+                                                         : reinterpret_cast<const uint4*>(hs)[i - n_codes];
+      }
+    }
   }
 
   if (tid == 0) MOE_STAMP(13);
@@ -805,6 +815,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   tc_fence_after_sync();
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
   if (tid == 0) {
+    // The last CTA of the call puts its claim counter back to rest.
+    if (atom_add_acq_rel_gpu(counters + 1, 1u) + 1u == static_cast<uint32_t>(G)) {
+      counters[0] = 0u;
+      counters[1] = 0u;
+    }
     MOE_STAMP(14);
     span_leave(a.span);
   }
@@ -813,18 +828,17 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 }  // namespace
 
 // The small-batch kernel serves a call when it has at most two tokens, the
-// layer has at most MOE_MAX_EXPERTS experts (the kept-expert bitmap), and no
-// CTA's FC1 range touches more items than it has partial-sum slots for.
+// layer has at most MOE_MAX_EXPERTS experts (the kept-expert bitmap), its
+// shared-memory layout fits, and no CTA's FC2 jobs span more units than it
+// has hidden images for.
 bool small_fits(const Geometry& g, int batch, int grid) {
-  if (batch > 2 || grid > kMaxGrid || grid + kMaxInterChunks > kSmallUnitPieces) return false;
-  static_assert(sizeof(SmallUnits) + kSmallHidden * sizeof(SmallPieces) <= 2 * (kMaxGrid + 1) * 4,
-                "the unit table and piece lists fit the table region");
+  if (batch > 2 || grid > kMaxGrid || g.KC1 > kXWarps * kXPerWarp) return false;
+  if (SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
+  if (small_seg_cap(g) > static_cast<int>(kDescSegMask)) return false;
   const int units = g.E < batch * kTopK ? g.E : batch * kTopK;
   for (int n = 1; n <= units; ++n) {
     const Split sp(n, g, grid);
     for (int c = 0; c < grid; ++c) {
-      const int a = sp.fc1_begin(c), b = sp.fc1_begin(c + 1);
-      if (b > a && (b - 1) / g.KC1 - a / g.KC1 + 1 > kSmallPieces) return false;
       const int j0 = sp.fc2_begin(c), j1 = sp.fc2_begin(c + 1);
       if (j1 > j0 && (j1 - 1) / g.NQ - j0 / g.NQ + 1 > kSmallHidden) return false;
     }
@@ -833,15 +847,14 @@ bool small_fits(const Geometry& g, int batch, int grid) {
 }
 
 cudaError_t small_configure() {
-  return cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Layout(kMaxInterChunks).bytes);
+  return cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout(a.g.KC2).bytes;
+  cfg.dynamicSmemBytes = SmallLayout(a.g.KC1, a.g.KC2).bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   int n = 0;

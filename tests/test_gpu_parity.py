@@ -311,9 +311,17 @@ def test_supported_limits(moe, E, H, I, B, dist):
 SMALL_PATHS = [1, 2]  # the small-batch kernel, the cluster variant
 
 
-def set_path(moe, layer, path, batch):
-    """Select an experts kernel for calls of `batch` tokens and check that it serves them."""
+SMALL_MAX_HIDDEN = 3840  # the small-batch kernel keeps x of all K chunks (30 of them) in shared memory
+
+
+def set_path(moe, layer, path, batch, hidden=None):
+    """Select an experts kernel for calls of `batch` tokens and check that it serves them
+    (the small-batch kernel serves layers up to SMALL_MAX_HIDDEN wide; wider ones fall
+    back to the grid kernel)."""
     moe.moe_debug_paths(layer.handle, path)
+    if path == 1 and hidden is not None and hidden > SMALL_MAX_HIDDEN:
+        assert moe.moe_kernel_path(layer.handle, batch) == 0
+        return
     assert moe.moe_kernel_path(layer.handle, batch) == path
     if path == 2:
         assert moe.moe_cluster_size(layer.handle, batch) >= 2
@@ -326,7 +334,7 @@ def set_path(moe, layer, path, batch):
     (8, 3584, 384, 1),     # fewer experts than slots: 8 units; clusters of 8
     (32, 3584, 384, 2),    # the TP8 shard's shape at two tokens; clusters of 4
     (1024, 256, 512, 2),   # the widest I with the smallest H
-    (16, 16384, 512, 1),   # the largest H and I
+    (16, 16384, 512, 1),   # the largest H and I (the small-batch path falls back to the grid kernel)
 ])
 def test_small_batch_path_shapes(moe, E, H, I, B, path):
     """The small-batch kernel and the cluster variant over odd shapes, against the oracle."""
@@ -334,7 +342,7 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
     import torch
 
     layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
-    set_path(moe, layer, path, B)
+    set_path(moe, layer, path, B, hidden=H)
     print(f"[E={E} H={H} I={I} B={B}] path {path}, clusters of {moe.moe_cluster_size(layer.handle, B)}")
     x = workload.make_x(B, H, seed=33)
     ids = workload.make_ids(B, E, seed=34) if E >= 16 else np.stack(
@@ -352,6 +360,26 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
                          if s == min(np.nonzero(ids[t] == ids[t, s])[0])], np.int32)
         ref = oracle.pairs_forward(weights, xq, xs, ids, pairs=keep)
         check_rows(got[keep], ref["out"], f"path {path} E={E} H={H} I={I} B={B}")
+    layer.close()
+
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_small_batch_widest_hidden(moe, B):
+    """The widest layer the small-batch kernel serves (30 K chunks of x in shared memory,
+    six per x warp), with the widest I, against the oracle."""
+    E, H, I = 16, SMALL_MAX_HIDDEN, 512
+    weights = workload.make_weights(E, H, I, seed13=36, seed2=37)
+    import torch
+
+    layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
+    set_path(moe, layer, 1, B, hidden=H)
+    x = workload.make_x(B, H, seed=38)
+    ids = workload.make_ids(B, E, seed=39)
+    got, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids)
+    check_rows(got, ref["out"], f"small E={E} H={H} I={I} B={B}")
     layer.close()
 
 
