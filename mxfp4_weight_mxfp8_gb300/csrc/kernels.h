@@ -60,7 +60,7 @@ struct ExpertsArgs {
   const uint16_t* x;          // BF16 [B, H]: quantized to MXFP8 in the kernel
   uint32_t* piece_sums;       // [2 parities][seg_cap][kSmallPieceWords]: FC1 segment sums, sentinel at rest
   uint32_t* piece_readers;    // [2][seg_cap]: consumers that read the segment, zero at rest
-  uint32_t* small_counters;   // [2][4]: segments claimed, CTAs finished (zero at rest)
+  uint32_t* small_counters;   // [2 parities][4]: [0] segments claimed (zero at rest)
   uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
   int seg_cap;                // segment slots per parity

@@ -336,10 +336,10 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.piece_readers = h->piece_readers;
   a.small_counters = h->small_counters;
   a.seg_cap = moe::small_seg_cap(h->g);
-  // Consecutive calls take alternate halves of the small kernel's slots and
-  // counters (any other kernel ignores them).
+  // Consecutive small-batch calls take alternate halves of that kernel's
+  // slots and counters.
   a.parity = h->small_parity;
-  h->small_parity ^= 1;
+  if (h->path == moe::kPathSmall && ids != nullptr && batch <= 2 && h->small_ok[batch]) h->small_parity ^= 1;
   a.pair_kept = h->pair_kept;
   MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
   return MOE_OK;

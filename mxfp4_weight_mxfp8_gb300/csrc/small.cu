@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   const int cta = blockIdx.x, G = gridDim.x;
   const int B = a.B;
   Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
-  uint32_t* counters = a.small_counters + 4 * a.parity;  // [0] segments claimed, [1] CTAs finished
+  uint32_t* counters = a.small_counters + 4 * a.parity;  // [0] segments claimed
   uint32_t* sums = a.piece_sums + static_cast<size_t>(a.parity) * a.seg_cap * kSmallPieceWords;
   uint32_t* readers = a.piece_readers + static_cast<size_t>(a.parity) * a.seg_cap;
   const int spi = (g.KC1 + kSegChunks - 1) / kSegChunks;  // segments per item
@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     misc[1] = 0;
     fence_mbar_init();
     prefetch_tensormap(&a.wmap);
+    misc[2] = first_claim;  // every role learns whether this CTA has FC1 work
   } else if (warp == kMmaWarp0 + 1 && lane == 0) {
     // Bring every cache line of the kernel's parameters in at once.
     asm volatile("" ::"l"(a.stages), "l"(a.hidden), "r"(a.g.SPE), "l"(a.trace), "l"(a.out),
@@ -353,6 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   const uint32_t tmem = misc[0];
   const int units = su->count;
   const int NS = units * g.P1 * spi;  // FC1 segments of the call
+  // x images are needed when this CTA runs FC1 segments (its first claim is
+  // one) and for the plan read-back of chunk cta.
+  const bool need_x = misc[2] < static_cast<uint32_t>(NS) || cta < g.KC1;
   const Split sp(units, g, G);
   const int j0 = sp.fc2_begin(cta), j1 = sp.fc2_begin(cta + 1);
   const int fc1_stages = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
@@ -391,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       // the CTAs that start last (which run the last units' FC2 jobs) find
       // their hidden vectors nearly done, and the CTAs that start first take
       // the first units' segments, which they consume themselves.
-      for (int ticket = static_cast<int>(first_claim); ok && ticket < NS;) {
+      int ticket = static_cast<int>(first_claim);
+      while (ok && ticket < NS) {
         const int next = static_cast<int>(atomicAdd(counters, 1u));
         const int seg = NS - 1 - ticket;
         const int item = seg / spi, part = seg - item * spi, u = item / g.P1, pp = item - u * g.P1;
@@ -401,6 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         ++segs;
         ticket = next;
       }
+      // Each CTA's claims end with one ticket past the segments, so the call
+      // takes NS + G tickets; the CTA holding the last one puts the counter
+      // back to rest (every other claim of the call is in by then).
+      if (ticket == NS + G - 1) *reinterpret_cast<volatile uint32_t*>(counters) = 0u;
       if (ok) ok = issue(0, kDescEnd);
       MOE_STAMP_VALUE(3, static_cast<uint64_t>(segs));
       for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
@@ -550,19 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     if (a.x != nullptr) {
       // x is an input of the call: quantized without waiting for the
       // previous launch.
+      if (need_x) {
 #pragma unroll
-      for (int i = 0; i < kXPerWarp; ++i) {
-        const int c = xw + i * kXWarps;
-        if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+        for (int i = 0; i < kXPerWarp; ++i) {
+          const int c = xw + i * kXWarps;
+          if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+        }
+        fence_proxy_async_shared();
       }
-      fence_proxy_async_shared();
       mbar_arrive(xready);
       grid_dependency_wait();
     } else {
       // The call's prep grid ran just before (inputs in host memory: it reads
       // x once): copy its plan of every chunk into the images.
       grid_dependency_wait();
-      for (int c = 0; c < g.KC1; ++c) {
+      for (int c = 0; need_x && c < g.KC1; ++c) {
         const int r = lane >> 3, c16 = lane & 7;  // rows 0..3 of the image, 16 bytes each
         const bool tok = r < B;
         cp_async_16(XC + c * kActImageBytes + swizzle128(r, c16),
@@ -623,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     // Its share of the x chunks first.
-    if (a.x != nullptr) {
+    if (a.x != nullptr && need_x) {
 #pragma unroll
       for (int i = 0; i < kXPerWarp; ++i) {
         const int c = xw + i * kXWarps;
@@ -815,11 +826,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   tc_fence_after_sync();
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
   if (tid == 0) {
-    // The last CTA of the call puts its claim counter back to rest.
-    if (atom_add_acq_rel_gpu(counters + 1, 1u) + 1u == static_cast<uint32_t>(G)) {
-      counters[0] = 0u;
-      counters[1] = 0u;
-    }
     MOE_STAMP(14);
     span_leave(a.span);
   }

@@ -862,3 +862,54 @@ def test_stacked_combined_calls_read_the_previous_output(moe, batch):
         got = stack(False)
         for i in range(depth):
             np.testing.assert_array_equal(got[i], ref[i], err_msg=f"rep {rep} layer {i}")
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_small_calls_replayed_in_graphs(moe, batch):
+    """Small-batch calls captured in CUDA graphs and replayed: handles A and B as
+    A, B, A and handle C as C, C, C. Across replays a handle's calls need not
+    alternate between the two halves of its segment slots and claim counters (B and
+    C start each replay on the half their last call used), so each call must leave
+    its half at rest. Every replayed output equals the eager call's bits."""
+    import torch
+
+    weights, _, _ = cached_inputs("tiny")
+    dev = torch.device("cuda:0")
+    handles = [moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights)) for _ in range(3)]
+    H = handles[0].hidden
+    x = workload.make_x(batch, H, seed=71 + batch)
+    ids = workload.make_ids(batch, weights[0].shape[0], seed=72 + batch)
+    xd, idsd = to_device(x, ids)
+    ref = handles[0](xd, idsd)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status(handles[0].handle) == moe.MOE_OK
+    want = ref.view(torch.int16).cpu().numpy()
+    order = [0, 1, 0, 2, 2, 2]
+    outs = [torch.empty_like(ref) for _ in order]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):  # warm up on the capture stream
+        for h, o in zip(order, outs):
+            handles[h](xd, idsd, out=o, stream=stream.cuda_stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for h, o in zip(order, outs):
+            handles[h](xd, idsd, out=o, stream=stream.cuda_stream)
+    for rep in range(3):
+        for o in outs:
+            o.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for h in handles:
+            assert moe.moe_sync_status(h.handle) == moe.MOE_OK, f"replay {rep}"
+        for i, o in enumerate(outs):
+            assert np.array_equal(o.view(torch.int16).cpu().numpy(), want), f"replay {rep}, call {i}"
+    # Eager calls after the replays.
+    for h in handles:
+        got = h(xd, idsd)
+        torch.cuda.synchronize()
+        assert moe.moe_sync_status(h.handle) == moe.MOE_OK
+        assert np.array_equal(got.view(torch.int16).cpu().numpy(), want)
+    del graph
+    for h in handles:
+        h.close()
