@@ -197,6 +197,9 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
                : "memory");
 }
 
+// Wait until every earlier cp.async copy of this thread has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Arrive on the mbarrier once this thread's earlier cp.async copies land
 // (no pending-count increment: the barrier's count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

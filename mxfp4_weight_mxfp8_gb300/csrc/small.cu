@@ -53,7 +53,7 @@ constexpr int kSmallMaxUnits = 2 * kTopK;  // distinct experts of two tokens
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
 constexpr int kSmallSlots = 5;             // weight ring depth
 constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
-constexpr int kXPerWarp = 6;               // K chunks per x warp, at most (KC1 <= 30)
+constexpr int kXRaw = 512;                 // x of chunk c lands at byte 512 of its image (rows 4-7, unused)
 constexpr int kXAtomStride = kUnitRows * 16;  // scale rows 0..7 of chunk c's atom (an N = 8 MMA reads no more)
 constexpr int kSmemLimit = 232448;         // dynamic shared memory one CTA may take
 
@@ -147,16 +147,15 @@ __device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, int lane, int
   }
 }
 
-// MXFP8 of one 128-value K chunk of the call's tokens: lane l quantizes
-// values 4l..4l+3 of each token row (the 8 lanes of a 32-block combine their
-// maxima, ceil-rule E8M0 scale, e4m3 codes) into row `token` of the chunk's
-// 128B-swizzled image and scale rows.
-__device__ __forceinline__ void quantize_rows(const uint2 (&xv)[2], int B, uint8_t* img, uint8_t* atom,
-                                              int lane) {
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (r >= B) continue;  // the same for every lane
-    const uint32_t w[2] = {xv[r].x, xv[r].y};
+// MXFP8 of one 128-value K chunk of the call's tokens, from its BF16 rows at
+// img + kXRaw: lane l quantizes values 4l..4l+3 of each token row (the 8
+// lanes of a 32-block combine their maxima, ceil-rule E8M0 scale, e4m3 codes)
+// into row `token` of the chunk's 128B-swizzled image (bytes 0..255, apart
+// from the BF16 rows) and its scale rows.
+__device__ __forceinline__ void quantize_rows(int B, uint8_t* img, uint8_t* atom, int lane) {
+  for (int r = 0; r < B; ++r) {
+    const uint2 xv = *reinterpret_cast<const uint2*>(img + kXRaw + r * 2 * kChunkK + lane * 8);
+    const uint32_t w[2] = {xv.x, xv.y};
     float v[4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -185,79 +184,6 @@ __device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g
   for (int k = sp.job_owner(u * g.NQ); k <= sp.job_owner(u * g.NQ + g.NQ - 1); ++k)
     n += sp.fc2_begin(k + 1) > sp.fc2_begin(k);
   return n;
-}
-
-// The build's sums: acc[item][t] and acc[item][2 + t] (gate and up of unit
-// row t < R, tile row m) over all nseg segments of the unit (slots seg0 ..),
-// item-major, added in segment order. Each thread polls exactly the sums it
-// adds up: 32 / R segments' loads in flight, then the sentinels among them
-// re-loaded until every sum has landed (bounded); the masked-out terms add
-// -0.0, which leaves every sum (a zero's sign included) unchanged.
-template <int R>
-__device__ __forceinline__ void sum_segments(const uint32_t* sums, int seg0, int nseg, int spi, int valid, int B,
-                                             int m, const ExpertsArgs& a, float (&acc)[4][4]) {
-  constexpr int NB = 32 / R;
-  const uint64_t t_wait = global_timer_ns();
-#ifdef MOE_TRACE
-  const long long c0 = clock64();
-  uint32_t rounds = 0;
-#endif
-  for (int e0 = 0; e0 < nseg; e0 += NB) {
-    // Slots are consecutive: entry e0 + i is at base + i * kSmallPieceWords.
-    const uint32_t* base = sums + static_cast<size_t>(seg0 + e0) * kSmallPieceWords + m;
-    uint32_t v[NB][2 * R];
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-#pragma unroll
-      for (int t = 0; t < R; ++t) {
-        const bool ld = e0 + i < nseg && t < valid;
-        v[i][t] = ld ? load_relaxed_gpu(base + i * kSmallPieceWords + t * kTileM) : 0x80000000u;
-        v[i][R + t] = ld ? load_relaxed_gpu(base + i * kSmallPieceWords + (B + t) * kTileM) : 0x80000000u;
-      }
-    }
-    for (uint32_t poll = 0;; ++poll) {
-      bool missing = false;
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-#pragma unroll
-        for (int t = 0; t < R; ++t) {
-          if (v[i][t] == kPieceSentinel) {
-            missing = true;
-            v[i][t] = load_relaxed_gpu(base + i * kSmallPieceWords + t * kTileM);
-          }
-          if (v[i][R + t] == kPieceSentinel) {
-            missing = true;
-            v[i][R + t] = load_relaxed_gpu(base + i * kSmallPieceWords + (B + t) * kTileM);
-          }
-        }
-      }
-#ifdef MOE_TRACE
-      if (poll == 0 && e0 == 0 && m == 64) MOE_STAMP_VALUE(27, static_cast<uint64_t>(clock64() - c0));
-      ++rounds;
-#endif
-      if (!missing) break;
-      if ((poll & 7u) == 7u && global_timer_ns() - t_wait > a.timeout_ns) {
-        report(a.status, MOE_ERR_DEVICE_TIMEOUT);
-        break;  // go on with whatever landed
-      }
-    }
-#ifdef MOE_TRACE
-    if (m == 64) MOE_STAMP_VALUE(26, static_cast<uint64_t>(rounds));
-#endif
-    // Entry e is segment e % spi of item e / spi (at most 4 items).
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      const int e = e0 + i;
-      const int item = e < nseg ? (e >= spi) + (e >= 2 * spi) + (e >= 3 * spi) : -1;
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-#pragma unroll
-        for (int t = 0; t < R; ++t) {
-          acc[p][t] += item == p ? __uint_as_float(v[i][t]) : -0.0f;
-          acc[p][2 + t] += item == p ? __uint_as_float(v[i][R + t]) : -0.0f;
-        }
-    }
-  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ ExpertsArgs a) {
@@ -301,17 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   uint32_t first_claim = 0;
   if (warp == kProducerWarp && lane < B * kTopK) my_id = a.ids[lane];
   if (tid == 0) first_claim = atomicAdd(counters, 1u);
-  uint2 xv[kXPerWarp][2];
   const int xw = warp - kGatherWarp;  // x warp 0..4 (warps 5..9)
-  if (xw >= 0 && a.x != nullptr) {
-#pragma unroll
-    for (int i = 0; i < kXPerWarp; ++i) {
-      const int c = xw + i * kXWarps;
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-        if (c < g.KC1 && r < B)
-          xv[i][r] = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(r) * g.H + c * kChunkK) + lane);
-    }
+  if (xw >= 0 && a.x != nullptr && lane < 16 * B) {
+    // Chunk c's BF16 rows, 16 bytes a lane, into its image (all in flight).
+    const int r = lane >> 4, j = lane & 15;
+    for (int c = xw; c < g.KC1; c += kXWarps)
+      cp_async_16(XC + c * kActImageBytes + kXRaw + r * 2 * kChunkK + j * 16,
+                  a.x + static_cast<size_t>(r) * g.H + c * kChunkK + j * 8, 16u);
   }
   if (tid == 0) {
     span_enter(a.span);
@@ -495,6 +417,18 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         }
         ++k;
       }
+      // The weight scales of the first FC2 stages go into TMEM while the
+      // hidden vectors are being built: they need only their own stage.
+      const int fc2_stages = (j1 - j0) * g.KC2;
+      const int pre = fc2_stages < kSmallSlots ? fc2_stages : kSmallSlots;
+      for (int i = 0; i < pre && ok; ++i) {
+        const int ni = n + i, si = ni % kSmallSlots;
+        if (!(ok = wait_bar(cx, &full[si], (ni / kSmallSlots) & 1))) break;
+        tc_fence_after_sync();
+        tc_copy_scales(tmem + kTmemScaleBase + si * kSlotScaleColumns + issuer * 8,
+                       desc_scales(ASF + si * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+      }
+      int fc2_n = 0;  // FC2 stages taken so far
       for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
         if (cur.u != cu) {
           ++ordinal;
@@ -523,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
             const int hc = hb * g.KC2 + c;
             const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
-            tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+            if (fc2_n >= pre) tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
             const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
@@ -535,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           if (lead) MOE_STAMP(11);
           tc_commit(&empty[slot]);
           advance();
+          ++fc2_n;
         }
         if (!ok) break;
         if (lead) meta[set] = make_int4(1, cur.j, 0, 0);
@@ -556,18 +491,27 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     }
   } else if (warp == kGatherWarp) {
     // ------------------------------------------------- activations (FC1)
+    uint32_t back_codes[2] = {0u, 0u}, back_scales = 0u;  // plan read-back of chunk cta
     if (a.x != nullptr) {
       // x is an input of the call: quantized without waiting for the
       // previous launch.
+      cp_async_wait_all();
+      __syncwarp();
       if (need_x) {
-#pragma unroll
-        for (int i = 0; i < kXPerWarp; ++i) {
-          const int c = xw + i * kXWarps;
-          if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
-        }
+        for (int c = xw; c < g.KC1; c += kXWarps)
+          quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
         fence_proxy_async_shared();
       }
       mbar_arrive(xready);
+      if (cta < g.KC1 && wait_bar(cx, xready, 0)) {
+        // The plan of chunk cta, read from its image now: the epilogue reuses
+        // the images' region once this CTA's FC1 is done.
+        const uint8_t* img = XC + cta * kActImageBytes;
+        for (int r = 0; r < B; ++r) {
+          back_codes[r] = *reinterpret_cast<const uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4);
+          if (lane < 4) back_scales |= static_cast<uint32_t>(XS[cta * kXAtomStride + scale_atom(r, lane)]) << (8 * r);
+        }
+      }
       grid_dependency_wait();
     } else {
       // The call's prep grid ran just before (inputs in host memory: it reads
@@ -601,7 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     // flags (and reports dropped pairs), CTA c the MXFP8 plan of K chunk c of
     // every token (from its image).
     if (a.x != nullptr) {
-      const bool have_x = wait_bar(cx, xready, 0);  // the images of every x warp
       if (cta == 0) {
         if (lane == 0) *a.unit_count = units;
         for (int i = lane; i < units * kUnitRows; i += 32) {
@@ -615,14 +558,13 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         const unsigned all = pairs == 32 ? 0xFFFFFFFFu : (1u << pairs) - 1u;
         if (lane == 0 && su->kept != all) report(a.status, MOE_ERR_DEVICE_IDS);
       }
-      for (int cc = cta; have_x && cc < g.KC1; cc += G) {
-        const uint8_t* img = XC + cc * kActImageBytes;
+      if (cta < g.KC1) {
         for (int r = 0; r < B; ++r) {
-          *reinterpret_cast<uint32_t*>(a.plan_codes + static_cast<size_t>(r) * g.H + cc * kChunkK + lane * 4) =
-              *reinterpret_cast<const uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4);
+          *reinterpret_cast<uint32_t*>(a.plan_codes + static_cast<size_t>(r) * g.H + cta * kChunkK + lane * 4) =
+              back_codes[r];
           if (lane < 4)
-            a.plan_scales[static_cast<size_t>(r) * (g.H / kBlock) + cc * (kChunkK / kBlock) + lane] =
-                XS[cc * kXAtomStride + scale_atom(r, lane)];
+            a.plan_scales[static_cast<size_t>(r) * (g.H / kBlock) + cta * (kChunkK / kBlock) + lane] =
+                static_cast<uint8_t>(back_scales >> (8 * r));
         }
       }
     }
@@ -634,13 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     // Its share of the x chunks first.
-    if (a.x != nullptr && need_x) {
-#pragma unroll
-      for (int i = 0; i < kXPerWarp; ++i) {
-        const int c = xw + i * kXWarps;
-        if (c < g.KC1) quantize_rows(xv[i], B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+    if (a.x != nullptr) {
+      cp_async_wait_all();
+      __syncwarp();
+      if (need_x) {
+        for (int c = xw; c < g.KC1; c += kXWarps)
+          quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+        fence_proxy_async_shared();
       }
-      fence_proxy_async_shared();
     }
     mbar_arrive(xready);
     if (et == 0) MOE_STAMP(28);
@@ -658,11 +601,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     // segment's loads go out together (16 at a time), and each item's
     // segments are summed in order: the masked-out terms add -0.0, which
     // leaves every sum (a zero's sign included) unchanged.
-    bool fc1_over = false, built = j1 <= j0;
+    // A CTA whose first claim found no segment has no FC1 work: its hidden
+    // images need only the other CTAs' segments (the end-of-FC1 entry
+    // still comes through the accumulator ring, in order).
+    bool fc1_over = misc[2] >= static_cast<uint32_t>(NS), built = j1 <= j0;
     int k = 0;
     for (;;) {
       if (!built && fc1_over) {
         built = true;
+        wait_bar(cx, xready, 0);  // every x copy has landed before the region is reused
         int ordinal = 0;
         for (int j = j0; j < j1 && ordinal < kSmallHidden; ++ordinal) {
           const int u = j / g.NQ;
@@ -674,30 +621,75 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
           uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
           if (et == 0) MOE_STAMP(7);
-          // acc[item][gate row 0, gate row 1, up row 0, up row 1]
-          float acc[4][4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[p][r] = -0.0f;
-          if (B == 1)
-            sum_segments<1>(sums, seg0, nseg, spi, valid, B, m, a, acc);
-          else
-            sum_segments<2>(sums, seg0, nseg, spi, valid, B, m, a, acc);
-          if (et == 0) MOE_STAMP(21);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            if (p >= g.P1 || p * kTileM + q * 32 >= g.I) continue;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (t >= valid) break;
-              const float h = silu_times(acc[p][t], acc[p][2 + t]);
-              const float amax = warp_amax(h);
-              const int E = mx_exponent(amax, g.floor_rule != 0);
-              hc[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
-              if (lane == 0) hs[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
+          // The unit's segment sums land in the x images' region (free once
+          // this CTA's FC1 MMAs are done and the x copies have landed), a few
+          // items at a time: row rr < valid of segment e is the gate of unit
+          // row rr, row valid + rr its up. Every 16-byte copy is in flight
+          // at once; a copy that brought a sentinel word back is issued again
+          // until its segment has landed (bounded).
+          float* land = reinterpret_cast<float*>(XC);
+          const int rows = 2 * valid;
+          const int per_item = spi * rows * kTileM;  // floats of one item's segments
+          const int fit = (g.KC1 * kActImageBytes / 4) / per_item;  // items the region holds (>= 1)
+          const int ipb = fit < 4 ? fit : 4;                          // items per landing
+          for (int p0 = 0; p0 < g.P1; p0 += ipb) {
+            const int p1 = p0 + ipb < g.P1 ? p0 + ipb : g.P1;
+            const int copies = (p1 - p0) * spi * rows * (kTileM / 4);
+            const uint32_t* from = sums + static_cast<size_t>(seg0 + p0 * spi) * kSmallPieceWords;
+            auto copy = [&](int i) {  // copy i: segment i / (rows * 32), row (i / 32) % rows, 16 bytes i % 32
+              const int e = i / (rows * 32), rr = (i >> 5) - e * rows, c4 = (i & 31) * 4;
+              const int row = rr < valid ? rr : B + rr - valid;
+              cp_async_16(land + (e * rows + rr) * kTileM + c4,
+                          from + static_cast<size_t>(e) * kSmallPieceWords + row * kTileM + c4, 16u);
+            };
+            for (int i = et; i < copies; i += 128) copy(i);
+            const uint64_t t_wait = global_timer_ns();
+            for (uint32_t poll = 0;; ++poll) {
+              cp_async_wait_all();
+              bool missing = false;
+              for (int i = et; i < copies; i += 128) {
+                const uint4 w = *reinterpret_cast<const uint4*>(land + (i >> 5) * kTileM + (i & 31) * 4);
+                if (w.x == kPieceSentinel || w.y == kPieceSentinel || w.z == kPieceSentinel || w.w == kPieceSentinel) {
+                  missing = true;
+                  copy(i);
+                }
+              }
+              if (!missing) {
+#ifdef MOE_TRACE
+                if (et == 0) MOE_STAMP_VALUE(26, static_cast<uint64_t>(poll));
+                if (et == 0) MOE_STAMP(27);
+#endif
+                break;
+              }
+              if ((poll & 7u) == 7u && global_timer_ns() - t_wait > a.timeout_ns) {
+                report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                cp_async_wait_all();
+                break;  // go on with whatever landed
+              }
             }
+            epilogue_sync();
+            if (et == 0) MOE_STAMP(24);
+            // Each item's sums in segment order (from -0.0, so a zero's sign
+            // is kept), SiLU(gate) * up and the MXFP8 requant of rows m.
+            for (int p = p0; p < p1; ++p) {
+              if (p * kTileM + q * 32 >= g.I) continue;  // the same for the whole warp
+              for (int t = 0; t < valid; ++t) {
+                float gate = -0.0f, up = -0.0f;
+                const float* src = land + (p - p0) * per_item + m;
+                for (int e = 0; e < spi; ++e) {
+                  gate += src[(e * rows + t) * kTileM];
+                  up += src[(e * rows + valid + t) * kTileM];
+                }
+                const float h = silu_times(gate, up);
+                const float amax = warp_amax(h);
+                const int E = mx_exponent(amax, g.floor_rule != 0);
+                hc[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
+                if (lane == 0) hs[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
+              }
+            }
+            epilogue_sync();  // the landing is read before the next one overwrites it
           }
+          if (et == 0) MOE_STAMP(21);
           fence_proxy_async_shared();  // generic writes, read by the tensor core
           epilogue_sync();
           if (et == 0) MOE_STAMP(8);
@@ -838,8 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 // shared-memory layout fits, and no CTA's FC2 jobs span more units than it
 // has hidden images for.
 bool small_fits(const Geometry& g, int batch, int grid) {
-  if (batch > 2 || grid > kMaxGrid || g.KC1 > kXWarps * kXPerWarp) return false;
-  if (SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
+  if (batch > 2 || grid > kMaxGrid || SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
+  // The hidden build lands one item's segments (two rows per token) in the x images' region.
+  const int spi = (g.KC1 + kSegChunks - 1) / kSegChunks;
+  if (spi * 2 * batch * kTileM * 4 > g.KC1 * kActImageBytes) return false;
   if (small_seg_cap(g) > static_cast<int>(kDescSegMask)) return false;
   const int units = g.E < batch * kTopK ? g.E : batch * kTopK;
   for (int n = 1; n <= units; ++n) {
