@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     if (lane == 0) {
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
-      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase + issuer * kHiddenScaleColumns;
+      // The hidden scale atoms, copied into TMEM once per unit by the epilogue.
+      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase;
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0;
       uint32_t phase = 0;
       bool ok = true, have_x = false, fc2_seen = false;
@@ -436,9 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           if (!(ok = wait_bar(cx, &hfull[hb], 0))) break;
           if (lead) MOE_STAMP(9);
           tc_fence_after_sync();
-          // The unit's hidden scale atoms, once for all its jobs.
-          for (int c = 0; c < g.KC2; ++c)
-            tc_copy_scales(hsf_cols + hb * 16 + c * 4, desc_scales(HSF + (hb * g.KC2 + c) * kScaleAtomBytes));
           cu = cur.u;
         }
         const int set = k % NACC;
@@ -676,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
               for (int t = 0; t < valid; ++t) {
                 float gate = -0.0f, up = -0.0f;
                 const float* src = land + (p - p0) * per_item + m;
+#pragma unroll 4
                 for (int e = 0; e < spi; ++e) {
                   gate += src[(e * rows + t) * kTileM];
                   up += src[(e * rows + valid + t) * kTileM];
@@ -693,7 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           fence_proxy_async_shared();  // generic writes, read by the tensor core
           epilogue_sync();
           if (et == 0) MOE_STAMP(8);
-          if (et == 0 && u != a.withhold_image) mbar_arrive(&hfull[ordinal]);
+          // The unit's hidden scale atoms go into TMEM once, for every issuer;
+          // the copies' completion delivers the image.
+          if (et == 0 && u != a.withhold_image) {
+            tc_fence_after_sync();
+            for (int c = 0; c < g.KC2; ++c)
+              tc_copy_scales(tmem + kTmemHiddenScaleBase + ordinal * 16 + c * 4,
+                             desc_scales(hs + c * kScaleAtomBytes));
+            tc_commit(&hfull[ordinal]);
+          }
           // This CTA has read every segment of the unit: count it per slot.
           // The unit's last consumer puts the sentinels back and clears the
           // count, so the slot is at rest for the call after next.
@@ -727,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         if (lane == 0) mbar_arrive(&accempty[set]);
         ++k;
         fc1_over = true;
+        if (j1 <= j0) break;  // and it has no FC2 job
         continue;
       }
       float v0[8], v1[8], x0[8], x1[8];
@@ -791,6 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           store_row32_bf16(dst + kTileM, v1[t], lane);
         }
         if (et == 0) MOE_STAMP(12);
+        if (j == j1 - 1) break;  // this CTA's last FC2 job (the end entry need not be waited for)
       }
     }
     // Read-back of the hidden images: the CTA holding a unit's first FC2 job
