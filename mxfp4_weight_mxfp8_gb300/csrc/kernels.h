@@ -97,16 +97,22 @@ bool small_fits(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
 // The small-batch kernel's FC1 segment slots: gate and up FP32 sums of up to
-// two token rows per 128-row tile (one segment: a run of kSegChunks K chunks
-// of one item), and a read count per slot, in two halves that consecutive
-// calls alternate. A slot holds kPieceSentinel in every word between uses (no
-// finite or canonical-NaN FP32 sum has this pattern), so a consumer polls the
-// sums themselves.
+// two token rows per 128-row tile (one segment: an even share of the K chunks
+// of one item, about kSegChunks of them), and a read count per slot, in two
+// halves that consecutive calls alternate. A slot holds kPieceSentinel in
+// every word between uses (no finite or canonical-NaN FP32 sum has this
+// pattern), so a consumer polls the sums themselves.
 constexpr int kSmallPieceWords = 2 * 2 * 128;
 constexpr uint32_t kPieceSentinel = 0xFFFFFFFFu;
-constexpr int kSegChunks = 4;
+constexpr int kSegChunks = 7;
+// Segments per item: KC1 / kSegChunks rounded, at least one; segment s of an
+// item covers K chunks [s * KC1 / spi, (s + 1) * KC1 / spi).
+__host__ __device__ inline int small_spi(int kc1) {
+  const int n = (2 * kc1 + kSegChunks) / (2 * kSegChunks);
+  return n > 1 ? n : 1;
+}
 // Segment slots per parity of a layer: 32 units of ceil(I / 128) items.
-inline int small_seg_cap(const Geometry& g) { return 2 * kTopK * g.P1 * ((g.KC1 + kSegChunks - 1) / kSegChunks); }
+inline int small_seg_cap(const Geometry& g) { return 2 * kTopK * g.P1 * small_spi(g.KC1); }
 inline size_t small_piece_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * kSmallPieceWords * 4; }
 inline size_t small_reader_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * 4; }
 constexpr size_t kSmallCounterBytes = 2 * 4 * 4;

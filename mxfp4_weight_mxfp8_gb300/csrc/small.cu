@@ -20,9 +20,10 @@
 //     each expert; the epilogue keeps the unit's own columns). For
 //     read-back, CTA 0 writes the unit table and the kept-pair flags and CTA c
 //     the plan of K chunk c.
-//   - FC1 is cut into segments (kSegChunks K chunks of one item) that the
-//     CTAs claim from a counter as their producers get to them, so the CTAs
-//     that start first (consecutive launches overlap) take more of the work.
+//   - FC1 is cut into segments (an even share of an item's K chunks, about
+//     kSegChunks of them) that the CTAs claim from a counter as their
+//     producers get to them, so the CTAs that start first (consecutive
+//     launches overlap) take more of the work.
 //     FC2 jobs stay split evenly over the CTAs.
 //   - The FC1 -> FC2 hand-off takes one trip through L2. Each segment stores
 //     its FP32 partial sums into its own slot, whose words hold a sentinel
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   uint32_t* counters = a.small_counters + 4 * a.parity;  // [0] segments claimed
   uint32_t* sums = a.piece_sums + static_cast<size_t>(a.parity) * a.seg_cap * kSmallPieceWords;
   uint32_t* readers = a.piece_readers + static_cast<size_t>(a.parity) * a.seg_cap;
-  const int spi = (g.KC1 + kSegChunks - 1) / kSegChunks;  // segments per item
+  const int spi = small_spi(g.KC1);  // segments per item
 
   // The routing ids and this CTA's first FC1 segment first: everything the
   // producer streams depends on them. The x warps load their chunks of x.
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         const int next = static_cast<int>(atomicAdd(counters, 1u));
         const int seg = NS - 1 - ticket;
         const int item = seg / spi, part = seg - item * spi, u = item / g.P1, pp = item - u * g.P1;
-        const int c0 = part * kSegChunks, c1 = c0 + kSegChunks < g.KC1 ? c0 + kSegChunks : g.KC1;
+        const int c0 = part * g.KC1 / spi, c1 = (part + 1) * g.KC1 / spi;
         const int base = su->expert[u] * g.SPE + pp * g.KC1;
         for (int c = c0; c < c1 && ok; ++c) ok = issue(base + c, stage_desc(seg, c, c == c0, c == c1 - 1));
         ++segs;
@@ -841,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 bool small_fits(const Geometry& g, int batch, int grid) {
   if (batch > 2 || grid > kMaxGrid || SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
   // The hidden build lands one item's segments (two rows per token) in the x images' region.
-  const int spi = (g.KC1 + kSegChunks - 1) / kSegChunks;
+  const int spi = small_spi(g.KC1);
   if (spi * 2 * batch * kTileM * 4 > g.KC1 * kActImageBytes) return false;
   if (small_seg_cap(g) > static_cast<int>(kDescSegMask)) return false;
   const int units = g.E < batch * kTopK ? g.E : batch * kTopK;
