@@ -104,7 +104,7 @@ cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bo
 // pattern), so a consumer polls the sums themselves.
 constexpr int kSmallPieceWords = 2 * 2 * 128;
 constexpr uint32_t kPieceSentinel = 0xFFFFFFFFu;
-constexpr int kSegChunks = 7;
+constexpr int kSegChunks = 10;
 // Segments per item: KC1 / kSegChunks rounded, at least one; segment s of an
 // item covers K chunks [s * KC1 / spi, (s + 1) * KC1 / spi).
 __host__ __device__ inline int small_spi(int kc1) {

@@ -52,11 +52,18 @@ namespace {
 
 constexpr int kSmallMaxUnits = 2 * kTopK;  // distinct experts of two tokens
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
-constexpr int kSmallSlots = 5;             // weight ring depth
+constexpr int kSmallSlots = 2;             // weight ring depth (two CTAs share an SM)
 constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
 constexpr int kXRaw = 512;                 // x of chunk c lands at byte 512 of its image (rows 4-7, unused)
 constexpr int kXAtomStride = kUnitRows * 16;  // scale rows 0..7 of chunk c's atom (an N = 8 MMA reads no more)
-constexpr int kSmemLimit = 232448;         // dynamic shared memory one CTA may take
+// Two CTAs per SM, one of each of two consecutive calls, so that one streams
+// while the other hands off and runs its FC2 jobs: each takes at most half of
+// the SM's 228 KB of shared memory (less 1 KB reserved per CTA) and half of
+// its 512 TMEM columns.
+constexpr int kSmemLimit = (233472 - 2 * 1024) / 2;  // dynamic shared memory one CTA may take
+constexpr int kSmallTmemColumns = 256;
+constexpr int kSmallHiddenScaleBase = kTmemScaleBase + kSmallSlots * kSlotScaleColumns;  // 2 x 16 columns
+static_assert(kSmallHiddenScaleBase + 2 * 16 <= kSmallTmemColumns, "the small kernel's TMEM columns");
 
 // Stage descriptors, one per ring slot in shared memory: the producer writes
 // it before arriving on the slot's full barrier.
@@ -187,7 +194,7 @@ __device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g
   return n;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ ExpertsArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constant__ ExpertsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
     if (lane == 0) MOE_STAMP(17);
   }
   if (warp == kMmaWarp0) {
-    tmem_alloc(&misc[0], kTmemColumns);
+    tmem_alloc(&misc[0], kSmallTmemColumns);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
       // The hidden scale atoms, copied into TMEM once per unit by the epilogue.
-      const uint32_t hsf_cols = tmem + kTmemHiddenScaleBase;
+      const uint32_t hsf_cols = tmem + kSmallHiddenScaleBase;
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0;
       uint32_t phase = 0;
       bool ok = true, have_x = false, fc2_seen = false;
@@ -698,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
           if (et == 0 && u != a.withhold_image) {
             tc_fence_after_sync();
             for (int c = 0; c < g.KC2; ++c)
-              tc_copy_scales(tmem + kTmemHiddenScaleBase + ordinal * 16 + c * 4,
+              tc_copy_scales(tmem + kSmallHiddenScaleBase + ordinal * 16 + c * 4,
                              desc_scales(hs + c * kScaleAtomBytes));
             tc_commit(&hfull[ordinal]);
           }
@@ -826,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemColumns);
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kSmallTmemColumns);
   if (tid == 0) {
     MOE_STAMP(14);
     span_leave(a.span);

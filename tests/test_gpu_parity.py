@@ -311,7 +311,7 @@ def test_supported_limits(moe, E, H, I, B, dist):
 SMALL_PATHS = [1, 2]  # the small-batch kernel, the cluster variant
 
 
-SMALL_MAX_HIDDEN = 5376  # at I = 512 the small-batch kernel's x images of all K chunks (42) fit shared memory
+SMALL_MAX_HIDDEN = 3584  # at I = 512 the small-batch kernel's x images of all K chunks (28) fit its half SM
 
 
 def set_path(moe, layer, path, batch, hidden=None):
@@ -365,8 +365,8 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
 
 @pytest.mark.parametrize("B", [1, 2])
 def test_small_batch_widest_hidden(moe, B):
-    """The widest layer the small-batch kernel serves at the widest I (42 K chunks of x
-    in shared memory), against the oracle."""
+    """The widest layer the small-batch kernel serves at the widest I (28 K chunks of x
+    in shared memory, two CTAs per SM), against the oracle."""
     E, H, I = 16, SMALL_MAX_HIDDEN, 512
     weights = workload.make_weights(E, H, I, seed13=36, seed2=37)
     import torch
