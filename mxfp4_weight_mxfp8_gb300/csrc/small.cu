@@ -426,18 +426,6 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         }
         ++k;
       }
-      // The weight scales of the first FC2 stages go into TMEM while the
-      // hidden vectors are being built: they need only their own stage.
-      const int fc2_stages = (j1 - j0) * g.KC2;
-      const int pre = fc2_stages < kSmallSlots ? fc2_stages : kSmallSlots;
-      for (int i = 0; i < pre && ok; ++i) {
-        const int ni = n + i, si = ni % kSmallSlots;
-        if (!(ok = wait_bar(cx, &full[si], (ni / kSmallSlots) & 1))) break;
-        tc_fence_after_sync();
-        tc_copy_scales(tmem + kTmemScaleBase + si * kSlotScaleColumns + issuer * 8,
-                       desc_scales(ASF + si * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-      }
-      int fc2_n = 0;  // FC2 stages taken so far
       for (Fc2Cursor cur(j0, g); cur.j < j1 && ok; cur.next(g)) {
         if (cur.u != cu) {
           ++ordinal;
@@ -463,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
             const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
             const int hc = hb * g.KC2 + c;
             const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
-            if (fc2_n >= pre) tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
+            tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
             const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
             const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
@@ -475,7 +463,6 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           if (lead) MOE_STAMP(11);
           tc_commit(&empty[slot]);
           advance();
-          ++fc2_n;
         }
         if (!ok) break;
         if (lead) meta[set] = make_int4(1, cur.j, 0, 0);
