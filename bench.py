@@ -423,8 +423,9 @@ class OurArm:
         handle, B = self.layers[0].handle, self.cfg.batch
         path = self.moe.moe_kernel_path(handle, B)
         if path == self.moe.PATH_SMALL:
-            return ("small_kernel (the whole call in one launch, one CTA per SM: MXFP8 quantize and "
-                    "unit table in the kernel; FC1 partial sums summed by every FC2 CTA; tcgen05 "
+            return ("small_kernel (the whole call in one launch, two CTAs per SM, one of each of "
+                    "two consecutive calls: MXFP8 quantize and unit table in the kernel; FC1 segments "
+                    "claimed from a counter, their sums gathered by every FC2 CTA; tcgen05 "
                     "block-scaled MMA)")
         if path == self.moe.PATH_CLUSTER:
             C = self.moe.moe_cluster_size(handle, B)
