@@ -275,20 +275,24 @@ int moe_copy_hidden(moe_handle h, uint8_t* codes, uint8_t* scales, int units);
  * mbarrier wait runs out and the CTA gives up (-1 = off, the default).
  * Checks the abort path: the call records MOE_ERR_DEVICE_TIMEOUT, finishes,
  * and the next call is unaffected. MOE_ERR_ARG below -1.
- * moe_debug_paths - which experts kernel calls of one or two tokens run on:
- * 1 (the default) the small-batch kernel (one CTA per SM, the unit table
+ * moe_debug_paths - which experts kernel small calls run on:
+ * 1 (the default) the small-batch kernel for calls of one or two tokens
+ * (two CTAs per SM, one of each of two consecutive calls; the unit table
  * derived from the routing ids in the kernel, every FC2 CTA summing the FC1
- * partial sums of its units itself) where the layer's shape fits it;
- * 0 the persistent grid kernel; 2 the cluster variant (one thread-block
- * cluster of up to 8 CTAs per unit, partial sums and hidden chunks through
- * distributed shared memory) where the shape fits it. Calls of more tokens,
- * and calls whose path does not fit, run on the grid kernel. The kernels
- * cut the FC1 K range into split-K pieces at different stages, so their FP32
- * sums are grouped differently and may differ in the last bits.
- * MOE_ERR_ARG for other values.
+ * segment sums of its units itself) where the layer's shape fits it;
+ * 0 the persistent grid kernel; 2 the cluster variant for one or two tokens
+ * (one thread-block cluster of up to 8 CTAs per unit, partial sums and
+ * hidden chunks through distributed shared memory) where the shape fits it;
+ * 3 the small-batch kernel for calls of up to 8 tokens where the shape fits
+ * it (measured no faster than the grid kernel at 3 to 8 tokens, hence not
+ * the default there). Other calls, and calls whose path does not fit, run
+ * on the grid kernel. The kernels cut the FC1 K range into split-K pieces at
+ * different stages, so their FP32 sums are grouped differently and may
+ * differ in the last bits. MOE_ERR_ARG for other values.
  * moe_kernel_path - the kernel a call of `batch` tokens runs on under the
- * current setting: 0 grid, 1 small-batch, 2 cluster variant (calls through
- * moe_experts, which has no routing ids, never take path 1).
+ * current setting: 0 grid, 1 small-batch (under path 1 or 3), 2 cluster
+ * variant (calls through moe_experts, which has no routing ids, never take
+ * the small-batch kernel).
  * -MOE_ERR_ARG for a null handle or a batch outside [1, MOE_MAX_BATCH].
  */
 int moe_set_timeout(moe_handle h, uint64_t nanoseconds);

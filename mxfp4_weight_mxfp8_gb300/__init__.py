@@ -23,7 +23,7 @@ __all__ = [
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
     "MAX_BATCH", "moe_device_supported", "moe_debug_kernel_span", "moe_read_kernel_span",
-    "moe_kernel_path", "PATH_GRID", "PATH_SMALL", "PATH_CLUSTER",
+    "moe_kernel_path", "PATH_GRID", "PATH_SMALL", "PATH_CLUSTER", "PATH_SMALL_WIDE",
 ]
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
@@ -208,11 +208,12 @@ def moe_debug_withhold_image(handle, unit: int):
     return _check(_lib.moe_debug_withhold_image(handle, unit), "moe_debug_withhold_image")
 
 
-PATH_GRID, PATH_SMALL, PATH_CLUSTER = 0, 1, 2
+PATH_GRID, PATH_SMALL, PATH_CLUSTER, PATH_SMALL_WIDE = 0, 1, 2, 3
 
 
 def moe_debug_paths(handle, path: int):
-    """0 grid kernel, 1 small-batch kernel (default), 2 cluster variant."""
+    """0 grid kernel, 1 small-batch kernel for 1-2 tokens (default), 2 cluster variant,
+    3 small-batch kernel for up to 8 tokens."""
     return _check(_lib.moe_debug_paths(handle, path), "moe_debug_paths")
 
 

@@ -1407,8 +1407,8 @@ cudaError_t experts_occupancy(const Geometry& g, int* blocks_per_sm) {
 }
 
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
-                           int path, bool small_ok) {
-  if (path == kPathSmall && small_ok && a.ids != nullptr && a.B <= 2)
+                           int path, bool small) {
+  if (small && a.ids != nullptr && a.B <= kSmallMaxBatch)  // small: the path serves this call
     return launch_small(a, grid, stream, pdl);
   // Calls of more than 8 tokens run 16-row units (pairs of the table's units).
   const int rows = a.B > kUnitRows ? 16 : 8;

@@ -64,6 +64,7 @@ struct ExpertsArgs {
   uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
   int seg_cap;                // segment slots per parity
+  int piece_words;            // words per segment slot (2 x the batch bound x 128)
   int parity;                 // which half of the slots and counters this call uses
 };
 
@@ -88,21 +89,28 @@ struct ClusterPlan {
 // kernel; kPathSmall (default) the small-batch kernel for calls of one or two
 // tokens whose routing ids are given and whose split fits it (small_fits),
 // else the grid kernel; kPathCluster the cluster variant for one or two
-// tokens where the shape fits it, else the grid kernel.
-enum ExpertsPath : int { kPathGrid = 0, kPathSmall = 1, kPathCluster = 2 };
+// tokens where the shape fits it, else the grid kernel; kPathSmallWide the
+// small-batch kernel for calls of up to kSmallMaxBatch tokens where it fits.
+enum ExpertsPath : int { kPathGrid = 0, kPathSmall = 1, kPathCluster = 2, kPathSmallWide = 3 };
 cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl,
-                           int path, bool small_ok);
+                           int path, bool small);
 int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serves this call
 bool small_fits(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
+constexpr int kSmallMaxBatch = 8;  // calls of up to 8 tokens may take the small-batch kernel
+// Whether a handle's path value sends a call of `batch` tokens to the
+// small-batch kernel (where small_fits also holds).
+inline bool small_path_serves(int path, int batch) {
+  return (path == kPathSmall && batch <= 2) || (path == kPathSmallWide && batch <= kSmallMaxBatch);
+}
 // The small-batch kernel's FC1 segment slots: gate and up FP32 sums of up to
-// two token rows per 128-row tile (one segment: an even share of the K chunks
-// of one item, about kSegChunks of them), and a read count per slot, in two
-// halves that consecutive calls alternate. A slot holds kPieceSentinel in
-// every word between uses (no finite or canonical-NaN FP32 sum has this
+// kSmallMaxBatch token rows per 128-row tile (one segment: an even share of the
+// K chunks of one item, about kSegChunks of them), and a read count per slot,
+// in two halves that consecutive calls alternate. A slot holds kPieceSentinel
+// in every word between uses (no finite or canonical-NaN FP32 sum has this
 // pattern), so a consumer polls the sums themselves.
-constexpr int kSmallPieceWords = 2 * 2 * 128;
+constexpr int kSmallPieceWords = 2 * kSmallMaxBatch * 128;
 constexpr uint32_t kPieceSentinel = 0xFFFFFFFFu;
 constexpr int kSegChunks = 10;
 // Segments per item: KC1 / kSegChunks rounded, at least one; segment s of an
@@ -111,8 +119,8 @@ __host__ __device__ inline int small_spi(int kc1) {
   const int n = (2 * kc1 + kSegChunks) / (2 * kSegChunks);
   return n > 1 ? n : 1;
 }
-// Segment slots per parity of a layer: 32 units of ceil(I / 128) items.
-inline int small_seg_cap(const Geometry& g) { return 2 * kTopK * g.P1 * small_spi(g.KC1); }
+// Segment slots per parity of a layer: 128 units of ceil(I / 128) items.
+inline int small_seg_cap(const Geometry& g) { return kSmallMaxBatch * kTopK * g.P1 * small_spi(g.KC1); }
 inline size_t small_piece_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * kSmallPieceWords * 4; }
 inline size_t small_reader_bytes(const Geometry& g) { return 2 * static_cast<size_t>(small_seg_cap(g)) * 4; }
 constexpr size_t kSmallCounterBytes = 2 * 4 * 4;

@@ -41,7 +41,7 @@ struct moe_ctx {
   int withhold = -1;
   int withhold_image = -1;
   int path = moe::kPathSmall;  // which experts kernel one- and two-token calls run on
-  int small_ok[3] = {0, 0, 0};  // [batch]: the small-batch kernel's split fits this layer
+  int small_ok[moe::kSmallMaxBatch + 1] = {};  // [batch]: the small-batch kernel's split fits this layer
   uint64_t* span = nullptr;  // launch clock of the experts kernel: [CTA][start, end]
   uint32_t* piece_sums = nullptr;      // small-batch kernel: FC1 segment slots (sentinel at rest)
   uint32_t* piece_readers = nullptr;   // small-batch kernel: read counts per slot (zero at rest)
@@ -176,7 +176,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
     return MOE_ERR_UNSUPPORTED;
   }
   h->grid = h->sms < moe::kMaxGrid ? h->sms : moe::kMaxGrid;  // one co-resident CTA per SM
-  for (int b = 1; b <= 2; ++b) h->small_ok[b] = moe::small_fits(g, b, h->grid) ? 1 : 0;
+  for (int b = 1; b <= moe::kSmallMaxBatch; ++b) h->small_ok[b] = moe::small_fits(g, b, h->grid) ? 1 : 0;
 
   // Weights: one 17 KB block per stage.
   h->stage_bytes = static_cast<size_t>(g.E) * g.SPE * moe::kStageBytes;
@@ -300,7 +300,7 @@ int check_device(const moe_ctx* h) {
 // Whether a call of `batch` tokens with its routing ids runs on the
 // small-batch kernel alone (no prep grid).
 bool small_call(const moe_ctx* h, int batch) {
-  return batch <= 2 && h->path == moe::kPathSmall && h->small_ok[batch];
+  return batch <= moe::kSmallMaxBatch && moe::small_path_serves(h->path, batch) && h->small_ok[batch];
 }
 
 // ids: the call's routing ids when the same call's prep grid runs just
@@ -336,12 +336,14 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
   a.piece_readers = h->piece_readers;
   a.small_counters = h->small_counters;
   a.seg_cap = moe::small_seg_cap(h->g);
+  a.piece_words = moe::kSmallPieceWords;
   // Consecutive small-batch calls take alternate halves of that kernel's
   // slots and counters.
   a.parity = h->small_parity;
-  if (h->path == moe::kPathSmall && ids != nullptr && batch <= 2 && h->small_ok[batch]) h->small_parity ^= 1;
+  const bool small = ids != nullptr && small_call(h, batch);
+  if (small) h->small_parity ^= 1;
   a.pair_kept = h->pair_kept;
-  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, batch <= 2 && h->small_ok[batch]));
+  MOE_CUDA(moe::launch_experts(a, h->grid, stream, true, h->path, small));
   return MOE_OK;
 }
 
@@ -638,7 +640,7 @@ int moe_debug_withhold_image(moe_handle h, int unit) {
 }
 
 int moe_debug_paths(moe_handle h, int path) {
-  if (h == nullptr || path < moe::kPathGrid || path > moe::kPathCluster) return MOE_ERR_ARG;
+  if (h == nullptr || path < moe::kPathGrid || path > moe::kPathSmallWide) return MOE_ERR_ARG;
   h->path = path;
   ++h->settings;
   return MOE_OK;
@@ -691,7 +693,7 @@ int moe_cluster_size(moe_handle h, int batch) {
 
 int moe_kernel_path(moe_handle h, int batch) {
   if (h == nullptr || check_batch(batch)) return -MOE_ERR_ARG;
-  if (batch <= 2 && h->path == moe::kPathSmall && h->small_ok[batch]) return moe::kPathSmall;
+  if (small_call(h, batch)) return moe::kPathSmall;
   if (h->path == moe::kPathCluster && moe::cluster_size_for(h->g, batch) > 0) return moe::kPathCluster;
   return moe::kPathGrid;
 }
@@ -786,7 +788,10 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
     return MOE_ERR_ARG;
   const Geometry& g = h->g;
   const int cap = moe::unit_capacity(batch, g.E);
-  const bool small = small_call(h, batch);
+  // Here the small-batch kernel serves one or two tokens (its segment slots
+  // then hold two rows each: a smaller share of the static buffer).
+  const bool small = batch <= 2 && small_call(h, batch);
+  const int small_cap = 2 * MOE_TOPK * g.P1 * moe::small_spi(g.KC1), small_words = 2 * 2 * moe::kTileM;
   const size_t sizes[] = {
       static_cast<size_t>(batch) * g.H,                            // plan codes
       static_cast<size_t>(batch) * (g.H / moe::kBlock),            // plan scales
@@ -797,9 +802,9 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
       static_cast<size_t>(cap) * g.KC2 * 4,                        // hidden flags
       static_cast<size_t>(h->grid) * 2 * 2 * (batch > moe::kUnitRows ? 16 : 8) * moe::kTileM * 4,  // partials
       static_cast<size_t>(cap) * g.hidden_bytes,                   // hidden images
-      small ? moe::small_reader_bytes(g) / 2 : 0,                 // small-batch read counts (one half)
+      small ? static_cast<size_t>(small_cap) * 4 : 0,             // small-batch read counts (one half)
       static_cast<size_t>(cap) * 4,                                // pairs of units
-      small ? moe::small_piece_bytes(g) / 2 : 0,                  // small-batch segment slots (one half)
+      small ? static_cast<size_t>(small_cap) * small_words * 4 : 0,  // small-batch segment slots (one half)
       small ? moe::kSmallCounterBytes : 0,                         // small-batch claim counters
   };
   size_t offsets[13], total = 0;
@@ -839,8 +844,8 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   uint32_t* piece_sums = reinterpret_cast<uint32_t*>(w + offsets[11]);
   uint32_t* small_counters = reinterpret_cast<uint32_t*>(w + offsets[12]);
   if (small) {  // memsets, not allocations; the call takes half 0 of the slots
-    MOE_CUDA(cudaMemsetAsync(piece_readers, 0, moe::small_reader_bytes(g) / 2, s));
-    MOE_CUDA(cudaMemsetAsync(piece_sums, 0xFF, moe::small_piece_bytes(g) / 2, s));
+    MOE_CUDA(cudaMemsetAsync(piece_readers, 0, static_cast<size_t>(small_cap) * 4, s));
+    MOE_CUDA(cudaMemsetAsync(piece_sums, 0xFF, static_cast<size_t>(small_cap) * small_words * 4, s));
     MOE_CUDA(cudaMemsetAsync(small_counters, 0, moe::kSmallCounterBytes, s));
   } else {
     MOE_CUDA(moe::launch_prep(pa, s));
@@ -872,7 +877,8 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
     ea.piece_sums = piece_sums;
     ea.piece_readers = piece_readers;
     ea.small_counters = small_counters;
-    ea.seg_cap = moe::small_seg_cap(g);
+    ea.seg_cap = small_cap;
+    ea.piece_words = small_words;
     ea.parity = 0;
     ea.pair_kept = nullptr;
   }

@@ -50,7 +50,8 @@
 namespace moe {
 namespace {
 
-constexpr int kSmallMaxUnits = 2 * kTopK;  // distinct experts of two tokens
+constexpr int kSmallMaxTokens = kSmallMaxBatch;  // tokens of a call (one unit per expert: <= 8 rows)
+constexpr int kSmallMaxUnits = kSmallMaxTokens * kTopK;  // distinct experts of the call
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
 constexpr int kSmallSlots = 2;             // weight ring depth (two CTAs share an SM)
 constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
@@ -76,14 +77,17 @@ __device__ __forceinline__ uint32_t stage_desc(int seg, int c, bool first, bool 
          (last ? kDescLast : 0u);
 }
 
-// The unit table of the call, in shared memory.
+// The unit table of the call, in shared memory: one unit per kept expert
+// (at most 8 tokens, so at most 8 rows).
 struct SmallUnits {
   int count;
   int expert[kSmallMaxUnits];
-  int row[kSmallMaxUnits][2];   // pair t * 16 + s, -1 padding
-  int valid[kSmallMaxUnits];
-  unsigned bits[MOE_MAX_EXPERTS / 32];  // kept experts
-  unsigned kept;                        // bit p: pair p got a unit row
+  int16_t row[kSmallMaxUnits][kUnitRows];  // pair t * 16 + s of rows 0 .. valid - 1
+  uint8_t valid[kSmallMaxUnits];
+  uint8_t tokens[kSmallMaxUnits];          // bit t: token t has a row in the unit
+  unsigned bits[MOE_MAX_EXPERTS / 32];     // kept experts
+  int below[MOE_MAX_EXPERTS / 32];         // units of the experts in lower words of bits
+  unsigned kept[kSmallMaxUnits / 32];      // bit p % 32 of word p / 32: pair p got a unit row
 };
 
 // Shared-memory carve-up of the small kernel (images on 1024-byte boundaries).
@@ -110,78 +114,89 @@ struct SmallLayout {
   }
 };
 
-// Warp 0: the canonical unit table of <= 32 pairs. Pair p = lane; a pair is
-// kept when its id is in [0, E) and no lower slot of its token has the same
-// id. Unit u is the u-th kept expert in ascending order; its rows are its
-// pairs in token order.
-__device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, int lane, int e) {
-  const int pairs = a.B * kTopK;  // 16 or 32
-  su->bits[lane] = 0;
-  su->row[lane][0] = -1;
-  su->row[lane][1] = -1;
-  const bool valid = lane < pairs && e >= 0 && e < a.g.E;
+// Warps 0 .. nw - 1: the canonical unit table of <= 128 pairs (B <= 8).
+// Pair p = 32 * warp + lane; a pair is kept when its id is in [0, E) and no
+// lower slot of its token has the same id. Unit u is the u-th kept expert in
+// ascending order (at most 8 tokens: one unit per expert); its rows are its
+// pairs in token order. `emask` (shared memory, E / 4 words) holds each
+// expert's token bits while the table is built.
+__device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, uint32_t* emask, int p, int e, int nw) {
+  const int pairs = a.B * kTopK, lane = p & 31, warp = p >> 5, E = a.g.E;
+  auto sync = [&]() { asm volatile("bar.sync 3, %0;" ::"r"(nw * 32) : "memory"); };
+  for (int i = p; i < MOE_MAX_EXPERTS / 32; i += nw * 32) su->bits[i] = 0;
+  for (int i = p; i < (E + 3) / 4; i += nw * 32) emask[i] = 0;
+  sync();
+  const int t = p >> 4;  // the pair's token
+  const bool valid = p < pairs && e >= 0 && e < E;
+  // A token's 16 pairs share a warp (lanes 0-15 or 16-31).
   const unsigned in_token = __match_any_sync(0xFFFFFFFFu, valid ? 2 * e + (lane >> 4) : -1 - lane);
   const bool kept = valid && __ffs(in_token) - 1 == lane;
   const unsigned kept_mask = __ballot_sync(0xFFFFFFFFu, kept);
-  __syncwarp();
-  if (kept) atomicOr(&su->bits[e >> 5], 1u << (e & 31));
-  __syncwarp();
-  const unsigned word = su->bits[lane];
-  const int cnt = __popc(word);
-  int incl = cnt;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int other = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl += other;
-  }
-  const int units = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  int k = incl - cnt;
-  for (unsigned w = word; w != 0; w &= w - 1, ++k) su->expert[k] = lane * 32 + __ffs(w) - 1;
-  // Rows: the unit of a kept pair is its expert's rank; the row within the
-  // unit is the number of lower lanes (lower tokens) with the same expert.
-  const int we = kept ? (e >> 5) : 0;
-  const int below = __shfl_sync(0xFFFFFFFFu, incl - cnt, we);
-  const unsigned same = __match_any_sync(0xFFFFFFFFu, kept ? e : -1 - lane);
+  if (lane == 0) su->kept[warp] = kept_mask;
   if (kept) {
-    const int u = below + __popc(su->bits[we] & ((1u << (e & 31)) - 1u));
-    const int r = __popc(same & ((1u << lane) - 1u));
-    su->row[u][r] = lane;
+    atomicOr(&su->bits[e >> 5], 1u << (e & 31));
+    atomicOr(&emask[e >> 2], 1u << ((e & 3) * 8 + t));
   }
-  __syncwarp();
-  if (lane < units) su->valid[lane] = (su->row[lane][0] >= 0) + (su->row[lane][1] >= 0);
-  if (lane == 0) {
-    su->count = units;
-    su->kept = kept_mask;
+  sync();
+  if (warp == 0) {
+    const unsigned word = su->bits[lane];
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int other = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += other;
+    }
+    su->below[lane] = incl - cnt;
+    int k = incl - cnt;
+    for (unsigned w = word; w != 0; w &= w - 1, ++k) su->expert[k] = lane * 32 + __ffs(w) - 1;
+    if (lane == 31) su->count = incl;
+  }
+  sync();
+  if (kept) {
+    // The unit of a kept pair is its expert's rank; its row is the number of
+    // lower tokens with the same expert.
+    const int u = su->below[e >> 5] + __popc(su->bits[e >> 5] & ((1u << (e & 31)) - 1u));
+    const unsigned m = (emask[e >> 2] >> ((e & 3) * 8)) & 0xFFu;
+    const int r = __popc(m & ((1u << t) - 1u));
+    su->row[u][r] = static_cast<int16_t>(p);
+    if (r == 0) {
+      su->valid[u] = static_cast<uint8_t>(__popc(m));
+      su->tokens[u] = static_cast<uint8_t>(m);
+    }
   }
 }
 
-// MXFP8 of one 128-value K chunk of the call's tokens, from its BF16 rows at
-// img + kXRaw: lane l quantizes values 4l..4l+3 of each token row (the 8
-// lanes of a 32-block combine their maxima, ceil-rule E8M0 scale, e4m3 codes)
-// into row `token` of the chunk's 128B-swizzled image (bytes 0..255, apart
-// from the BF16 rows) and its scale rows.
-__device__ __forceinline__ void quantize_rows(int B, uint8_t* img, uint8_t* atom, int lane) {
-  for (int r = 0; r < B; ++r) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(img + kXRaw + r * 2 * kChunkK + lane * 8);
-    const uint32_t w[2] = {xv.x, xv.y};
-    float v[4];
+// MXFP8 of one token row of a 128-value K chunk: lane l quantizes values
+// 4l..4l+3 (the 8 lanes of a 32-block combine their maxima, ceil-rule E8M0
+// scale, e4m3 codes) into row r of the chunk's 128B-swizzled image and its
+// scale row.
+__device__ __forceinline__ void quantize_one(uint2 xv, int r, uint8_t* img, uint8_t* atom, int lane) {
+  const uint32_t w[2] = {xv.x, xv.y};
+  float v[4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    const int E = mx_exponent(amax, false);
-    const float inv = pow2f(-E);
-    uint32_t codes = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) codes |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
-    *reinterpret_cast<uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4) = codes;
-    if ((lane & 7) == 0) atom[scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
+  for (int i = 0; i < 2; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  const int E = mx_exponent(amax, false);
+  const float inv = pow2f(-E);
+  uint32_t codes = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) codes |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
+  *reinterpret_cast<uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4) = codes;
+  if ((lane & 7) == 0) atom[scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
+}
+
+// One or two tokens: the chunk's BF16 rows sit at img + kXRaw (image rows
+// 4-7, which no token uses).
+__device__ __forceinline__ void quantize_rows(int B, uint8_t* img, uint8_t* atom, int lane) {
+  for (int r = 0; r < B; ++r)
+    quantize_one(*reinterpret_cast<const uint2*>(img + kXRaw + r * 2 * kChunkK + lane * 8), r, img, atom, lane);
 }
 
 // The CTAs that run FC2 jobs of unit u (those holding jobs u * NQ ..
@@ -225,18 +240,20 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
   const int B = a.B;
   Ctx cx{&a, reinterpret_cast<volatile uint32_t*>(&misc[1])};
   uint32_t* counters = a.small_counters + 4 * a.parity;  // [0] segments claimed
-  uint32_t* sums = a.piece_sums + static_cast<size_t>(a.parity) * a.seg_cap * kSmallPieceWords;
+  const int pw = a.piece_words;  // words per segment slot
+  uint32_t* sums = a.piece_sums + static_cast<size_t>(a.parity) * a.seg_cap * pw;
   uint32_t* readers = a.piece_readers + static_cast<size_t>(a.parity) * a.seg_cap;
   const int spi = small_spi(g.KC1);  // segments per item
 
   // The routing ids and this CTA's first FC1 segment first: everything the
   // producer streams depends on them. The x warps load their chunks of x.
+  const int nw = (B * kTopK + 31) / 32;  // warps that derive the unit table (one pair a lane)
   int my_id = -1;
   uint32_t first_claim = 0;
-  if (warp == kProducerWarp && lane < B * kTopK) my_id = a.ids[lane];
+  if (tid < B * kTopK) my_id = a.ids[tid];
   if (tid == 0) first_claim = atomicAdd(counters, 1u);
   const int xw = warp - kGatherWarp;  // x warp 0..4 (warps 5..9)
-  if (xw >= 0 && a.x != nullptr && lane < 16 * B) {
+  if (xw >= 0 && a.x != nullptr && B <= 2 && lane < 16 * B) {
     // Chunk c's BF16 rows, 16 bytes a lane, into its image (all in flight).
     const int r = lane >> 4, j = lane & 15;
     for (int c = xw; c < g.KC1; c += kXWarps)
@@ -269,9 +286,11 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
     for (int i = 0; i < kAgreeSlots; ++i) agree[i] = -1;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp) {
-    derive_units(a, su, lane, my_id);
-    if (lane == 0) MOE_STAMP(17);
+  if (warp < nw) {
+    // The experts' token bits go to the hidden images' region, unused until
+    // the hand-off.
+    derive_units(a, su, reinterpret_cast<uint32_t*>(HC), tid, my_id, nw);
+    if (tid == 0) MOE_STAMP(17);
   }
   if (warp == kMmaWarp0) {
     tmem_alloc(&misc[0], kSmallTmemColumns);
@@ -289,6 +308,33 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
   const bool need_x = misc[2] < static_cast<uint32_t>(NS) || cta < g.KC1;
   const Split sp(units, g, G);
   const int j0 = sp.fc2_begin(cta), j1 = sp.fc2_begin(cta + 1);
+  // This x warp's chunks of x to MXFP8: one or two tokens from the BF16 rows
+  // copied at entry; more from registers, the next chunk's rows loading while
+  // one is quantized.
+  auto quantize_x = [&]() {
+    if (B <= 2) {
+      for (int c = xw; c < g.KC1; c += kXWarps)
+        quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+    } else {
+      uint2 cur[kSmallMaxTokens], nxt[kSmallMaxTokens];
+      auto load = [&](uint2 (&v)[kSmallMaxTokens], int c) {
+#pragma unroll
+        for (int r = 0; r < kSmallMaxTokens; ++r)
+          if (r < B && c < g.KC1)
+            v[r] = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(r) * g.H + c * kChunkK) + lane);
+      };
+      load(cur, xw);
+      for (int c = xw; c < g.KC1; c += kXWarps) {
+        load(nxt, c + kXWarps);
+#pragma unroll
+        for (int r = 0; r < kSmallMaxTokens; ++r)
+          if (r < B) quantize_one(cur[r], r, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+#pragma unroll
+        for (int r = 0; r < kSmallMaxTokens; ++r) cur[r] = nxt[r];
+      }
+    }
+    fence_proxy_async_shared();
+  };
   const int fc1_stages = g.P1 * g.KC1;  // FC2 stages follow the FC1 stages of an expert
 
   if (warp == kProducerWarp) {
@@ -484,25 +530,25 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
     }
   } else if (warp == kGatherWarp) {
     // ------------------------------------------------- activations (FC1)
-    uint32_t back_codes[2] = {0u, 0u}, back_scales = 0u;  // plan read-back of chunk cta
+    uint32_t back_codes[kSmallMaxTokens], back_scales[kSmallMaxTokens];  // plan read-back of chunk cta
     if (a.x != nullptr) {
       // x is an input of the call: quantized without waiting for the
       // previous launch.
-      cp_async_wait_all();
-      __syncwarp();
-      if (need_x) {
-        for (int c = xw; c < g.KC1; c += kXWarps)
-          quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
-        fence_proxy_async_shared();
+      if (B <= 2) {
+        cp_async_wait_all();
+        __syncwarp();
       }
+      if (need_x) quantize_x();
       mbar_arrive(xready);
       if (cta < g.KC1 && wait_bar(cx, xready, 0)) {
         // The plan of chunk cta, read from its image now: the epilogue reuses
         // the images' region once this CTA's FC1 is done.
         const uint8_t* img = XC + cta * kActImageBytes;
-        for (int r = 0; r < B; ++r) {
+#pragma unroll
+        for (int r = 0; r < kSmallMaxTokens; ++r) {
+          if (r >= B) break;
           back_codes[r] = *reinterpret_cast<const uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4);
-          if (lane < 4) back_scales |= static_cast<uint32_t>(XS[cta * kXAtomStride + scale_atom(r, lane)]) << (8 * r);
+          back_scales[r] = lane < 4 ? XS[cta * kXAtomStride + scale_atom(r, lane)] : 0u;
         }
       }
       grid_dependency_wait();
@@ -511,12 +557,14 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       // x once): copy its plan of every chunk into the images.
       grid_dependency_wait();
       for (int c = 0; need_x && c < g.KC1; ++c) {
-        const int r = lane >> 3, c16 = lane & 7;  // rows 0..3 of the image, 16 bytes each
-        const bool tok = r < B;
-        cp_async_16(XC + c * kActImageBytes + swizzle128(r, c16),
-                    a.plan_codes + static_cast<size_t>(tok ? r : 0) * g.H + c * kChunkK + c16 * 16,
-                    tok ? 16u : 0u);
-        if (lane < 2) {
+        for (int r0 = 0; r0 < B; r0 += 4) {  // rows r0 .. r0 + 3 of the image, 16 bytes a lane
+          const int r = r0 + (lane >> 3), c16 = lane & 7;
+          const bool tok = r < B;
+          cp_async_16(XC + c * kActImageBytes + swizzle128(r, c16),
+                      a.plan_codes + static_cast<size_t>(tok ? r : 0) * g.H + c * kChunkK + c16 * 16,
+                      tok ? 16u : 0u);
+        }
+        if (lane < kSmallMaxTokens) {
           const bool st = lane < B;
           cp_async_4(XS + c * kXAtomStride + lane * 16,
                      a.plan_scales + static_cast<size_t>(st ? lane : 0) * (g.H / kBlock) + c * (kChunkK / kBlock),
@@ -542,22 +590,27 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         if (lane == 0) *a.unit_count = units;
         for (int i = lane; i < units * kUnitRows; i += 32) {
           const int uu = i / kUnitRows, r = i % kUnitRows;
-          a.unit_rows[i] = static_cast<int16_t>(r < 2 ? su->row[uu][r] : -1);
+          a.unit_rows[i] = static_cast<int16_t>(r < su->valid[uu] ? su->row[uu][r] : -1);
         }
         for (int uu = lane; uu < units; uu += 32) a.unit_expert[uu] = su->expert[uu];
         const int pairs = B * kTopK;
         if (a.pair_kept != nullptr)
-          for (int pp = lane; pp < pairs; pp += 32) a.pair_kept[pp] = (su->kept >> pp) & 1u;
-        const unsigned all = pairs == 32 ? 0xFFFFFFFFu : (1u << pairs) - 1u;
-        if (lane == 0 && su->kept != all) report(a.status, MOE_ERR_DEVICE_IDS);
+          for (int pp = lane; pp < pairs; pp += 32) a.pair_kept[pp] = (su->kept[pp >> 5] >> (pp & 31)) & 1u;
+        if (lane < nw) {
+          const int left = pairs - 32 * lane;
+          const unsigned all = left >= 32 ? 0xFFFFFFFFu : (1u << left) - 1u;
+          if (su->kept[lane] != all) report(a.status, MOE_ERR_DEVICE_IDS);
+        }
       }
       if (cta < g.KC1) {
-        for (int r = 0; r < B; ++r) {
+#pragma unroll
+        for (int r = 0; r < kSmallMaxTokens; ++r) {
+          if (r >= B) break;
           *reinterpret_cast<uint32_t*>(a.plan_codes + static_cast<size_t>(r) * g.H + cta * kChunkK + lane * 4) =
               back_codes[r];
           if (lane < 4)
             a.plan_scales[static_cast<size_t>(r) * (g.H / kBlock) + cta * (kChunkK / kBlock) + lane] =
-                static_cast<uint8_t>(back_scales >> (8 * r));
+                static_cast<uint8_t>(back_scales[r]);
         }
       }
     }
@@ -570,13 +623,11 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
     const bool fc2_upper_half = g.I > 2 * kBlock;  // issuers 1 and 3 own FC2 K-steps 2-3
     // Its share of the x chunks first.
     if (a.x != nullptr) {
-      cp_async_wait_all();
-      __syncwarp();
-      if (need_x) {
-        for (int c = xw; c < g.KC1; c += kXWarps)
-          quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
-        fence_proxy_async_shared();
+      if (B <= 2) {
+        cp_async_wait_all();
+        __syncwarp();
       }
+      if (need_x) quantize_x();
     }
     mbar_arrive(xready);
     if (et == 0) MOE_STAMP(28);
@@ -628,12 +679,12 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           for (int p0 = 0; p0 < g.P1; p0 += ipb) {
             const int p1 = p0 + ipb < g.P1 ? p0 + ipb : g.P1;
             const int copies = (p1 - p0) * spi * rows * (kTileM / 4);
-            const uint32_t* from = sums + static_cast<size_t>(seg0 + p0 * spi) * kSmallPieceWords;
+            const uint32_t* from = sums + static_cast<size_t>(seg0 + p0 * spi) * pw;
             auto copy = [&](int i) {  // copy i: segment i / (rows * 32), row (i / 32) % rows, 16 bytes i % 32
               const int e = i / (rows * 32), rr = (i >> 5) - e * rows, c4 = (i & 31) * 4;
               const int row = rr < valid ? rr : B + rr - valid;
               cp_async_16(land + (e * rows + rr) * kTileM + c4,
-                          from + static_cast<size_t>(e) * kSmallPieceWords + row * kTileM + c4, 16u);
+                          from + static_cast<size_t>(e) * pw + row * kTileM + c4, 16u);
             };
             for (int i = et; i < copies; i += 128) copy(i);
             const uint64_t t_wait = global_timer_ns();
@@ -703,8 +754,8 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           for (int e = et; e < nseg; e += 128) {
             const int s = seg0 + e;
             if (atom_add_acq_rel_gpu(readers + s, 1u) + 1u == static_cast<uint32_t>(nreaders)) {
-              uint4* w = reinterpret_cast<uint4*>(sums + static_cast<size_t>(s) * kSmallPieceWords);
-              for (int i = 0; i < kSmallPieceWords / 4; ++i)
+              uint4* w = reinterpret_cast<uint4*>(sums + static_cast<size_t>(s) * pw);
+              for (int i = 0; i < 2 * B * kTileM / 4; ++i)  // the words this call's tokens use
                 w[i] = make_uint4(kPieceSentinel, kPieceSentinel, kPieceSentinel, kPieceSentinel);
               readers[s] = 0u;
             }
@@ -767,15 +818,16 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         // rows. A sum with the sentinel's bit pattern (a NaN) is stored as
         // the canonical NaN.
         const int seg = md.y, u = seg / (g.P1 * spi);
-        const int valid = su->valid[u];
         if (u != a.withhold_unit) {
-          uint32_t* dst = sums + static_cast<size_t>(seg) * kSmallPieceWords;
+          // Token j's column goes to the unit row of token j, if it has one.
+          uint32_t* dst = sums + static_cast<size_t>(seg) * pw;
+          const unsigned tokens = su->tokens[u];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (t >= valid) break;
-            const bool second = (su->row[u][t] >> 4) != 0;  // the row's token
-            const uint32_t gb = __float_as_uint(second ? v0[1] : v0[0]);
-            const uint32_t ub = __float_as_uint(second ? v1[1] : v1[0]);
+          for (int j = 0; j < kSmallMaxTokens; ++j) {
+            if (j >= B) break;
+            if (!((tokens >> j) & 1u)) continue;
+            const int t = __popc(tokens & ((1u << j) - 1u));
+            const uint32_t gb = __float_as_uint(v0[j]), ub = __float_as_uint(v1[j]);
             dst[t * kTileM + m] = gb == kPieceSentinel ? 0x7FFFFFFFu : gb;
             dst[(B + t) * kTileM + m] = ub == kPieceSentinel ? 0x7FFFFFFFu : ub;
           }
@@ -786,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         const int valid = await_prev() ? su->valid[u] : 0;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < kUnitRows; ++t) {
           if (t >= valid) break;
           // Each warp writes its 32 outputs of each tile as four 16-byte stores.
           uint16_t* dst = a.out + static_cast<size_t>(su->row[u][t]) * g.H + qq * 2 * kTileM + q * 32;
@@ -829,12 +881,12 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
 
 }  // namespace
 
-// The small-batch kernel serves a call when it has at most two tokens, the
+// The small-batch kernel serves a call when it has at most eight tokens, the
 // layer has at most MOE_MAX_EXPERTS experts (the kept-expert bitmap), its
 // shared-memory layout fits, and no CTA's FC2 jobs span more units than it
 // has hidden images for.
 bool small_fits(const Geometry& g, int batch, int grid) {
-  if (batch > 2 || grid > kMaxGrid || SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
+  if (batch > kSmallMaxTokens || grid > kMaxGrid || SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
   // The hidden build lands one item's segments (two rows per token) in the x images' region.
   const int spi = small_spi(g.KC1);
   if (spi * 2 * batch * kTileM * 4 > g.KC1 * kActImageBytes) return false;

@@ -311,18 +311,19 @@ def test_supported_limits(moe, E, H, I, B, dist):
 SMALL_PATHS = [1, 2]  # the small-batch kernel, the cluster variant
 
 
-SMALL_MAX_HIDDEN = 3584  # at I = 512 the small-batch kernel's x images of all K chunks (28) fit its half SM
+SMALL_MAX_HIDDEN = 3328  # at I = 512 the small-batch kernel's x images of all K chunks (26) fit its half SM
+SMALL_TOO_WIDE = {(16384, 512), (SMALL_MAX_HIDDEN + 256, 512)}  # (H, I) the small-batch kernel leaves to the grid
 
 
-def set_path(moe, layer, path, batch, hidden=None):
-    """Select an experts kernel for calls of `batch` tokens and check that it serves them
-    (the small-batch kernel serves layers up to SMALL_MAX_HIDDEN wide; wider ones fall
-    back to the grid kernel)."""
+def set_path(moe, layer, path, batch, shape=None):
+    """Select an experts kernel for calls of `batch` tokens and check that it serves them.
+    Paths 1 and 3 both run the small-batch kernel, which leaves the (H, I) shapes in
+    SMALL_TOO_WIDE (its per-chunk x images would not fit half an SM) to the grid kernel."""
     moe.moe_debug_paths(layer.handle, path)
-    if path == 1 and hidden is not None and hidden > SMALL_MAX_HIDDEN:
+    if path in (1, 3) and shape is not None and tuple(shape) in SMALL_TOO_WIDE:
         assert moe.moe_kernel_path(layer.handle, batch) == 0
         return
-    assert moe.moe_kernel_path(layer.handle, batch) == path
+    assert moe.moe_kernel_path(layer.handle, batch) == (1 if path == 3 else path)
     if path == 2:
         assert moe.moe_cluster_size(layer.handle, batch) >= 2
 
@@ -342,7 +343,7 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
     import torch
 
     layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
-    set_path(moe, layer, path, B, hidden=H)
+    set_path(moe, layer, path, B, shape=(H, I))
     print(f"[E={E} H={H} I={I} B={B}] path {path}, clusters of {moe.moe_cluster_size(layer.handle, B)}")
     x = workload.make_x(B, H, seed=33)
     ids = workload.make_ids(B, E, seed=34) if E >= 16 else np.stack(
@@ -363,16 +364,16 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
     layer.close()
 
 
-@pytest.mark.parametrize("B", [1, 2])
+@pytest.mark.parametrize("B", [1, 2, 8])
 def test_small_batch_widest_hidden(moe, B):
-    """The widest layer the small-batch kernel serves at the widest I (28 K chunks of x
-    in shared memory, two CTAs per SM), against the oracle."""
+    """The widest layer the small-batch kernel serves at the widest I (26 K chunks of x
+    in shared memory, two CTAs per SM), against the oracle; one chunk more falls back."""
     E, H, I = 16, SMALL_MAX_HIDDEN, 512
     weights = workload.make_weights(E, H, I, seed13=36, seed2=37)
     import torch
 
     layer = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0") for w in weights))
-    set_path(moe, layer, 1, B, hidden=H)
+    set_path(moe, layer, 1 if B <= 2 else 3, B, shape=(H, I))
     x = workload.make_x(B, H, seed=38)
     ids = workload.make_ids(B, E, seed=39)
     got, status = run_layer(moe, layer, x, ids)
@@ -381,6 +382,54 @@ def test_small_batch_widest_hidden(moe, B):
     ref = oracle.pairs_forward(weights, xq, xs, ids)
     check_rows(got, ref["out"], f"small E={E} H={H} I={I} B={B}")
     layer.close()
+    wider = moe.MoeLayer(tuple(torch.from_numpy(w).to("cuda:0")
+                               for w in workload.make_weights(E, H + 256, I, seed13=36, seed2=37)))
+    set_path(moe, wider, 1 if B <= 2 else 3, B, shape=(H + 256, I))
+    wider.close()
+
+
+@pytest.mark.parametrize("shape,B", [((32, 1024, 128), 3), ((32, 1024, 128), 5), ((32, 1024, 128), 8),
+                                     ("tp16_b8", 8)])
+def test_small_batch_wide_path(moe, shape, B):
+    """Path 3: the small-batch kernel for calls of up to eight tokens (one FC1 segment
+    holds eight token rows per tile; the hand-off lands them all), against the oracle.
+    Path 1 sends the same calls to the grid kernel."""
+    if shape == "tp16_b8":
+        weights, _, _ = cached_inputs(shape)
+    else:
+        weights = workload.make_weights(*shape, seed13=42, seed2=43)
+    layer = layer_for(moe, weights)
+    E, H = weights[0].shape[0], layer.hidden
+    x = workload.make_x(B, H, seed=44 + B)
+    ids = workload.make_ids(B, E, seed=45 + B)
+    try:
+        moe.moe_debug_paths(layer.handle, 1)
+        assert moe.moe_kernel_path(layer.handle, B) == 0
+        set_path(moe, layer, 3, B)
+        got, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        again, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
+    xq, xs = oracle.quantize_x(x)
+    ref = oracle.pairs_forward(weights, xq, xs, ids)
+    check_rows(got, ref["out"], f"path 3 {shape} B={B}")
+    assert np.array_equal(got, again)
+
+
+def test_small_batch_wide_path_falls_back(moe):
+    """Where three tokens' segment sums would not fit the x images' region (H = 256:
+    two K chunks), path 3 leaves the call to the grid kernel; one and two tokens stay."""
+    weights, _, _ = cached_inputs("tiny")
+    layer = layer_for(moe, weights)
+    try:
+        moe.moe_debug_paths(layer.handle, 3)
+        assert [moe.moe_kernel_path(layer.handle, b) for b in (1, 2, 3, 8)] == [1, 1, 0, 0]
+        with pytest.raises(moe.MoeError):
+            moe.moe_debug_paths(layer.handle, 4)
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
 
 
 @pytest.mark.parametrize("path", SMALL_PATHS, ids=["small", "cluster"])
