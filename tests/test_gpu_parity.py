@@ -389,7 +389,7 @@ def test_small_batch_widest_hidden(moe, B):
 
 
 @pytest.mark.parametrize("shape,B", [((32, 1024, 128), 3), ((32, 1024, 128), 5), ((32, 1024, 128), 8),
-                                     ("tp16_b8", 8)])
+                                     ((16, 512, 96), 3), ((16, 512, 96), 4), ("tp16_b8", 8)])
 def test_small_batch_wide_path(moe, shape, B):
     """Path 3: the small-batch kernel for calls of up to eight tokens (one FC1 segment
     holds eight token rows per tile; the hand-off lands them all), against the oracle.
@@ -416,6 +416,58 @@ def test_small_batch_wide_path(moe, shape, B):
     ref = oracle.pairs_forward(weights, xq, xs, ids)
     check_rows(got, ref["out"], f"path 3 {shape} B={B}")
     assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("B", [5, 8])
+def test_small_batch_wide_path_reads_back_and_reports_bad_ids(moe, B):
+    """Path 3 at five and eight tokens over 32 experts, so most units hold several tokens'
+    rows (the unit table spans several warps and the token masks): the plan and unit table
+    left for read-back are the oracle's, bit for bit. A call with a repeated and two
+    out-of-range ids reports them and keeps every other pair exact; the table it leaves
+    drops those pairs; the next call gives the first call's bits again."""
+    weights = workload.make_weights(32, 1024, 128, seed13=52, seed2=53)
+    layer = layer_for(moe, weights)
+    x = workload.make_x(B, 1024, seed=54 + B)
+    ids = workload.make_ids(B, 32, seed=55 + B)
+    xq, xs = oracle.quantize_x(x)
+    try:
+        set_path(moe, layer, 3, B)
+        first, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        codes = np.zeros((B, 1024), np.uint8)
+        scales = np.zeros((B, 1024 // 32), np.uint8)
+        moe.moe_copy_plan(layer.handle, codes, scales, B)
+        np.testing.assert_array_equal(codes, xq)
+        np.testing.assert_array_equal(scales, xs)
+        experts, rows = units_of(moe, layer, B)
+        ref_e, ref_r = oracle.group(ids, 32)
+        assert (ref_r >= 0).sum(axis=1).max() >= 2  # units of several rows
+        np.testing.assert_array_equal(experts, ref_e)
+        np.testing.assert_array_equal(rows, ref_r)
+        check_rows(first, oracle.pairs_forward(weights, xq, xs, ids)["out"], f"path 3 E32 B={B}")
+
+        bad = ids.copy()
+        bad[1, 9] = bad[1, 3]   # a repeat: slot 9 is dropped
+        bad[B - 1, 0] = -1      # out of range
+        bad[B - 1, 15] = 32     # out of range
+        dropped = {1 * 16 + 9, (B - 1) * 16, (B - 1) * 16 + 15}
+        got, status = run_layer(moe, layer, x, bad)
+        assert status == moe.MOE_ERR_DEVICE_IDS
+        keep = np.array([p for p in range(B * 16) if p not in dropped], np.int32)
+        check_rows(got[keep], oracle.pairs_forward(weights, xq, xs, bad, pairs=keep)["out"],
+                   f"path 3 E32 B={B} with bad ids")
+        clean = bad.copy()
+        clean[1, 9] = -1
+        experts, rows = units_of(moe, layer, B)
+        ref_e, ref_r = oracle.group(clean, 32)
+        np.testing.assert_array_equal(experts, ref_e)
+        np.testing.assert_array_equal(rows, ref_r)
+
+        again, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        np.testing.assert_array_equal(again, first)
+    finally:
+        moe.moe_debug_paths(layer.handle, 1)
 
 
 def test_small_batch_wide_path_falls_back(moe):
