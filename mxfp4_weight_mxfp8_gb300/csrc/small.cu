@@ -1,4 +1,4 @@
-// Kernel 3 (+4) for calls of one or two tokens: the small-batch experts kernel.
+// Kernel 3 (+4) for calls of up to eight tokens: the small-batch experts kernel.
 //
 // Pages: ...cutedsl.moe.experts (ExpertsKernel: the TMA producer warp, the
 // block-scaled FC1/FC2 tcgen05 stages, store_hidden, the hidden exchange
@@ -9,12 +9,12 @@
 // parity).
 //
 // The persistent grid kernel's roles, ring and MMAs, with these changes for a
-// call of at most 32 (token, slot) pairs:
+// call of at most 128 (token, slot) pairs:
 //   - A call on device buffers is this one launch: no prep grid runs before
 //     it (calls on host buffers keep the prep grid, which reads x once, and
 //     copy its plan). Every CTA derives the unit table from the routing ids
-//     itself (warp 0: one pair per lane; a unit per distinct kept expert,
-//     experts ascending, rows in token order: the canonical table), and five
+//     itself (one pair per thread; a unit per distinct kept expert, experts
+//     ascending, rows in token order: the canonical table), and five
 //     warps quantize x to MXFP8 once, into a shared-memory image per K chunk
 //     that holds every token of the call (the FC1 MMA computes all tokens for
 //     each expert; the epilogue keeps the unit's own columns). For
@@ -41,6 +41,11 @@
 //     copies) waits for the previous call to end, and a CTA lets the next
 //     launch start only after that wait, so the call after next finds this
 //     call's half at rest.
+//   - Two builds (SmallCfg below): calls of one or two tokens take the packed
+//     one, whose x and hidden images start 256 bytes apart, which leaves room
+//     for a 3-slot weight ring in half an SM; the wide one (2 slots, full
+//     8-row images) serves up to eight tokens and the layers too wide for
+//     the packed one.
 // The warp roles: warp 0 TMA producer, warps 1-4 MMA issuers, warp 5 the
 // activations (x quantization; the wait for the previous call; read-back),
 // warps 6-9 the epilogue (x quantization first; FC1 segment sums; the hidden
@@ -51,20 +56,49 @@ namespace moe {
 namespace {
 
 constexpr int kSmallMaxTokens = kSmallMaxBatch;  // tokens of a call (one unit per expert: <= 8 rows)
-constexpr int kSmallMaxUnits = kSmallMaxTokens * kTopK;  // distinct experts of the call
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
-constexpr int kSmallSlots = 2;             // weight ring depth (two CTAs share an SM)
 constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
 constexpr int kXRaw = 512;                 // x of chunk c lands at byte 512 of its image (rows 4-7, unused)
-constexpr int kXAtomStride = kUnitRows * 16;  // scale rows 0..7 of chunk c's atom (an N = 8 MMA reads no more)
 // Two CTAs per SM, one of each of two consecutive calls, so that one streams
 // while the other hands off and runs its FC2 jobs: each takes at most half of
 // the SM's 228 KB of shared memory (less 1 KB reserved per CTA) and half of
 // its 512 TMEM columns.
 constexpr int kSmemLimit = (233472 - 2 * 1024) / 2;  // dynamic shared memory one CTA may take
 constexpr int kSmallTmemColumns = 256;
-constexpr int kSmallHiddenScaleBase = kTmemScaleBase + kSmallSlots * kSlotScaleColumns;  // 2 x 16 columns
-static_assert(kSmallHiddenScaleBase + 2 * 16 <= kSmallTmemColumns, "the small kernel's TMEM columns");
+
+// The two builds of the kernel:
+//   - Wide: a 2-slot weight ring, and for every K chunk a full 8-row image
+//     of the call's tokens (an N = 8 MMA reads 8 rows of 128 bytes); up to 8
+//     tokens.
+//   - Packed: one or two tokens. An MMA still reads 8 rows per K chunk, but
+//     only rows 0 and 1 hold tokens, so chunk images start 256 bytes apart
+//     and a chunk's rows 2-7 are the next chunks' rows (their output columns
+//     are never read). The same for the hidden images and the scale atoms
+//     (rows 16 bytes apart: 32 bytes a chunk). That frees the shared memory
+//     of a third ring slot. The bytes of a row keep the 128-byte swizzle of
+//     their absolute shared-memory address (the pattern a TMA copy writes:
+//     16-byte chunk j of the row at address A sits at chunk j ^ (A >> 7) & 7),
+//     and the MMA reads them back through a descriptor whose start is the
+//     image's (a multiple of 256 bytes) and whose base offset is 0: it
+//     swizzles the addresses it forms, as for the K steps inside an atom.
+template <int S, bool P>
+struct SmallCfg {
+  static constexpr int kSlots = S;                                  // weight ring depth
+  static constexpr int kMaxUnits = (P ? 2 : kSmallMaxTokens) * kTopK;  // distinct experts of a call
+  static constexpr int kImage = P ? 256 : kActImageBytes;          // bytes between chunk images
+  static constexpr int kXScale = P ? 32 : kUnitRows * 16;          // bytes between x scale atoms
+  static constexpr int kHScale = P ? 32 : kScaleAtomBytes;         // bytes between hidden scale atoms
+  static constexpr int kHiddenScaleBase = kTmemScaleBase + S * kSlotScaleColumns;  // 2 units x 16 columns
+  static_assert(kHiddenScaleBase + 2 * 16 <= kSmallTmemColumns, "the small kernel's TMEM columns");
+  // Byte offset of the 16-byte chunk c16 of row r of image i in a region
+  // that starts on a 1024-byte boundary.
+  __host__ __device__ static constexpr uint32_t at(int i, int r, int c16) {
+    return static_cast<uint32_t>(i * kImage + r * 128) +
+           ((static_cast<uint32_t>(c16) ^ (static_cast<uint32_t>(i * kImage / 128 + r) & 7u)) << 4);
+  }
+};
+using WideCfg = SmallCfg<2, false>;
+using PackedCfg = SmallCfg<3, true>;
 
 // Stage descriptors, one per ring slot in shared memory: the producer writes
 // it before arriving on the slot's full barrier.
@@ -79,38 +113,49 @@ __device__ __forceinline__ uint32_t stage_desc(int seg, int c, bool first, bool 
 
 // The unit table of the call, in shared memory: one unit per kept expert
 // (at most 8 tokens, so at most 8 rows).
+template <int U>
 struct SmallUnits {
   int count;
-  int expert[kSmallMaxUnits];
-  int16_t row[kSmallMaxUnits][kUnitRows];  // pair t * 16 + s of rows 0 .. valid - 1
-  uint8_t valid[kSmallMaxUnits];
-  uint8_t tokens[kSmallMaxUnits];          // bit t: token t has a row in the unit
+  int expert[U];
+  int16_t row[U][kUnitRows];               // pair t * 16 + s of rows 0 .. valid - 1
+  uint8_t valid[U];
+  uint8_t tokens[U];                       // bit t: token t has a row in the unit
   unsigned bits[MOE_MAX_EXPERTS / 32];     // kept experts
   int below[MOE_MAX_EXPERTS / 32];         // units of the experts in lower words of bits
-  unsigned kept[kSmallMaxUnits / 32];      // bit p % 32 of word p / 32: pair p got a unit row
+  unsigned kept[U / 32];                   // bit p % 32 of word p / 32: pair p got a unit row
 };
 
-// Shared-memory carve-up of the small kernel (images on 1024-byte boundaries).
+// Shared-memory carve-up of the small kernel (image regions on 1024-byte
+// boundaries). An operand read past a region's last image or scale atom
+// (the rows and scale rows no token uses) reads the regions after it; the
+// end guard keeps every such read inside the allocation.
+template <class C>
 struct SmallLayout {
-  int w, xc, hcodes, xs, asf, hsf, table, bars, meta, desc, misc, agree, bytes;
+  int w, asf, hcodes, xc, xs, hsf, table, bars, meta, desc, misc, agree, bytes;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
   __host__ __device__ SmallLayout(int kc1, int kc2) {
     int o = 0;
-    w = o;                    o += kSmallSlots * kStageSmemWeights;
-    xc = o = up(o, 1024);     o += kc1 * kActImageBytes;
-    hcodes = o = up(o, 1024); o += kSmallHidden * kc2 * kActImageBytes;
-    xs = o = up(o, 16);       o += kc1 * kXAtomStride + (kScaleAtomBytes - kXAtomStride);
-    asf = o = up(o, 16);      o += kSmallSlots * 2 * kScaleAtomBytes;
-    hsf = o = up(o, 16);      o += kSmallHidden * kc2 * kScaleAtomBytes;
-    table = o = up(o, 16);    o += static_cast<int>(sizeof(SmallUnits));
+    w = o;                    o += C::kSlots * kStageSmemWeights;
+    asf = o;                  o += C::kSlots * 2 * kScaleAtomBytes;
+    hcodes = o = up(o, 1024); o += kSmallHidden * kc2 * C::kImage;
+    xc = o = up(o, 1024);     o += kc1 * C::kImage;
+    xs = o = up(o, 16);       o += kc1 * C::kXScale;
+    hsf = o = up(o, 16);      o += kSmallHidden * kc2 * C::kHScale;
+    table = o = up(o, 16);    o += static_cast<int>(sizeof(SmallUnits<C::kMaxUnits>));
     // full, empty per slot; accfull, accempty per set; hfull per unit;
     // drained per issuer; x ready; previous call done.
-    bars = o = up(o, 16);     o += (2 * kSmallSlots + 2 * NACC + kSmallHidden + kMmaWarps + 2) * 8;
+    bars = o = up(o, 16);     o += (2 * C::kSlots + 2 * NACC + kSmallHidden + kMmaWarps + 2) * 8;
     meta = o = up(o, 16);     o += NACC * 16;
-    desc = o = up(o, 16);     o += kSmallSlots * 4;
+    desc = o = up(o, 16);     o += C::kSlots * 4;
     misc = o = up(o, 16);     o += 16;
     agree = o = up(o, 16);    o += kAgreeSlots * 4;
-    bytes = o + 1024;  // slack for aligning the dynamic shared-memory base to 1024
+    int end = o;
+    const int reads[4] = {xc + kc1 * C::kImage + (kActImageBytes - C::kImage),
+                          hcodes + kSmallHidden * kc2 * C::kImage + (kActImageBytes - C::kImage),
+                          xs + kc1 * C::kXScale + (kScaleAtomBytes - C::kXScale),
+                          hsf + kSmallHidden * kc2 * C::kHScale + (kScaleAtomBytes - C::kHScale)};
+    for (int r : reads) end = end > r ? end : r;
+    bytes = end + 1024;  // slack for aligning the dynamic shared-memory base to 1024
   }
 };
 
@@ -120,7 +165,8 @@ struct SmallLayout {
 // ascending order (at most 8 tokens: one unit per expert); its rows are its
 // pairs in token order. `emask` (shared memory, E / 4 words) holds each
 // expert's token bits while the table is built.
-__device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, uint32_t* emask, int p, int e, int nw) {
+template <class SU>
+__device__ void derive_units(const ExpertsArgs& a, SU* su, uint32_t* emask, int p, int e, int nw) {
   const int pairs = a.B * kTopK, lane = p & 31, warp = p >> 5, E = a.g.E;
   auto sync = [&]() { asm volatile("bar.sync 3, %0;" ::"r"(nw * 32) : "memory"); };
   for (int i = p; i < MOE_MAX_EXPERTS / 32; i += nw * 32) su->bits[i] = 0;
@@ -169,9 +215,10 @@ __device__ void derive_units(const ExpertsArgs& a, SmallUnits* su, uint32_t* ema
 
 // MXFP8 of one token row of a 128-value K chunk: lane l quantizes values
 // 4l..4l+3 (the 8 lanes of a 32-block combine their maxima, ceil-rule E8M0
-// scale, e4m3 codes) into row r of the chunk's 128B-swizzled image and its
-// scale row.
-__device__ __forceinline__ void quantize_one(uint2 xv, int r, uint8_t* img, uint8_t* atom, int lane) {
+// scale, e4m3 codes) into row r of image c of the x images (128B-swizzled)
+// and its scale row.
+template <class C>
+__device__ __forceinline__ void quantize_one(uint2 xv, int r, int c, uint8_t* xc, uint8_t* xs, int lane) {
   const uint32_t w[2] = {xv.x, xv.y};
   float v[4];
 #pragma unroll
@@ -188,15 +235,8 @@ __device__ __forceinline__ void quantize_one(uint2 xv, int r, uint8_t* img, uint
   uint32_t codes = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) codes |= static_cast<uint32_t>(e4m3_code(v[i] * inv)) << (8 * i);
-  *reinterpret_cast<uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4) = codes;
-  if ((lane & 7) == 0) atom[scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
-}
-
-// One or two tokens: the chunk's BF16 rows sit at img + kXRaw (image rows
-// 4-7, which no token uses).
-__device__ __forceinline__ void quantize_rows(int B, uint8_t* img, uint8_t* atom, int lane) {
-  for (int r = 0; r < B; ++r)
-    quantize_one(*reinterpret_cast<const uint2*>(img + kXRaw + r * 2 * kChunkK + lane * 8), r, img, atom, lane);
+  *reinterpret_cast<uint32_t*>(xc + C::at(c, r, lane >> 2) + (lane & 3) * 4) = codes;
+  if ((lane & 7) == 0) xs[c * C::kXScale + scale_atom(r, lane >> 3)] = static_cast<uint8_t>(E + 127);
 }
 
 // The CTAs that run FC2 jobs of unit u (those holding jobs u * NQ ..
@@ -209,22 +249,26 @@ __device__ __forceinline__ int unit_consumers(const Split& sp, const Geometry& g
   return n;
 }
 
+template <class C>
 __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constant__ ExpertsArgs a) {
+  constexpr int S = C::kSlots;
+  constexpr bool kPacked = C::kImage < kActImageBytes;
+  using Units = SmallUnits<C::kMaxUnits>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const Geometry& g = a.g;
-  const SmallLayout L(g.KC1, g.KC2);
+  const SmallLayout<C> L(g.KC1, g.KC2);
   uint8_t* W = sm + L.w;
   uint8_t* XC = sm + L.xc;
   uint8_t* XS = sm + L.xs;
   uint8_t* ASF = sm + L.asf;
   uint8_t* HC = sm + L.hcodes;
   uint8_t* HSF = sm + L.hsf;
-  SmallUnits* su = reinterpret_cast<SmallUnits*>(sm + L.table);
+  Units* su = reinterpret_cast<Units*>(sm + L.table);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
-  uint64_t* empty = full + kSmallSlots;
-  uint64_t* accfull = empty + kSmallSlots;
+  uint64_t* empty = full + S;
+  uint64_t* accfull = empty + S;
   uint64_t* accempty = accfull + NACC;
   uint64_t* hfull = accempty + NACC;
   uint64_t* drained = hfull + kSmallHidden;  // [issuer]
@@ -253,17 +297,22 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
   if (tid < B * kTopK) my_id = a.ids[tid];
   if (tid == 0) first_claim = atomicAdd(counters, 1u);
   const int xw = warp - kGatherWarp;  // x warp 0..4 (warps 5..9)
+  // One or two tokens: chunk c's BF16 rows (256 bytes each) go to rows 4-7 of
+  // its wide image, which no token uses, or to the packed build's last ring
+  // slot, whose first weights the producer loads only once x is quantized.
+  auto x_raw = [&](int c) -> uint8_t* {
+    return kPacked ? W + (S - 1) * kStageSmemWeights + c * 2 * 2 * kChunkK : XC + c * kActImageBytes + kXRaw;
+  };
   if (xw >= 0 && a.x != nullptr && B <= 2 && lane < 16 * B) {
-    // Chunk c's BF16 rows, 16 bytes a lane, into its image (all in flight).
+    // Chunk c's BF16 rows, 16 bytes a lane (all in flight).
     const int r = lane >> 4, j = lane & 15;
     for (int c = xw; c < g.KC1; c += kXWarps)
-      cp_async_16(XC + c * kActImageBytes + kXRaw + r * 2 * kChunkK + j * 16,
-                  a.x + static_cast<size_t>(r) * g.H + c * kChunkK + j * 8, 16u);
+      cp_async_16(x_raw(c) + r * 2 * kChunkK + j * 16, a.x + static_cast<size_t>(r) * g.H + c * kChunkK + j * 8, 16u);
   }
   if (tid == 0) {
     span_enter(a.span);
     MOE_STAMP(0);
-    for (int s = 0; s < kSmallSlots; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);            // the producer (with the bytes, or a descriptor alone)
       mbar_init(&empty[s], kMmaWarps);   // one commit (or arrival) per issuer
     }
@@ -287,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
     fence_mbar_init();
   }
   if (warp < nw) {
-    // The experts' token bits go to the hidden images' region, unused until
-    // the hand-off.
+    // The experts' token bits (at most 1 KB) go to the hidden images' region
+    // and, in the packed build, on into the x images' region: neither is
+    // written before the block barrier below.
     derive_units(a, su, reinterpret_cast<uint32_t*>(HC), tid, my_id, nw);
     if (tid == 0) MOE_STAMP(17);
   }
@@ -314,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
   auto quantize_x = [&]() {
     if (B <= 2) {
       for (int c = xw; c < g.KC1; c += kXWarps)
-        quantize_rows(B, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+        for (int r = 0; r < B; ++r)
+          quantize_one<C>(*reinterpret_cast<const uint2*>(x_raw(c) + r * 2 * kChunkK + lane * 8), r, c, XC, XS, lane);
     } else {
       uint2 cur[kSmallMaxTokens], nxt[kSmallMaxTokens];
       auto load = [&](uint2 (&v)[kSmallMaxTokens], int c) {
@@ -328,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         load(nxt, c + kXWarps);
 #pragma unroll
         for (int r = 0; r < kSmallMaxTokens; ++r)
-          if (r < B) quantize_one(cur[r], r, XC + c * kActImageBytes, XS + c * kXAtomStride, lane);
+          if (r < B) quantize_one<C>(cur[r], r, c, XC, XS, lane);
 #pragma unroll
         for (int r = 0; r < kSmallMaxTokens; ++r) cur[r] = nxt[r];
       }
@@ -345,7 +396,10 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       uint32_t phase = 0;
       bool ok = true;
       auto issue = [&](int stage, uint32_t desc) {
-        if (n >= kSmallSlots && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
+        if (n >= S && !wait_bar(cx, &empty[slot], phase ^ 1)) return false;
+        // The packed build's last slot holds the BF16 rows of x until the
+        // x warps have quantized them.
+        if (kPacked && n == S - 1 && !wait_bar(cx, xready, 0)) return false;
         sdesc[slot] = desc;
         if (desc == kDescEnd) {
           mbar_arrive(&full[slot]);
@@ -360,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           MOE_STAMP(2);
         }
         ++n;
-        if (++slot == kSmallSlots) {
+        if (++slot == S) {
           slot = 0;
           phase ^= 1;
         }
@@ -395,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       MOE_STAMP_VALUE(15, static_cast<uint64_t>(n));
       // Drain: every issued stage consumed and released before exit.
       if (ok)
-        for (int k = (n > kSmallSlots ? n - kSmallSlots : 0); k < n && ok; ++k)
-          ok = wait_bar(cx, &empty[k % kSmallSlots], (k / kSmallSlots) & 1);
+        for (int k = (n > S ? n - S : 0); k < n && ok; ++k)
+          ok = wait_bar(cx, &empty[k % S], (k / S) & 1);
       if (!ok) settle_copies();
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
@@ -405,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       const int issuer = warp - kMmaWarp0, t = issuer >> 1, k0 = 2 * (issuer & 1);
       const bool lead = issuer == 0;  // writes the accumulator metadata
       // The hidden scale atoms, copied into TMEM once per unit by the epilogue.
-      const uint32_t hsf_cols = tmem + kSmallHiddenScaleBase;
+      const uint32_t hsf_cols = tmem + C::kHiddenScaleBase;
       int n = 0, slot = 0, k = 0, ordinal = -1, cu = -1, hb = 0;
       uint32_t phase = 0;
       bool ok = true, have_x = false, fc2_seen = false;
@@ -415,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       };
       auto advance = [&]() {
         ++n;
-        if (++slot == kSmallSlots) {
+        if (++slot == S) {
           slot = 0;
           phase ^= 1;
         }
@@ -443,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         tc_fence_after_sync();
         const uint32_t sf = tmem + kTmemScaleBase + slot * kSlotScaleColumns + issuer * 8;
         tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
-        tc_copy_scales(sf + 4, desc_scales(XS + c * kXAtomStride));
+        tc_copy_scales(sf + 4, desc_scales(XS + c * C::kXScale));
         const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
-        const uint64_t dx = desc_sw128(XC + c * kActImageBytes + k0 * 32);
+        const uint64_t dx = desc_sw128(XC + c * C::kImage + k0 * 32);
         const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
         // Descriptor start addresses count 16-byte units: +2 is the next K-step.
         tc_mma_mxf8f6f4(dt, dw, dx, mma_idesc(k0), sf, sf + 4, (d & kDescFirst) ? 0u : 1u);
@@ -499,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
             const uint32_t sfh = hsf_cols + hb * 16 + c * 4;
             tc_copy_scales(sf, desc_scales(ASF + slot * 2 * kScaleAtomBytes + t * kScaleAtomBytes));
             const uint64_t dw = desc_sw128(W + slot * kStageSmemWeights + t * (kStageSmemWeights / 2) + k0 * 32);
-            const uint64_t dh = desc_sw128(HC + hc * kActImageBytes + k0 * 32);
+            const uint64_t dh = desc_sw128(HC + hc * C::kImage + k0 * 32);
             const uint32_t dt = tmem + set * kAccSetColumns + issuer * 8;
             tc_mma_mxf8f6f4(dt, dw, dh, mma_idesc(k0), sf, sfh, started ? 1u : 0u);
             if (k0 + 1 < ksteps)
@@ -543,12 +597,11 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
       if (cta < g.KC1 && wait_bar(cx, xready, 0)) {
         // The plan of chunk cta, read from its image now: the epilogue reuses
         // the images' region once this CTA's FC1 is done.
-        const uint8_t* img = XC + cta * kActImageBytes;
 #pragma unroll
         for (int r = 0; r < kSmallMaxTokens; ++r) {
           if (r >= B) break;
-          back_codes[r] = *reinterpret_cast<const uint32_t*>(img + swizzle128(r, lane >> 2) + (lane & 3) * 4);
-          back_scales[r] = lane < 4 ? XS[cta * kXAtomStride + scale_atom(r, lane)] : 0u;
+          back_codes[r] = *reinterpret_cast<const uint32_t*>(XC + C::at(cta, r, lane >> 2) + (lane & 3) * 4);
+          back_scales[r] = lane < 4 ? XS[cta * C::kXScale + scale_atom(r, lane)] : 0u;
         }
       }
       grid_dependency_wait();
@@ -560,13 +613,15 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         for (int r0 = 0; r0 < B; r0 += 4) {  // rows r0 .. r0 + 3 of the image, 16 bytes a lane
           const int r = r0 + (lane >> 3), c16 = lane & 7;
           const bool tok = r < B;
-          cp_async_16(XC + c * kActImageBytes + swizzle128(r, c16),
-                      a.plan_codes + static_cast<size_t>(tok ? r : 0) * g.H + c * kChunkK + c16 * 16,
-                      tok ? 16u : 0u);
+          // A packed image's rows past the tokens are the next images' rows.
+          if (!kPacked || tok)
+            cp_async_16(XC + C::at(c, r, c16),
+                        a.plan_codes + static_cast<size_t>(tok ? r : 0) * g.H + c * kChunkK + c16 * 16,
+                        tok ? 16u : 0u);
         }
-        if (lane < kSmallMaxTokens) {
+        if (lane < C::kXScale / 16) {
           const bool st = lane < B;
-          cp_async_4(XS + c * kXAtomStride + lane * 16,
+          cp_async_4(XS + c * C::kXScale + lane * 16,
                      a.plan_scales + static_cast<size_t>(st ? lane : 0) * (g.H / kBlock) + c * (kChunkK / kBlock),
                      st ? 4u : 0u);
         }
@@ -662,8 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           // named barriers, and the build's only waits are bounded polls.
           const int valid = su->valid[u];
           const int seg0 = u * g.P1 * spi, nseg = g.P1 * spi;
-          uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
-          uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
+          const int h0 = ordinal * g.KC2;  // this unit's first hidden image
           if (et == 0) MOE_STAMP(7);
           // The unit's segment sums land in the x images' region (free once
           // this CTA's FC1 MMAs are done and the x copies have landed), a few
@@ -674,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           float* land = reinterpret_cast<float*>(XC);
           const int rows = 2 * valid;
           const int per_item = spi * rows * kTileM;  // floats of one item's segments
-          const int fit = (g.KC1 * kActImageBytes / 4) / per_item;  // items the region holds (>= 1)
+          const int fit = (g.KC1 * C::kImage / 4) / per_item;  // items the region holds (>= 1)
           const int ipb = fit < 4 ? fit : 4;                          // items per landing
           for (int p0 = 0; p0 < g.P1; p0 += ipb) {
             const int p1 = p0 + ipb < g.P1 ? p0 + ipb : g.P1;
@@ -728,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
                 const float h = silu_times(gate, up);
                 const float amax = warp_amax(h);
                 const int E = mx_exponent(amax, g.floor_rule != 0);
-                hc[p * kActImageBytes + swizzle128(t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
-                if (lane == 0) hs[p * kScaleAtomBytes + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
+                HC[C::at(h0 + p, t, m >> 4) + (m & 15)] = e4m3_code(h * pow2f(-E));
+                if (lane == 0) HSF[(h0 + p) * C::kHScale + scale_atom(t, q)] = static_cast<uint8_t>(E + 127);
               }
             }
             epilogue_sync();  // the landing is read before the next one overwrites it
@@ -743,8 +797,8 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           if (et == 0 && u != a.withhold_image) {
             tc_fence_after_sync();
             for (int c = 0; c < g.KC2; ++c)
-              tc_copy_scales(tmem + kSmallHiddenScaleBase + ordinal * 16 + c * 4,
-                             desc_scales(hs + c * kScaleAtomBytes));
+              tc_copy_scales(tmem + C::kHiddenScaleBase + ordinal * 16 + c * 4,
+                             desc_scales(HSF + (h0 + c) * C::kHScale));
             tc_commit(&hfull[ordinal]);
           }
           // This CTA has read every segment of the unit: count it per slot.
@@ -857,13 +911,23 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
         const int u = j / g.NQ;
         j = (u + 1) * g.NQ;
         if (j0 > u * g.NQ) continue;
-        const uint8_t* hc = HC + ordinal * g.KC2 * kActImageBytes;
-        const uint8_t* hs = HSF + ordinal * g.KC2 * kScaleAtomBytes;
+        // In the read-back layout: a full 8-row image per K chunk, then a
+        // 512-byte scale atom per chunk (the packed build stores rows 0-1).
+        const int h0 = ordinal * g.KC2, rows = kPacked ? 2 : kUnitRows;
+        const int per_atom = kPacked ? rows : kScaleAtomBytes / 16;
         uint8_t* img = a.hidden + static_cast<size_t>(u) * g.hidden_bytes;
-        const int n_codes = g.KC2 * kActImageBytes / 16, n_all = g.KC2 * kHiddenChunkBytes / 16;
-        for (int i = et; i < n_all; i += 128)
-          reinterpret_cast<uint4*>(img)[i] = i < n_codes ? reinterpret_cast<const uint4*>(hc)[i]
-                                                         : reinterpret_cast<const uint4*>(hs)[i - n_codes];
+        const int n_codes = g.KC2 * rows * 8, n_all = n_codes + g.KC2 * per_atom;
+        for (int i = et; i < n_all; i += 128) {
+          if (i < n_codes) {
+            const int p = i / (rows * 8), r = (i >> 3) % rows, c16 = i & 7;
+            *reinterpret_cast<uint4*>(img + p * kActImageBytes + swizzle128(r, c16)) =
+                *reinterpret_cast<const uint4*>(HC + C::at(h0 + p, r, c16));
+          } else {
+            const int p = (i - n_codes) / per_atom, v = (i - n_codes) % per_atom;
+            *reinterpret_cast<uint4*>(img + g.KC2 * kActImageBytes + p * kScaleAtomBytes + v * 16) =
+                *reinterpret_cast<const uint4*>(HSF + (h0 + p) * C::kHScale + v * 16);
+          }
+        }
       }
     }
   }
@@ -881,15 +945,19 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
 
 }  // namespace
 
-// The small-batch kernel serves a call when it has at most eight tokens, the
-// layer has at most MOE_MAX_EXPERTS experts (the kept-expert bitmap), its
-// shared-memory layout fits, and no CTA's FC2 jobs span more units than it
-// has hidden images for.
-bool small_fits(const Geometry& g, int batch, int grid) {
-  if (batch > kSmallMaxTokens || grid > kMaxGrid || SmallLayout(g.KC1, g.KC2).bytes > kSmemLimit) return false;
-  // The hidden build lands one item's segments (two rows per token) in the x images' region.
+namespace {
+
+// Whether build C of the kernel serves calls of `batch` tokens on this layer:
+// its shared-memory layout fits half an SM, the hidden build can land one
+// item's segments (two rows per token) in the x images' region, the segment
+// slots fit the descriptors' field, and no CTA's FC2 jobs span more units
+// than it has hidden images for.
+template <class C>
+bool fits(const Geometry& g, int batch, int grid) {
+  if (batch > C::kMaxUnits / kTopK || grid > kMaxGrid || SmallLayout<C>(g.KC1, g.KC2).bytes > kSmemLimit)
+    return false;
   const int spi = small_spi(g.KC1);
-  if (spi * 2 * batch * kTileM * 4 > g.KC1 * kActImageBytes) return false;
+  if (spi * 2 * batch * kTileM * 4 > g.KC1 * C::kImage) return false;
   if (small_seg_cap(g) > static_cast<int>(kDescSegMask)) return false;
   const int units = g.E < batch * kTopK ? g.E : batch * kTopK;
   for (int n = 1; n <= units; ++n) {
@@ -902,15 +970,12 @@ bool small_fits(const Geometry& g, int batch, int grid) {
   return true;
 }
 
-cudaError_t small_configure() {
-  return cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-}
-
-cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
+template <class C>
+cudaError_t launch(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = SmallLayout(a.g.KC1, a.g.KC2).bytes;
+  cfg.dynamicSmemBytes = SmallLayout<C>(a.g.KC1, a.g.KC2).bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   int n = 0;
@@ -921,7 +986,29 @@ cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bo
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, small_kernel, a);
+  return cudaLaunchKernelEx(&cfg, small_kernel<C>, a);
+}
+
+}  // namespace
+
+// The small-batch kernel serves a call of at most eight tokens on a layer of
+// at most MOE_MAX_EXPERTS experts (the kept-expert bitmap) when one of its
+// builds fits; calls of one or two tokens take the packed build (a 3-slot
+// ring) where it fits.
+bool small_fits(const Geometry& g, int batch, int grid) {
+  return fits<PackedCfg>(g, batch, grid) || fits<WideCfg>(g, batch, grid);
+}
+
+cudaError_t small_configure() {
+  cudaError_t e = cudaFuncSetAttribute(small_kernel<WideCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(small_kernel<PackedCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  return e;
+}
+
+cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
+  if (fits<PackedCfg>(a.g, a.B, grid)) return launch<PackedCfg>(a, grid, stream, pdl);
+  return launch<WideCfg>(a, grid, stream, pdl);
 }
 
 }  // namespace moe

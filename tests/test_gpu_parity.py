@@ -40,14 +40,16 @@ _LAYERS: dict = {}
 
 
 def layer_for(moe, weights):
+    """One prepared layer per weight set for the session. The cache keeps the weight
+    set itself too, so that its id() cannot be reused by a later weight set."""
     import torch
 
     w13 = weights[0]
     key = (w13.shape, id(weights))
     if key not in _LAYERS:
         dev = torch.device("cuda:0")
-        _LAYERS[key] = moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights))
-    return _LAYERS[key]
+        _LAYERS[key] = (moe.MoeLayer(tuple(torch.from_numpy(w).to(dev) for w in weights)), weights)
+    return _LAYERS[key][0]
 
 
 def to_device(x_bits, ids):
@@ -311,16 +313,25 @@ def test_supported_limits(moe, E, H, I, B, dist):
 SMALL_PATHS = [1, 2]  # the small-batch kernel, the cluster variant
 
 
-SMALL_MAX_HIDDEN = 3328  # at I = 512 the small-batch kernel's x images of all K chunks (26) fit its half SM
-SMALL_TOO_WIDE = {(16384, 512), (SMALL_MAX_HIDDEN + 256, 512)}  # (H, I) the small-batch kernel leaves to the grid
+# The widest layer the small-batch kernel serves at I = 512: its packed build (one or two
+# tokens, 3-slot ring, x images 256 bytes apart) holds 32 K chunks of x in half an SM, its
+# wide build (up to eight tokens, full 1 KB images) 26.
+SMALL_MAX_HIDDEN = {1: 4096, 2: 4096, 8: 3328}
+
+
+def small_too_wide(shape, batch):
+    """Whether the small-batch kernel leaves a layer of this (H, I) to the grid kernel."""
+    H, I = shape
+    widest = SMALL_MAX_HIDDEN[1] if batch <= 2 else SMALL_MAX_HIDDEN[8]
+    return I == 512 and H > widest
 
 
 def set_path(moe, layer, path, batch, shape=None):
     """Select an experts kernel for calls of `batch` tokens and check that it serves them.
-    Paths 1 and 3 both run the small-batch kernel, which leaves the (H, I) shapes in
-    SMALL_TOO_WIDE (its per-chunk x images would not fit half an SM) to the grid kernel."""
+    Paths 1 and 3 both run the small-batch kernel, which leaves layers wider than
+    SMALL_MAX_HIDDEN (its x images would not fit half an SM) to the grid kernel."""
     moe.moe_debug_paths(layer.handle, path)
-    if path in (1, 3) and shape is not None and tuple(shape) in SMALL_TOO_WIDE:
+    if path in (1, 3) and shape is not None and small_too_wide(shape, batch):
         assert moe.moe_kernel_path(layer.handle, batch) == 0
         return
     assert moe.moe_kernel_path(layer.handle, batch) == (1 if path == 3 else path)
@@ -366,9 +377,10 @@ def test_small_batch_path_shapes(moe, E, H, I, B, path):
 
 @pytest.mark.parametrize("B", [1, 2, 8])
 def test_small_batch_widest_hidden(moe, B):
-    """The widest layer the small-batch kernel serves at the widest I (26 K chunks of x
-    in shared memory, two CTAs per SM), against the oracle; one chunk more falls back."""
-    E, H, I = 16, SMALL_MAX_HIDDEN, 512
+    """The widest layer the small-batch kernel serves at the widest I (32 K chunks of x
+    in the packed build at one or two tokens, 26 in the wide build; two CTAs per SM),
+    against the oracle; two chunks more fall back."""
+    E, H, I = 16, SMALL_MAX_HIDDEN[B], 512
     weights = workload.make_weights(E, H, I, seed13=36, seed2=37)
     import torch
 
