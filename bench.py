@@ -424,7 +424,8 @@ class OurArm:
         path = self.moe.moe_kernel_path(handle, B)
         if path == self.moe.PATH_SMALL:
             return ("small_kernel (the whole call in one launch, two CTAs per SM, one of each of "
-                    "two consecutive calls: MXFP8 quantize and unit table in the kernel; FC1 segments "
+                    "two consecutive calls; one or two tokens: packed x and hidden images and a "
+                    "3-slot weight ring: MXFP8 quantize and unit table in the kernel; FC1 segments "
                     "claimed from a counter, their sums gathered by every FC2 CTA; tcgen05 "
                     "block-scaled MMA)")
         if path == self.moe.PATH_CLUSTER:
