@@ -576,6 +576,33 @@ def test_run_host_in_place_and_copied(moe):
     moe.moe_run_host(layer.handle, xh, torch.from_numpy(ids).pin_memory(), outh, 1)
 
 
+@pytest.mark.parametrize("batch", [1, 2])
+def test_run_host_on_the_packed_small_build(moe, batch):
+    """One or two tokens on a layer where the small kernel's packed build (x and hidden
+    images 256 bytes apart) fits: moe_run_host copies the prep grid's plan into those
+    images (pinned buffers in place, pageable ones copied) and equals moe_run, which
+    quantizes x in the kernel, bit for bit; moe_run matches the oracle."""
+    import torch
+
+    weights = workload.make_weights(32, 1024, 128, seed13=60, seed2=61)
+    layer = layer_for(moe, weights)
+    x = workload.make_x(batch, 1024, seed=62 + batch)
+    ids = workload.make_ids(batch, 32, seed=63 + batch)
+    assert moe.moe_kernel_path(layer.handle, batch) == moe.PATH_SMALL
+    want, status = run_layer(moe, layer, x, ids)
+    assert status == moe.MOE_OK
+    xq, xs = oracle.quantize_x(x)
+    check_rows(want, oracle.pairs_forward(weights, xq, xs, ids)["out"], f"packed build B={batch}")
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    idsh = torch.from_numpy(ids).pin_memory()
+    outh = torch.zeros((batch, 16, 1024), dtype=torch.int16).pin_memory()
+    moe.moe_run_host(layer.handle, xh, idsh, outh, batch)
+    np.testing.assert_array_equal(outh.numpy().view(np.uint16).reshape(-1, 1024), want)
+    out = np.zeros((batch, 16, 1024), np.uint16)
+    moe.moe_run_host(layer.handle, x, ids, out, batch)
+    np.testing.assert_array_equal(out.reshape(-1, 1024), want)
+
+
 def test_run_host_replay_graph_follows_buffers_batch_and_settings(moe):
     """The in-place moe_run_host replays a captured graph. The same pinned
     buffers with new contents are read afresh, and a smaller batch, a
