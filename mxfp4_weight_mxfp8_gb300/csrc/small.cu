@@ -128,18 +128,30 @@ struct SmallUnits {
 // Shared-memory carve-up of the small kernel (image regions on 1024-byte
 // boundaries). An operand read past a region's last image or scale atom
 // (the rows and scale rows no token uses) reads the regions after it; the
-// end guard keeps every such read inside the allocation.
+// end guard keeps every such read inside the allocation. The hand-off lands
+// segment sums in the x images and x scales (free once this CTA's FC1 is
+// done), plus a pad where half an SM has room for one: enough for all of a
+// one-token unit's items at once (kc2 items of small_spi(kc1) segments, a
+// gate row and an up row each).
 template <class C>
 struct SmallLayout {
-  int w, asf, hcodes, xc, xs, hsf, table, bars, meta, desc, misc, agree, bytes;
+  int w, asf, hcodes, xc, xs, hsf, table, bars, meta, desc, misc, agree, bytes, land;
   __host__ __device__ static int up(int o, int a) { return (o + a - 1) / a * a; }
-  __host__ __device__ SmallLayout(int kc1, int kc2) {
+  __host__ __device__ SmallLayout(int kc1, int kc2) : SmallLayout(kc1, kc2, 0) {
+    const int want = kc2 * small_spi(kc1) * 2 * kTileM * 4 - land;
+    if (want > 0) {
+      const SmallLayout padded(kc1, kc2, up(want, 16));
+      if (padded.bytes <= kSmemLimit) *this = padded;
+    }
+  }
+  __host__ __device__ SmallLayout(int kc1, int kc2, int pad) {
     int o = 0;
     w = o;                    o += C::kSlots * kStageSmemWeights;
     asf = o;                  o += C::kSlots * 2 * kScaleAtomBytes;
     hcodes = o = up(o, 1024); o += kSmallHidden * kc2 * C::kImage;
     xc = o = up(o, 1024);     o += kc1 * C::kImage;
-    xs = o = up(o, 16);       o += kc1 * C::kXScale;
+    xs = o = up(o, 16);       o += kc1 * C::kXScale + pad;
+    land = o - xc;
     hsf = o = up(o, 16);      o += kSmallHidden * kc2 * C::kHScale;
     table = o = up(o, 16);    o += static_cast<int>(sizeof(SmallUnits<C::kMaxUnits>));
     // full, empty per slot; accfull, accempty per set; hfull per unit;
@@ -728,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 2) small_kernel(const __grid_constan
           float* land = reinterpret_cast<float*>(XC);
           const int rows = 2 * valid;
           const int per_item = spi * rows * kTileM;  // floats of one item's segments
-          const int fit = (g.KC1 * C::kImage / 4) / per_item;  // items the region holds (>= 1)
+          const int fit = (L.land / 4) / per_item;  // items the region holds (>= 1)
           const int ipb = fit < 4 ? fit : 4;                          // items per landing
           for (int p0 = 0; p0 < g.P1; p0 += ipb) {
             const int p1 = p0 + ipb < g.P1 ? p0 + ipb : g.P1;
@@ -957,7 +969,7 @@ bool fits(const Geometry& g, int batch, int grid) {
   if (batch > C::kMaxUnits / kTopK || grid > kMaxGrid || SmallLayout<C>(g.KC1, g.KC2).bytes > kSmemLimit)
     return false;
   const int spi = small_spi(g.KC1);
-  if (spi * 2 * batch * kTileM * 4 > g.KC1 * C::kImage) return false;
+  if (spi * 2 * batch * kTileM * 4 > SmallLayout<C>(g.KC1, g.KC2).land) return false;
   if (small_seg_cap(g) > static_cast<int>(kDescSegMask)) return false;
   const int units = g.E < batch * kTopK ? g.E : batch * kTopK;
   for (int n = 1; n <= units; ++n) {
