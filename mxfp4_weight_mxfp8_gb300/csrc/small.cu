@@ -58,7 +58,7 @@ namespace {
 constexpr int kSmallMaxTokens = kSmallMaxBatch;  // tokens of a call (one unit per expert: <= 8 rows)
 constexpr int kSmallHidden = 2;            // FC2 units one CTA may serve
 constexpr int kXWarps = 5;                 // warps that quantize x: the activation warp + the epilogue
-constexpr int kXRaw = 512;                 // x of chunk c lands at byte 512 of its image (rows 4-7, unused)
+constexpr int kXRaw = 512;                 // wide build: x of chunk c lands at byte 512 of its image (rows 4-7)
 // Two CTAs per SM, one of each of two consecutive calls, so that one streams
 // while the other hands off and runs its FC2 jobs: each takes at most half of
 // the SM's 228 KB of shared memory (less 1 KB reserved per CTA) and half of
