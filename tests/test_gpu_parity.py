@@ -676,9 +676,13 @@ def test_out_of_range_ids_are_reported_and_skipped(moe):
     check_rows(got[keep], ref["out"], "tiny with bad ids")
 
 
-@pytest.mark.parametrize("path", [1, 2, 0], ids=["small", "cluster", "grid"])
-def test_bounded_wait_reports_timeout_and_context_survives(moe, path):
-    weights, x, ids = cached_inputs("tiny")
+@pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("tiny", 0), ("tp8_b1", 1)],
+                         ids=["small", "cluster", "grid", "tp8_b1-small-packed"])
+def test_bounded_wait_reports_timeout_and_context_survives(moe, name, path):
+    """Unit 0's FC1 results are never published: its consumers' bounded waits run out,
+    the call reports the timeout, and the next call on the handle is exact (tiny at two
+    tokens runs the small kernel's wide build, TP8 at one token its packed build)."""
+    weights, x, ids = cached_inputs(name)
     layer = layer_for(moe, weights)
     try:
         set_path(moe, layer, path, x.shape[0])
@@ -695,7 +699,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe, path):
         moe.moe_set_timeout(layer.handle, 0)
         moe.moe_debug_paths(layer.handle, 1)
     xq, xs = oracle.quantize_x(x)
-    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], "tiny after timeout")
+    check_rows(got, oracle.pairs_forward(weights, xq, xs, ids)["out"], f"{name} after timeout")
 
 
 @pytest.mark.parametrize("name,path", [("tiny", 0), ("tp16_b8", 0), ("tiny", 1), ("tp8_b1", 1)],
