@@ -355,6 +355,23 @@ const char* moe_last_error_detail(void);
  */
 int moe_device_supported(int cc_major, int cc_minor, size_t smem_per_block_optin);
 
+/*
+ * moe_small_batch_build - which build of the small-batch kernel a call of
+ * `batch` tokens (1..8) would run on a layer of this shape with `grid` CTAs
+ * (the device's SM count, at most 256): 1 the packed build (one or two
+ * tokens; the tokens' MXFP8 images of successive K chunks start 256 bytes
+ * apart, which leaves room for a 3-slot weight ring in half an SM), 2 the
+ * wide build (up to eight tokens, full 8-row images, 2-slot ring), 0 neither
+ * fits the layer (its shared-memory layout, the landing of an item's segment
+ * sums, or the FC2 split), so the grid kernel serves the call. Which calls
+ * take the small-batch kernel at all is moe_debug_paths' setting. Pure host
+ * arithmetic, no CUDA call. -MOE_ERR_ARG for sizes moe_prepare would refuse
+ * or a batch or grid out of range. Source: [experts] ExpertsKernel (the
+ * small-batch decode's one-launch path; the pages' kernel takes up to eight
+ * tokens' rows in one MMA).
+ */
+int moe_small_batch_build(int experts, int hidden, int inter, int batch, int grid);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = [
     "moe_destroy", "moe_error_string",
     "MOE_OK", "MOE_ERR_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_IDS",
     "MOE_ERR_STATE", "TOPK", "UNIT_ROWS", "MOE_NOALLOC_SCRATCH_BYTES", "moe_last_error_detail",
-    "MAX_BATCH", "moe_device_supported", "moe_debug_kernel_span", "moe_read_kernel_span",
+    "MAX_BATCH", "moe_device_supported", "moe_small_batch_build", "SMALL_NONE", "SMALL_PACKED", "SMALL_WIDE", "moe_debug_kernel_span", "moe_read_kernel_span",
     "moe_kernel_path", "PATH_GRID", "PATH_SMALL", "PATH_CLUSTER", "PATH_SMALL_WIDE",
 ]
 
@@ -74,6 +74,7 @@ def _load():
         "moe_error_string": ([i32], ctypes.c_char_p),
         "moe_last_error_detail": ([], ctypes.c_char_p),
         "moe_device_supported": ([i32, i32, ctypes.c_size_t], i32),
+        "moe_small_batch_build": ([i32, i32, i32, i32, i32], i32),
         "moe_debug_kernel_span": ([vp, i32], i32),
         "moe_read_kernel_span": ([vp, ctypes.POINTER(u64)], i32),
     }
@@ -252,6 +253,17 @@ def moe_info(handle) -> MoeInfo:
 
 def moe_destroy(handle):
     _lib.moe_destroy(handle)
+
+
+SMALL_NONE, SMALL_PACKED, SMALL_WIDE = 0, 1, 2
+
+
+def moe_small_batch_build(experts: int, hidden: int, inter: int, batch: int, grid: int = 152) -> int:
+    """The small-batch kernel's build for such a call (SMALL_*); no GPU needed."""
+    n = _lib.moe_small_batch_build(experts, hidden, inter, batch, grid)
+    if n < 0:
+        raise MoeError(-n, "moe_small_batch_build")
+    return n
 
 
 def moe_device_supported(cc_major: int, cc_minor: int, smem_per_block_optin: int) -> int:

@@ -96,6 +96,11 @@ cudaError_t launch_experts(const ExpertsArgs& a, int grid, cudaStream_t stream, 
                            int path, bool small);
 int cluster_size_for(const Geometry& g, int batch);  // 0: the grid kernel serves this call
 bool small_fits(const Geometry& g, int batch, int grid);
+// The small-batch kernel's build for a call: kSmallPacked (one or two tokens,
+// x and hidden images 256 bytes apart, 3-slot ring), kSmallWide (up to 8
+// tokens, 2-slot ring) or 0 when neither fits the layer.
+constexpr int kSmallPacked = 1, kSmallWide = 2;
+int small_build(const Geometry& g, int batch, int grid);
 cudaError_t small_configure();
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl);
 constexpr int kSmallMaxBatch = 8;  // calls of up to 8 tokens may take the small-batch kernel

@@ -732,6 +732,14 @@ const char* moe_error_string(int status) {
 
 const char* moe_last_error_detail(void) { return g_detail; }
 
+int moe_small_batch_build(int experts, int hidden, int inter, int batch, int grid) {
+  if (experts < 1 || experts > MOE_MAX_EXPERTS) return -MOE_ERR_ARG;
+  if (hidden < 256 || hidden > MOE_MAX_HIDDEN || hidden % 256 != 0) return -MOE_ERR_ARG;
+  if (inter < 32 || inter > MOE_MAX_INTER || inter % 32 != 0) return -MOE_ERR_ARG;
+  if (batch < 1 || batch > moe::kSmallMaxBatch || grid < 1 || grid > moe::kMaxGrid) return -MOE_ERR_ARG;
+  return moe::small_build(moe::make_geometry(experts, hidden, inter), batch, grid);
+}
+
 int moe_device_supported(int cc_major, int cc_minor, size_t smem_per_block_optin) {
   if (cc_major != 10 || cc_minor != 3) return MOE_ERR_UNSUPPORTED;
   const size_t need = static_cast<size_t>(moe::experts_max_smem_bytes(moe::make_geometry(1, 256, MOE_MAX_INTER)));

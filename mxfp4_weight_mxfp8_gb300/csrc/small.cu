@@ -1007,9 +1007,13 @@ cudaError_t launch(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl
 // at most MOE_MAX_EXPERTS experts (the kept-expert bitmap) when one of its
 // builds fits; calls of one or two tokens take the packed build (a 3-slot
 // ring) where it fits.
-bool small_fits(const Geometry& g, int batch, int grid) {
-  return fits<PackedCfg>(g, batch, grid) || fits<WideCfg>(g, batch, grid);
+int small_build(const Geometry& g, int batch, int grid) {
+  if (fits<PackedCfg>(g, batch, grid)) return kSmallPacked;
+  if (fits<WideCfg>(g, batch, grid)) return kSmallWide;
+  return 0;
 }
+
+bool small_fits(const Geometry& g, int batch, int grid) { return small_build(g, batch, grid) != 0; }
 
 cudaError_t small_configure() {
   cudaError_t e = cudaFuncSetAttribute(small_kernel<WideCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
@@ -1019,7 +1023,7 @@ cudaError_t small_configure() {
 }
 
 cudaError_t launch_small(const ExpertsArgs& a, int grid, cudaStream_t stream, bool pdl) {
-  if (fits<PackedCfg>(a.g, a.B, grid)) return launch<PackedCfg>(a, grid, stream, pdl);
+  if (small_build(a.g, a.B, grid) == kSmallPacked) return launch<PackedCfg>(a, grid, stream, pdl);
   return launch<WideCfg>(a, grid, stream, pdl);
 }
 

@@ -53,6 +53,35 @@ def test_library_is_built_for_sm103a_only(lib):
     assert os.path.exists(lib.library()._name)
 
 
+def test_small_batch_build_rules_without_a_gpu(lib):
+    """Which build of the small-batch kernel a call gets, from host arithmetic alone
+    (the shared-memory layouts of half an SM, the landing of an item's segment sums and
+    the FC2 split over 152 CTAs)."""
+    b = lib.moe_small_batch_build
+    P, W, N = lib.SMALL_PACKED, lib.SMALL_WIDE, lib.SMALL_NONE
+    # The TP8 and TP16 shards: one or two tokens packed, more wide.
+    assert [b(384, 3584, 384, n) for n in (1, 2, 3, 8)] == [P, P, W, W]
+    assert [b(384, 3584, 256, n) for n in (1, 2, 8)] == [P, P, W]
+    # Widest layers at I = 512: packed up to H = 4096 (32 K chunks of 256-byte images),
+    # wide up to 3328 (26 K chunks of 1 KB images).
+    assert [b(16, 4096, 512, n) for n in (1, 2, 3)] == [P, P, N]
+    assert b(16, 4352, 512, 1) == N
+    assert [b(16, 3328, 512, n) for n in (3, 8)] == [W, W]
+    assert b(16, 3584, 512, 8) == N
+    assert b(16, 16384, 512, 1) == N
+    # H = 256: two K chunks hold one token's segment sums in the packed layout's pad,
+    # two tokens' only in the wide layout's full images.
+    assert [b(32, 256, 64, n) for n in (1, 2, 3)] == [P, W, N]
+    # Partial tiles (I = 96): the packed build at one token, the wide one up to four.
+    assert [b(16, 512, 96, n) for n in (1, 2, 4, 5)] == [P, W, W, N]
+    for bad in [(0, 3584, 384, 1), (384, 3600, 384, 1), (384, 3584, 40, 1), (384, 3584, 384, 0),
+                (384, 3584, 384, 9)]:
+        with pytest.raises(lib.MoeError):
+            b(*bad)
+    with pytest.raises(lib.MoeError):
+        b(384, 3584, 384, 1, grid=300)
+
+
 def test_device_support_check_without_a_gpu(lib):
     """moe_prepare's device check on faked properties: sm_103 with the
     kernel's shared memory is accepted; sm_100 (no sm_103a code), other
