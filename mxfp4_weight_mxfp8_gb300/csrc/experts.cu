@@ -120,9 +120,6 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
   if (tid == 0) {
     span_enter(a.span);
     MOE_STAMP(0);
-    // The next call's prep grid may start as this grid's CTAs leave: it
-    // writes nothing before it has waited for this grid to end.
-    grid_launch_dependents();
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + 32);       // producer (with bytes) + 32 gather lanes or a stand-in
       mbar_init(&empty[s], kMmaWarps);   // one commit per issuer
@@ -155,7 +152,37 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
   // The plan, unit table and cleared counters of the preceding prep grid.
   // Every unit's expert goes to shared memory in the same round trip as the
   // unit count (entries past the count are never used).
-  grid_dependency_wait();
+  if (a.early) {
+    // The prep grid raised `ready` to this call's number once its writes
+    // were out, without waiting for the previous experts grid (another
+    // handle's, still running on the other SMs).
+    if (tid == 0) {
+      const uint64_t t_start = global_timer_ns();
+      for (uint32_t i = 0; load_acquire_gpu(a.ready) != a.seq; ++i) {
+        __nanosleep(64);
+        if ((i & 15u) == 15u && global_timer_ns() - t_start > a.timeout_ns) {
+          report(a.status, MOE_ERR_DEVICE_TIMEOUT);
+          misc[1] = 1u;
+          break;
+        }
+      }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (misc[1] != 0u) {
+      // No tables: end without reading them, after the previous grid.
+      if (warp == kMmaWarp0) tmem_dealloc(misc[0], kTmemColumns);
+      grid_dependency_wait();
+      if (tid == 0) span_leave(a.span);
+      return;
+    }
+  } else {
+    grid_dependency_wait();
+    // The next call's prep grid may start now: the grid before this one has
+    // ended, and it writes nothing before it has waited for this grid to end.
+    if (tid == 0) grid_launch_dependents();
+  }
   uint32_t* xc = reinterpret_cast<uint32_t*>(sm + L.units);
   {
     const int cap = min(2 * a.B + min(g.E, kTopK * a.B), R == 8 ? kUnitCache8 : kUnitCache16);
@@ -583,6 +610,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
       }
     };
     int k = 0, out_unit = -1, out_pair = -1, out_pair2 = -1, out_valid = 0;
+    bool prev_ended = false;
     for (;;) {
       const int set = k % NACC;
       // The metadata and the abort flag are read together, after the wait.
@@ -725,6 +753,14 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
         if (et == 0) MOE_STAMP(8);
       } else {
         // ---- FC2 job: rows 256q' + m (v0) and 256q' + 128 + m (v1) -> BF16.
+        if (a.early && !prev_ended) {
+          // The previous call may write the same output rows: wait for the
+          // prep grid's end, which follows the previous experts grid's, and
+          // only then let the next call start.
+          grid_dependency_wait();
+          if (et == 0) grid_launch_dependents();
+          prev_ended = true;
+        }
         const int j = md.y, u = j / g.NQ, qq = j - u * g.NQ;
         if (u != out_unit) {
           out_pair = unit_row(u, et >> 4);

@@ -25,6 +25,18 @@ struct PrepArgs {
   int32_t* status;
   int roles;
   int quant_blocks;
+  // Early start (the previous launch on the stream was another handle's
+  // call): the blocks write without waiting for the previous grid, the last
+  // one raises *ready to seq (release), and every block then waits for the
+  // previous grid before it ends.
+  int early;
+  uint32_t seq;
+  uint32_t* ready;            // [1]: the number of the last call whose tables are out
+  uint32_t* arrive;           // [1]: blocks done writing (zero at rest)
+  // Its own experts kernel follows at once (moe_run): let it launch at this
+  // grid's start. Otherwise (moe_quantize, moe_group) the next launch waits
+  // for this grid's end.
+  int chained;
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
@@ -63,6 +75,12 @@ struct ExpertsArgs {
   uint32_t* small_counters;   // [2 parities][4]: [0] segments claimed (zero at rest)
   uint8_t* pair_kept;         // [B * 16] or null: 1 where the pair got a unit row
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
+  // Grid kernel, early start: read the tables once *ready == seq instead of
+  // waiting for the prep grid to end; wait for it only before the first
+  // output row (its end implies the previous experts grid's).
+  int early;
+  uint32_t seq;
+  const uint32_t* ready;
   int seg_cap;                // segment slots per parity
   int piece_words;            // words per segment slot (2 x the batch bound x 128)
   int parity;                 // which half of the slots and counters this call uses

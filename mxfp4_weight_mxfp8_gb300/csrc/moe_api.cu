@@ -5,6 +5,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "kernels.h"
@@ -47,6 +48,9 @@ struct moe_ctx {
   uint32_t* piece_readers = nullptr;   // small-batch kernel: read counts per slot (zero at rest)
   uint32_t* small_counters = nullptr;  // small-batch kernel: segment claims, CTAs done (zero at rest)
   int small_parity = 0;                // the half of the slots and counters the next call takes
+  uint32_t* ready = nullptr;   // [0] the number of the last early call whose prep grid wrote its tables
+  uint32_t* arrive = nullptr;  // [0] that prep grid's blocks done writing (zero at rest)
+  uint32_t seq = 0;            // early calls made
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
   int plan_batch = 0, group_batch = 0, grouped = 0, ran = 0;
@@ -217,9 +221,10 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(h->unit_cap) * 4,                     // pairs of units
       moe::small_piece_bytes(g),                                // small-batch segment slots
       moe::kSmallCounterBytes,                                  // small-batch claim counters
+      8,                                                        // early start: ready, arrive
   };
-  size_t offsets[17], total = 0;
-  for (int i = 0; i < 17; ++i) {
+  size_t offsets[18], total = 0;
+  for (int i = 0; i < 18; ++i) {
     offsets[i] = total;
     total += round256(sizes[i]);
   }
@@ -244,6 +249,8 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->wide_units = reinterpret_cast<uint32_t*>(w + offsets[14]);
   h->piece_sums = reinterpret_cast<uint32_t*>(w + offsets[15]);
   h->small_counters = reinterpret_cast<uint32_t*>(w + offsets[16]);
+  h->ready = reinterpret_cast<uint32_t*>(w + offsets[17]);
+  h->arrive = h->ready + 1;
   MOE_CUDA(cudaMemset(h->piece_sums, 0xFF, moe::small_piece_bytes(g)));  // every word the sentinel
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
@@ -277,6 +284,31 @@ moe::PrepArgs prep_args(moe_ctx* h, const void* x, const int32_t* ids, int batch
 
 int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE_OK : MOE_ERR_ARG; }
 
+// The handle whose call was the last this library launched on each stream.
+// A grid call that follows another handle's call on its stream starts early:
+// its prep grid writes this handle's tables (nothing the previous call
+// touches) without waiting for the previous grid, and its experts kernel
+// streams FC1 as soon as its CTAs are resident, waiting for the previous
+// grid only before its first output row. Every kernel of this library waits
+// for the grid before it ahead of ending, and lets the next launch start only
+// after that wait, so when an early prep grid starts, the call before the
+// previous one on the stream (possibly this handle's last) has ended.
+std::mutex g_stream_mutex;
+std::unordered_map<cudaStream_t, const moe_ctx*> g_last_handle;
+
+bool follows_other_handle(const moe_ctx* h, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_stream_mutex);
+  auto it = g_last_handle.find(s);
+  const bool other = it != g_last_handle.end() && it->second != h;
+  g_last_handle[s] = h;
+  return other;
+}
+
+void note_launch(const moe_ctx* h, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_stream_mutex);
+  g_last_handle[s] = h;
+}
+
 // A handle's buffers, tensor map and kernels belong to the device that was
 // current at moe_prepare: every call that launches, copies or synchronizes
 // refuses to run with another device current.
@@ -307,8 +339,13 @@ bool small_call(const moe_ctx* h, int batch) {
 // before on this stream (or, x given, when the call is the small-batch kernel
 // alone), else null.
 int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream,
-                   const void* x = nullptr) {
+                   const void* x = nullptr, bool early = false) {
   moe::ExpertsArgs a{};
+  if (early) {
+    a.early = 1;
+    a.seq = h->seq;
+    a.ready = h->ready;
+  }
   a.wmap = h->wmap;
   a.stages = h->stages;
   a.ids = ids;
@@ -359,11 +396,22 @@ int run_call(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* ou
   int rc;
   if (fused && small_call(h, batch)) {
     // One launch: the small-batch kernel quantizes x and groups the ids itself.
+    note_launch(h, s);
     rc = launch_experts(h, out_bf16, batch, topk_ids, s, x_bf16);
   } else {
-    MOE_CUDA(moe::launch_prep(
-        prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup), s));
-    rc = launch_experts(h, out_bf16, batch, topk_ids, s);
+    // The persistent grid kernel may start early after another handle's call.
+    const bool grid = !small_call(h, batch) && moe_kernel_path(h, batch) == moe::kPathGrid;
+    const bool early = follows_other_handle(h, s) && grid && fused;
+    moe::PrepArgs pa = prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup);
+    pa.chained = 1;
+    if (early) {
+      pa.early = 1;
+      pa.seq = ++h->seq;
+      pa.ready = h->ready;
+      pa.arrive = h->arrive;
+    }
+    MOE_CUDA(moe::launch_prep(pa, s));
+    rc = launch_experts(h, out_bf16, batch, topk_ids, s, nullptr, early);
   }
   if (rc != MOE_OK) return rc;
   h->plan_batch = batch;
@@ -434,6 +482,7 @@ int moe_prepare(moe_handle* out, const void* w13, const void* s13, const void* w
 int moe_quantize(moe_handle h, const void* x_bf16, int batch, void* stream) {
   if (h == nullptr || x_bf16 == nullptr || !aligned16(x_bf16) || check_batch(batch)) return MOE_ERR_ARG;
   MOE_CHECK_DEVICE(h);
+  note_launch(h, static_cast<cudaStream_t>(stream));
   MOE_CUDA(moe::launch_prep(prep_args(h, x_bf16, nullptr, batch, moe::kPrepQuantize),
                             static_cast<cudaStream_t>(stream)));
   h->plan_batch = batch;
@@ -444,6 +493,7 @@ int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream) {
   if (h == nullptr || topk_ids == nullptr || !aligned16(topk_ids) || check_batch(batch))
     return MOE_ERR_ARG;
   MOE_CHECK_DEVICE(h);
+  note_launch(h, static_cast<cudaStream_t>(stream));
   MOE_CUDA(moe::launch_prep(prep_args(h, nullptr, topk_ids, batch, moe::kPrepGroup),
                             static_cast<cudaStream_t>(stream)));
   h->grouped = 1;
@@ -480,6 +530,7 @@ int moe_experts(moe_handle h, void* out_bf16, int batch, void* stream) {
   if (h == nullptr || out_bf16 == nullptr || !aligned16(out_bf16) || check_batch(batch))
     return MOE_ERR_ARG;
   MOE_CHECK_DEVICE(h);
+  note_launch(h, static_cast<cudaStream_t>(stream));
   if (h->plan_batch != batch || h->group_batch != batch) return MOE_ERR_STATE;
   const int rc = launch_experts(h, out_bf16, batch, nullptr, static_cast<cudaStream_t>(stream));
   if (rc == MOE_OK) h->ran = 1;
@@ -519,6 +570,7 @@ int moe_run_host(moe_handle h, const void* x_host, const int32_t* ids_host, void
                  int batch, void* stream) {
   if (h == nullptr || !x_host || !ids_host || !out_host || check_batch(batch)) return MOE_ERR_ARG;
   MOE_CHECK_DEVICE(h);
+  note_launch(h, static_cast<cudaStream_t>(stream));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (h->host_atomics && aligned16(x_host) && aligned16(ids_host) && aligned16(out_host) &&
       is_pinned_host(x_host) && is_pinned_host(ids_host) && is_pinned_host(out_host)) {
@@ -847,7 +899,9 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.item_counters = reinterpret_cast<uint32_t*>(w + offsets[5]);
   pa.hidden_flags = reinterpret_cast<uint32_t*>(w + offsets[6]);
   pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
+  pa.chained = 1;          // this call's experts kernel follows at once
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  note_launch(h, s);
   uint32_t* piece_readers = reinterpret_cast<uint32_t*>(w + offsets[9]);
   uint32_t* piece_sums = reinterpret_cast<uint32_t*>(w + offsets[11]);
   uint32_t* small_counters = reinterpret_cast<uint32_t*>(w + offsets[12]);

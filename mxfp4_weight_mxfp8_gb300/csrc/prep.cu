@@ -84,7 +84,7 @@ __device__ void quantize_role(const PrepArgs& a, int block) {
 #pragma unroll
   for (int r = 0; r < kQuantChunks; ++r)
     q[r] = quantize_chunk(a, (block * kQuantChunks + r) * kPrepThreads + threadIdx.x);
-  ptx::grid_dependency_wait();
+  if (!a.early) ptx::grid_dependency_wait();
 #pragma unroll
   for (int r = 0; r < kQuantChunks; ++r) store_chunk(a, q[r]);
 }
@@ -157,7 +157,7 @@ __device__ void group_role(const PrepArgs& a, uint8_t* smem) {
   if (tid == kPrepThreads - 1) *grand = before + incl;
   int start = before + incl - local;
   // The previous grid on the stream may still read the tables written below.
-  ptx::grid_dependency_wait();
+  if (!a.early) ptx::grid_dependency_wait();
   if (dropped) report(a.status, MOE_ERR_DEVICE_IDS);
   if (a.pair_kept != nullptr)
 #pragma unroll
@@ -256,7 +256,7 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
     wbefore += (k.x < e && v.x > 0) + (k.y < e && v.y > 0) + (k.z < e && v.z > 0) + (k.w < e && v.w > 0);
   }
   // The previous grid on the stream may still read the tables written below.
-  ptx::grid_dependency_wait();
+  if (!a.early) ptx::grid_dependency_wait();
   if (tid < pairs && !kept) report(a.status, MOE_ERR_DEVICE_IDS);  // out of range or repeated
   if (a.pair_kept != nullptr && tid < pairs) a.pair_kept[tid] = kept ? 1 : 0;
   if (tid == 0) {
@@ -281,11 +281,12 @@ __device__ void group_small(const PrepArgs& a, uint8_t* smem) {
 // shared memory first, and waits for the previous grid to end only before
 // its first global write, so that work overlaps the previous experts
 // kernel's tail. ids and x themselves are read at once (see moe_run).
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+__global__ void __launch_bounds__(kPrepThreads, 6) prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  // Let the experts kernel start its prologue; it waits for this grid's end
-  // before reading anything written here.
-  ptx::grid_launch_dependents();
+  // Let the call's experts kernel start its prologue; it waits for this
+  // grid's end (or, started early, for the tables' flag) before reading
+  // anything written here.
+  if (a.chained) ptx::grid_launch_dependents();
   // The grouping block is block 0, dispatched first: it has the longest run.
   const int group_blocks = (a.roles & kPrepGroup) ? 1 : 0;
   if (group_blocks && blockIdx.x == 0) {
@@ -295,6 +296,23 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       group_role(a, smem);
   } else if (a.roles & kPrepQuantize) {
     quantize_role(a, blockIdx.x - group_blocks);
+  }
+  if (a.early) {
+    // Every block's writes are out before the last one raises the flag. The
+    // grid still ends only after the previous grid has (its last block waits
+    // for it; the others leave at once, freeing their SMs for the experts
+    // kernel), so that the experts kernel's wait for this grid covers that
+    // one too.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(a.arrive, 1u) == gridDim.x - 1) {
+        *a.arrive = 0u;
+        __threadfence();
+        ptx::store_release_gpu(a.ready, a.seq);
+      }
+    }
+    if (blockIdx.x == gridDim.x - 1) ptx::grid_dependency_wait();
   }
 }
 

@@ -603,6 +603,52 @@ def test_run_host_on_the_packed_small_build(moe, batch):
     np.testing.assert_array_equal(out.reshape(-1, 1024), want)
 
 
+@pytest.mark.parametrize("B", [4, 8, 40])
+def test_grid_calls_alternating_handles_start_early(moe, B):
+    """Grid-kernel calls alternating between two handles on one stream: each call after
+    the other handle's starts early (its prep grid writes the handle's tables without
+    waiting for the previous grid, its experts kernel streams FC1 while the previous call
+    runs, and waits for it only before its first output row). Every call's rows equal the
+    same call made alone, and when all calls write one output buffer it ends with the last
+    call's rows."""
+    import torch
+
+    wa = workload.make_weights(64, 1024, 256, seed13=70, seed2=71)
+    wb = workload.make_weights(64, 1024, 256, seed13=72, seed2=73)
+    la, lb = layer_for(moe, wa), layer_for(moe, wb)
+    assert moe.moe_kernel_path(la.handle, B) == moe.PATH_GRID
+    n = 6
+    layers = [la, lb] * (n // 2)
+    xs = [workload.make_x(B, 1024, seed=80 + i) for i in range(n)]
+    idss = [workload.make_ids(B, 64, seed=90 + i) for i in range(n)]
+    want = []
+    for layer, x, ids in zip(layers, xs, idss):
+        got, status = run_layer(moe, layer, x, ids)
+        assert status == moe.MOE_OK
+        want.append(got)
+    xq, xsc = oracle.quantize_x(xs[1])
+    check_rows(want[1], oracle.pairs_forward(wb, xq, xsc, idss[1])["out"], f"handle B, B={B}")
+    dev = [to_device(x, ids) for x, ids in zip(xs, idss)]
+    stream = torch.cuda.Stream()
+    for rep in range(3):
+        outs = [torch.full((B, 16, 1024), float("nan"), dtype=torch.bfloat16, device="cuda:0") for _ in range(n)]
+        shared = torch.full((B, 16, 1024), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for layer, (xd, idsd), o in zip(layers, dev, outs):
+                layer(xd, idsd, out=o, stream=stream.cuda_stream)
+            for layer, (xd, idsd) in zip(layers, dev):
+                layer(xd, idsd, out=shared, stream=stream.cuda_stream)
+        stream.synchronize()
+        for layer in (la, lb):
+            assert moe.moe_sync_status(layer.handle) == moe.MOE_OK
+        for i, o in enumerate(outs):
+            got = o.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * 16, 1024)
+            np.testing.assert_array_equal(got, want[i], err_msg=f"rep {rep} call {i}")
+        got = shared.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * 16, 1024)
+        np.testing.assert_array_equal(got, want[-1], err_msg=f"rep {rep}, shared output")
+
+
 def test_run_host_replay_graph_follows_buffers_batch_and_settings(moe):
     """The in-place moe_run_host replays a captured graph. The same pinned
     buffers with new contents are read afresh, and a smaller batch, a
