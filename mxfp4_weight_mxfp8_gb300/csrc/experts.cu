@@ -166,6 +166,10 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
           break;
         }
       }
+      if (misc[1] == 0u && atomicAdd(a.passed, 1u) == static_cast<uint32_t>(G) - 1u) {
+        *a.passed = 0u;
+        *reinterpret_cast<volatile uint32_t*>(a.ready) = 0u;
+      }
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -77,10 +77,13 @@ struct ExpertsArgs {
   uint64_t* trace;            // or null: per-CTA phase stamps (builds with MOE_TRACE only)
   // Grid kernel, early start: read the tables once *ready == seq instead of
   // waiting for the prep grid to end; wait for it only before the first
-  // output row (its end implies the previous experts grid's).
+  // output row (its end implies the previous experts grid's). The last CTA
+  // to see the flag puts it back to 0, so that a replay of the same call (a
+  // CUDA graph keeps seq) waits for its own prep grid.
   int early;
   uint32_t seq;
-  const uint32_t* ready;
+  uint32_t* ready;
+  uint32_t* passed;           // [1]: CTAs that saw the flag (zero at rest)
   int seg_cap;                // segment slots per parity
   int piece_words;            // words per segment slot (2 x the batch bound x 128)
   int parity;                 // which half of the slots and counters this call uses

@@ -50,6 +50,7 @@ struct moe_ctx {
   int small_parity = 0;                // the half of the slots and counters the next call takes
   uint32_t* ready = nullptr;   // [0] the number of the last early call whose prep grid wrote its tables
   uint32_t* arrive = nullptr;  // [0] that prep grid's blocks done writing (zero at rest)
+  uint32_t* passed = nullptr;  // [0] its experts kernel's CTAs that saw the flag (zero at rest)
   uint32_t seq = 0;            // early calls made
   int span_on = 0;
   uint64_t* trace = nullptr;  // phase stamps (MOE_TRACE builds only)
@@ -221,7 +222,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
       static_cast<size_t>(h->unit_cap) * 4,                     // pairs of units
       moe::small_piece_bytes(g),                                // small-batch segment slots
       moe::kSmallCounterBytes,                                  // small-batch claim counters
-      8,                                                        // early start: ready, arrive
+      16,                                                       // early start: ready, arrive, passed
   };
   size_t offsets[18], total = 0;
   for (int i = 0; i < 18; ++i) {
@@ -251,6 +252,7 @@ int build_handle(moe_ctx* h, const void* w13, const void* s13, const void* w2, c
   h->small_counters = reinterpret_cast<uint32_t*>(w + offsets[16]);
   h->ready = reinterpret_cast<uint32_t*>(w + offsets[17]);
   h->arrive = h->ready + 1;
+  h->passed = h->ready + 2;
   MOE_CUDA(cudaMemset(h->piece_sums, 0xFF, moe::small_piece_bytes(g)));  // every word the sentinel
   MOE_CUDA(cudaMallocHost(&h->status_host, 4));
   h->status_dev = h->status;
@@ -345,6 +347,7 @@ int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStr
     a.early = 1;
     a.seq = h->seq;
     a.ready = h->ready;
+    a.passed = h->passed;
   }
   a.wmap = h->wmap;
   a.stages = h->stages;
@@ -552,6 +555,8 @@ int moe_sync_status(moe_handle h, void* stream) {
     MOE_CUDA(cudaMemsetAsync(h->piece_readers, 0, moe::small_reader_bytes(h->g), s));
     MOE_CUDA(cudaMemsetAsync(h->piece_sums, 0xFF, moe::small_piece_bytes(h->g), s));
     MOE_CUDA(cudaMemsetAsync(h->small_counters, 0, moe::kSmallCounterBytes, s));
+    // An early-start call may have stopped before its flag went back to rest.
+    MOE_CUDA(cudaMemsetAsync(h->ready, 0, 3 * sizeof(uint32_t), s));
     MOE_CUDA(cudaStreamSynchronize(s));
   }
   return status;

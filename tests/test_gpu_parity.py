@@ -649,6 +649,58 @@ def test_grid_calls_alternating_handles_start_early(moe, B):
         np.testing.assert_array_equal(got, want[-1], err_msg=f"rep {rep}, shared output")
 
 
+def test_early_grid_calls_replayed_in_a_graph_with_new_inputs(moe):
+    """Grid-kernel calls alternating between two handles, captured once in a CUDA graph
+    and replayed with new routing ids and activations in the same buffers: the early-start
+    flag of each call is back at rest after the call, so a replay's experts kernel reads
+    the tables its own prep grid wrote, never the previous replay's."""
+    import torch
+
+    B = 8
+    wa = workload.make_weights(64, 1024, 256, seed13=74, seed2=75)
+    wb = workload.make_weights(64, 1024, 256, seed13=76, seed2=77)
+    layers = [layer_for(moe, wa), layer_for(moe, wb)] * 2
+    n = len(layers)
+    xbufs = [torch.empty((B, 1024), dtype=torch.bfloat16, device="cuda:0") for _ in range(n)]
+    idbufs = [torch.empty((B, 16), dtype=torch.int32, device="cuda:0") for _ in range(n)]
+    outs = [torch.empty((B, 16, 1024), dtype=torch.bfloat16, device="cuda:0") for _ in range(n)]
+
+    def fill(rep):
+        inputs = []
+        for i in range(n):
+            x = workload.make_x(B, 1024, seed=100 + 10 * rep + i)
+            ids = workload.make_ids(B, 64, seed=200 + 10 * rep + i)
+            xd, idsd = to_device(x, ids)
+            xbufs[i].copy_(xd)
+            idbufs[i].copy_(idsd)
+            inputs.append((x, ids))
+        return inputs
+
+    stream = torch.cuda.Stream()
+    fill(0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # warm up on the capture stream
+        for layer, xb, ib, o in zip(layers, xbufs, idbufs, outs):
+            layer(xb, ib, out=o, stream=stream.cuda_stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for layer, xb, ib, o in zip(layers, xbufs, idbufs, outs):
+            layer(xb, ib, out=o, stream=stream.cuda_stream)
+    for rep in range(1, 4):
+        inputs = fill(rep)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for layer in layers[:2]:
+            assert moe.moe_sync_status(layer.handle) == moe.MOE_OK, f"replay {rep}"
+        for i, (layer, (x, ids)) in enumerate(zip(layers, inputs)):
+            want, status = run_layer(moe, layer, x, ids)
+            assert status == moe.MOE_OK
+            got = outs[i].view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * 16, 1024)
+            np.testing.assert_array_equal(got, want, err_msg=f"replay {rep}, call {i}")
+
+
 def test_run_host_replay_graph_follows_buffers_batch_and_settings(moe):
     """The in-place moe_run_host replays a captured graph. The same pinned
     buffers with new contents are read afresh, and a smaller batch, a
