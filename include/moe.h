@@ -144,8 +144,15 @@ int moe_group(moe_handle h, const int32_t* topk_ids, int batch, void* stream);
  * must not be the out_bf16 of the moe_run call just before on the stream
  * (every other producer is safe: a kernel of the caller, or
  * moe_run_combined, whose last launch lets the next start only when it has
- * ended). Errors: MOE_ERR_ARG (nulls, misalignment, batch range),
- * MOE_ERR_CUDA.
+ * ended). A call on the persistent grid kernel that follows another
+ * handle's call on the same stream starts early: its prep grid writes this
+ * handle's tables without waiting for the previous launch, and its experts
+ * kernel streams weights while the previous call still runs, holding its
+ * output rows until that call has ended. Every launch of this library lets
+ * the next one start only after its own wait for the launch before it; a
+ * caller's kernel launched between two calls with programmatic stream
+ * serialization must likewise wait (griddepcontrol.wait) before it ends.
+ * Errors: MOE_ERR_ARG (nulls, misalignment, batch range), MOE_ERR_CUDA.
  */
 int moe_run(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* out_bf16, int batch,
             void* stream);
