@@ -94,10 +94,14 @@ struct Split {
                                    static_cast<uint32_t>(J));
     return c < G - 1 ? c : G - 1;
   }
+  // FC1 ranges are skewed toward the low CTAs: CTA c's range starts at
+  // T1 * x * (1 + (1 - x) / 4), x = c / G. CTAs start in block order as the
+  // previous call's CTAs leave (early start), so the ones that start first
+  // get up to a quarter more stages and all finish FC1 closer together.
   __host__ __device__ int fc1_begin(int c) const {
     if (c >= G) return T1;
-    const uint32_t cu = static_cast<uint32_t>(c);
-    return static_cast<int>(cu * static_cast<uint32_t>(T1) / static_cast<uint32_t>(G));
+    const uint64_t cu = static_cast<uint64_t>(c), g = static_cast<uint64_t>(G);
+    return static_cast<int>(static_cast<uint64_t>(T1) * cu * (5ull * g - cu) / (4ull * g * g));
   }
 };
 
