@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) experts_kernel(const __grid_c
   // Half A = units [0, units_a). Small calls keep one half: their chain of
   // reductions is latency-bound and more pieces per item only lengthen it.
   const int units_a = units > kHalvesFrom ? (units + 1) / 2 : units;
-  const Split half[2] = {Split(units_a, g, G), Split(units - units_a, g, G)};
+  const Split half[2] = {Split(units_a, g, G, a.skew), Split(units - units_a, g, G, a.skew)};
   const int stage_base[2] = {0, units_a * g.P1 * g.KC1};
   const int job_base[2] = {0, units_a * g.NQ};
   const int items_a = units_a * g.P1;

@@ -84,6 +84,7 @@ struct ExpertsArgs {
   uint32_t seq;
   uint32_t* ready;
   uint32_t* passed;           // [1]: CTAs that saw the flag (zero at rest)
+  int skew;                   // FC1 ranges skewed toward the low CTAs (see Split)
   int seg_cap;                // segment slots per parity
   int piece_words;            // words per segment slot (2 x the batch bound x 128)
   int parity;                 // which half of the slots and counters this call uses

@@ -295,20 +295,30 @@ int check_batch(int batch) { return (batch >= 1 && batch <= MOE_MAX_BATCH) ? MOE
 // for the grid before it ahead of ending, and lets the next launch start only
 // after that wait, so when an early prep grid starts, the call before the
 // previous one on the stream (possibly this handle's last) has ended.
+// `overlaps`: the call's last launch lets the next one start while it still
+// runs (moe_run, moe_run_noalloc), so the next call's CTAs start one by one
+// as its CTAs leave, and an early grid call skews its FC1 split to match.
+struct LastLaunch {
+  const moe_ctx* h;
+  bool overlaps;
+};
 std::mutex g_stream_mutex;
-std::unordered_map<cudaStream_t, const moe_ctx*> g_last_handle;
+std::unordered_map<cudaStream_t, LastLaunch> g_last_launch;
 
-bool follows_other_handle(const moe_ctx* h, cudaStream_t s) {
+// Whether this call follows another handle's call on `s` (early start), and
+// whether that call's last launch overlaps this one; records this call.
+bool follows_other_handle(const moe_ctx* h, cudaStream_t s, bool* prev_overlaps) {
   std::lock_guard<std::mutex> lock(g_stream_mutex);
-  auto it = g_last_handle.find(s);
-  const bool other = it != g_last_handle.end() && it->second != h;
-  g_last_handle[s] = h;
+  auto it = g_last_launch.find(s);
+  const bool other = it != g_last_launch.end() && it->second.h != h;
+  *prev_overlaps = other && it->second.overlaps;
+  g_last_launch[s] = LastLaunch{h, true};
   return other;
 }
 
-void note_launch(const moe_ctx* h, cudaStream_t s) {
+void note_launch(const moe_ctx* h, cudaStream_t s, bool overlaps = false) {
   std::lock_guard<std::mutex> lock(g_stream_mutex);
-  g_last_handle[s] = h;
+  g_last_launch[s] = LastLaunch{h, overlaps};
 }
 
 // A handle's buffers, tensor map and kernels belong to the device that was
@@ -341,8 +351,9 @@ bool small_call(const moe_ctx* h, int batch) {
 // before on this stream (or, x given, when the call is the small-batch kernel
 // alone), else null.
 int launch_experts(moe_ctx* h, void* out, int batch, const int32_t* ids, cudaStream_t stream,
-                   const void* x = nullptr, bool early = false) {
+                   const void* x = nullptr, bool early = false, bool skew = false) {
   moe::ExpertsArgs a{};
+  a.skew = skew ? 1 : 0;
   if (early) {
     a.early = 1;
     a.seq = h->seq;
@@ -399,12 +410,13 @@ int run_call(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* ou
   int rc;
   if (fused && small_call(h, batch)) {
     // One launch: the small-batch kernel quantizes x and groups the ids itself.
-    note_launch(h, s);
+    note_launch(h, s, true);
     rc = launch_experts(h, out_bf16, batch, topk_ids, s, x_bf16);
   } else {
     // The persistent grid kernel may start early after another handle's call.
     const bool grid = !small_call(h, batch) && moe_kernel_path(h, batch) == moe::kPathGrid;
-    const bool early = follows_other_handle(h, s) && grid && fused;
+    bool prev_overlaps = false;
+    const bool early = follows_other_handle(h, s, &prev_overlaps) && grid && fused;
     moe::PrepArgs pa = prep_args(h, x_bf16, topk_ids, batch, moe::kPrepQuantize | moe::kPrepGroup);
     pa.chained = 1;
     if (early) {
@@ -414,7 +426,7 @@ int run_call(moe_handle h, const void* x_bf16, const int32_t* topk_ids, void* ou
       pa.arrive = h->arrive;
     }
     MOE_CUDA(moe::launch_prep(pa, s));
-    rc = launch_experts(h, out_bf16, batch, topk_ids, s, nullptr, early);
+    rc = launch_experts(h, out_bf16, batch, topk_ids, s, nullptr, early, early && prev_overlaps);
   }
   if (rc != MOE_OK) return rc;
   h->plan_batch = batch;
@@ -526,6 +538,7 @@ int moe_run_combined(moe_handle h, const void* x_bf16, const int32_t* topk_ids,
   c.B = batch;
   c.H = h->g.H;
   MOE_CUDA(moe::launch_combine(c, static_cast<cudaStream_t>(stream)));
+  note_launch(h, static_cast<cudaStream_t>(stream));  // the combine lets nothing start early
   return MOE_OK;
 }
 
@@ -906,7 +919,7 @@ extern "C" int moe_run_noalloc(moe_handle h, const void* x_bf16, const int32_t* 
   pa.pair_kept = nullptr;  // only the combine reads these flags, and this call has no combine
   pa.chained = 1;          // this call's experts kernel follows at once
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  note_launch(h, s);
+  note_launch(h, s, true);
   uint32_t* piece_readers = reinterpret_cast<uint32_t*>(w + offsets[9]);
   uint32_t* piece_sums = reinterpret_cast<uint32_t*>(w + offsets[11]);
   uint32_t* small_counters = reinterpret_cast<uint32_t*>(w + offsets[12]);

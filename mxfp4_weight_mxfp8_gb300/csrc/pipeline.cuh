@@ -77,11 +77,12 @@ struct Layout {
 // ranges are kept equal rather than evening out FC1 + FC2 stages per CTA.
 // Every CTA computes the same table.
 struct Split {
-  int T1, J, G;
-  __host__ __device__ Split(int units, const Geometry& g, int grid) {
+  int T1, J, G, skew;
+  __host__ __device__ Split(int units, const Geometry& g, int grid, int skewed = 0) {
     T1 = units * g.P1 * g.KC1;
     J = units * g.NQ;
     G = grid;
+    skew = skewed;
   }
   // 32-bit products: T1 <= 2M stages and c <= 256 for every supported layer.
   __host__ __device__ int fc2_begin(int c) const {
@@ -94,13 +95,15 @@ struct Split {
                                    static_cast<uint32_t>(J));
     return c < G - 1 ? c : G - 1;
   }
-  // FC1 ranges are skewed toward the low CTAs: CTA c's range starts at
-  // T1 * x * (1 + (1 - x) / 4), x = c / G. CTAs start in block order as the
-  // previous call's CTAs leave (early start), so the ones that start first
-  // get up to a quarter more stages and all finish FC1 closer together.
+  // Even FC1 ranges, or (skewed) ranges that favour the low CTAs: CTA c's
+  // range then starts at T1 * x * (1 + (1 - x) / 4), x = c / G. A call that
+  // starts while the previous one still runs gets its CTAs in block order as
+  // the previous call's leave, so the ones that start first take up to a
+  // quarter more stages and all finish FC1 closer together.
   __host__ __device__ int fc1_begin(int c) const {
     if (c >= G) return T1;
     const uint64_t cu = static_cast<uint64_t>(c), g = static_cast<uint64_t>(G);
+    if (!skew) return static_cast<int>(cu * static_cast<uint64_t>(T1) / g);
     return static_cast<int>(static_cast<uint64_t>(T1) * cu * (5ull * g - cu) / (4ull * g * g));
   }
 };
